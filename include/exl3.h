@@ -1,0 +1,256 @@
+/*
+ * exl3.h -- C ABI of the GB300 (sm_103a) EXL3 trellis library.
+ *
+ * The library computes the EXL3 (exllamav3 trellis) quantized linear layer
+ *
+ *     y = s_out * rout * Had128( Had128((x * s_in) * rin) @ decode(code) )
+ *
+ * (radiance_escha.py, module docstring "THE FORWARD": rin is a pre-scale
+ * applied before its Hadamard, rout a post-scale applied after its own, rin
+ * already carries the weight scale and is applied exactly once, and no bias is
+ * applied), its merged-shard column-slice form (radiance_escha.py,
+ * escha_linear_into and EschaLinearMethod.apply: one call per source tensor,
+ * each writing its own columns of one output buffer), the grouped MoE form
+ * over a flat expert bank (bank.py: w13 = [w1 | w3] per slot, w2, K-sorted
+ * slots) and the int8 embedding gather (vllm-quantpack exl3/embedding.py,
+ * embedding()).
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer is a DEVICE pointer owned by the caller, unless a comment
+ *     says otherwise.  The library never allocates or frees device memory and
+ *     never synchronizes the stream; every call is asynchronous on `stream`
+ *     (a cudaStream_t; NULL is the legacy default stream).
+ *   - bf16 and fp16 values are passed as uint16_t bit patterns.
+ *   - Code tensors are int16 [IC/16][OC/16][16*K], one block of 16*K words per
+ *     16x16 weight tile, the first index along the input channels
+ *     (radiance_escha.py: "_TILE = 16  # code tensor is [IC//16, OC//16, 16*K]";
+ *     K = last dim / 16).  K must be 2, 3 or 4.
+ *   - IC and OC must be multiples of 128: the incoherence transform is blocked
+ *     at 128 channels and a boundary inside a block would change the transform
+ *     (radiance_escha.py, create_weights / process_weights_after_loading).
+ *   - Arguments are validated on the host before any launch.  A bad argument
+ *     returns EXL3_EINVAL (nothing is launched) and exl3_last_error() names the
+ *     sizes involved.  No entry point aborts the process.
+ *   - M == 0 (no rows) is a no-op returning EXL3_OK (radiance_escha.py,
+ *     escha_linear_into: "if M == 0: return").
+ *
+ * Trellis decode reading (the pages give only the tensor shapes): a tile's
+ * 16K words are a stream read most-significant bit first; weight t (0..255,
+ * at tile row t/16 along IC and column t%16 along OC) decodes the 16-bit state
+ * formed by stream bits [(t+1)K-16, (t+1)K), taken modulo the tile's 256K bits
+ * (tail-biting), through the QTIP 3INST hash
+ *     z = 89226354*s + 64248484 (mod 2^32); z' = (z & 0x8FFF8FFF) ^ 0x3B603B60;
+ *     w = fp16(half(z' & 0xFFFF) + half(z' >> 16)).
+ */
+#ifndef EXL3_GB300_H
+#define EXL3_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EXL3_OK = 0,
+    EXL3_EINVAL = 1,        /* bad size, alignment, K or pointer; nothing launched */
+    EXL3_EWORKSPACE = 2,    /* workspace missing or smaller than the query says */
+    EXL3_ECUDA = 3,         /* a CUDA runtime call or launch failed */
+    EXL3_EUNSUPPORTED = 4,  /* valid request this build does not implement */
+    EXL3_EDEVICE = 5        /* a kernel recorded an error (see exl3_workspace_error) */
+} exl3_status;
+
+/* A cudaStream_t, passed opaquely so that this header needs no CUDA headers. */
+typedef void *exl3_stream;
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char *exl3_last_error(void);
+
+/* Library version string. */
+const char *exl3_version(void);
+
+/* ---------------------------------------------------------------- workspace */
+
+/*
+ * Bytes of workspace exl3_linear / exl3_linear_into need for any call with
+ * M <= max_M, IC <= max_IC and OC <= max_OC.  It holds the pre-transformed
+ * activations, the split-K partial slab with its per-column-group arrival
+ * counters (radiance_escha.py, _ensure_scratch: an fp32 partial slab plus an
+ * int32 block counter, allocated once per device outside graph capture), an
+ * error word, and for large M the decoded weight staging of the prefill path.
+ * Returns 0 for invalid sizes.
+ */
+size_t exl3_linear_workspace_bytes(int64_t max_M, int32_t max_IC, int32_t max_OC);
+
+/*
+ * Prepare a freshly allocated workspace (zeroes counters and the error word).
+ * Must run once before the workspace's first use; the kernels leave the
+ * counters at zero again after every call.  ws must be 256-byte aligned.
+ * Two calls that share one workspace must not run concurrently.
+ */
+exl3_status exl3_workspace_init(void *ws, size_t ws_bytes, exl3_stream stream);
+
+/*
+ * Copy the workspace's device error word to *flag_host (host pointer) and
+ * synchronize `stream`.  0 = no kernel recorded an error.  A nonzero value
+ * names the first failure a kernel recorded (for example a bounded wait that
+ * gave up); the word stays set until exl3_workspace_init runs again.
+ */
+exl3_status exl3_workspace_error(const void *ws, size_t ws_bytes, int32_t *flag_host,
+                                 exl3_stream stream);
+
+/* ------------------------------------------------------------------ linear */
+
+/*
+ * One EXL3 projection into a column slice of a caller-owned output
+ * (radiance_escha.py, escha_linear_into):
+ *   x      bf16 [M][IC], row-major, contiguous
+ *   code   int16 [IC/16][OC/16][16*K]
+ *   s_in, rin    fp16 [IC]      pre-scales, applied before the input Had128
+ *   rout, s_out  fp16 [OC]      post-scales, applied after the output Had128
+ *   out    bf16 [M][ldo]; only columns [col0, col0 + OC) are written, every
+ *          other column is left untouched (a merged layer calls this once per
+ *          shard, advancing col0 by that shard's OC)
+ *   ws     workspace of at least exl3_linear_workspace_bytes(M, IC, OC) bytes
+ * Requires ldo >= OC, 0 <= col0, col0 + OC <= ldo, and 16-byte aligned x,
+ * code, and out + col0 rows (ldo and col0 multiples of 8).
+ * The decode/prefill choice by M is made inside this call (radiance_escha.py,
+ * escha_linear_into: the M <= 64 switch lives in the op).
+ */
+exl3_status exl3_linear_into(const uint16_t *x, int64_t M, int32_t IC,
+                             const int16_t *code, int32_t OC, int32_t K,
+                             const uint16_t *s_in, const uint16_t *rin,
+                             const uint16_t *rout, const uint16_t *s_out,
+                             uint16_t *out, int64_t ldo, int64_t col0,
+                             void *ws, size_t ws_bytes, exl3_stream stream);
+
+/*
+ * Steps 2 and 3 of THE FORWARD on activations that are already transformed:
+ *   out[:, col0:col0+OC] = bf16( (Had128(u @ decode(code)) * rout) * s_out )
+ *   u  fp16 [M][IC] = Had128((x * s_in) * rin), as exl3_pretransform writes it.
+ * For callers whose shards share one input transform (the radiance_escha.py
+ * docstring says rin and s_in are shared across merged shards, while its
+ * loader measured them differing per shard): transform once, then call this
+ * per shard.  Same requirements as exl3_linear_into, with u in place of x.
+ */
+exl3_status exl3_gemm_into(const uint16_t *u, int64_t M, int32_t IC,
+                           const int16_t *code, int32_t OC, int32_t K,
+                           const uint16_t *rout, const uint16_t *s_out,
+                           uint16_t *out, int64_t ldo, int64_t col0,
+                           void *ws, size_t ws_bytes, exl3_stream stream);
+
+/* exl3_linear_into with out = y [M][OC] contiguous (ldo = OC, col0 = 0). */
+exl3_status exl3_linear(const uint16_t *x, int64_t M, int32_t IC,
+                        const int16_t *code, int32_t OC, int32_t K,
+                        const uint16_t *s_in, const uint16_t *rin,
+                        const uint16_t *rout, const uint16_t *s_out,
+                        uint16_t *y, void *ws, size_t ws_bytes, exl3_stream stream);
+
+/*
+ * The activation pre-transform on its own (step 1 of THE FORWARD):
+ *   u[m][:] = Had128((x[m][:] * s_in) * rin) per 128-channel block, fp16 out.
+ * x bf16 [M][IC], u fp16 [M][IC].
+ */
+exl3_status exl3_pretransform(const uint16_t *x, int64_t M, int32_t IC,
+                              const uint16_t *s_in, const uint16_t *rin,
+                              uint16_t *u, exl3_stream stream);
+
+/*
+ * Decode a whole code tensor to dense fp16 weights W [IC][OC] (row-major):
+ * W[16a + t/16][16b + t%16] = weight t of tile code[a][b].  The exllamav3
+ * reconstruct kernel plays this role on the pages (vllm-quantpack linear.py,
+ * _cut_tp: "the reconstruct kernel rejects an output width that is not a
+ * multiple of 128"); here it is the decoded-weight parity hook.
+ */
+exl3_status exl3_reconstruct(const int16_t *code, int32_t IC, int32_t OC, int32_t K,
+                             uint16_t *W, exl3_stream stream);
+
+/* Decode every 16-bit trellis state: table[s] = fp16 weight of state s,
+ * table has 65536 entries. */
+exl3_status exl3_codebook_table(uint16_t *table, exl3_stream stream);
+
+/* -------------------------------------------------------------------- MoE */
+
+/*
+ * One layer's EXL3 expert bank (bank.py, Exl3Bank: allocate / views / tables).
+ * All pointers are device pointers; "per slot" arrays are indexed by physical
+ * slot p, and perm maps logical expert e to its slot p = perm[e].
+ *   w13      int16, flat: slot p's w1 code tensor [H/16][I/16][16*k_gu[p]]
+ *            starts at word off_w1[p], its w3 tensor (same shape) at off_w3[p]
+ *   w2       int16, flat: slot p's w2 code tensor [I/16][H/16][16*k_d[p]]
+ *            starts at word off_w2[p]
+ *   off_w1, off_w3, off_w2   int64 [E]  word offsets (multiples of 8)
+ *   perm     int32 [E]  logical expert -> slot
+ *   k_gu, k_d   int32 [E]  per slot: K of w1/w3 and of w2, each 2, 3 or 4
+ *   w13_suh  fp16 [E][2][H]   input pre-scales of w1 (index 0) and w3 (1)
+ *   w13_svh  fp16 [E][2][I]   output post-scales of w1 and w3
+ *   w2_suh   fp16 [E][I]      input pre-scale of w2
+ *   w2_svh   fp16 [E][H]      output post-scale of w2
+ */
+typedef struct exl3_moe_bank {
+    const int16_t *w13;
+    const int16_t *w2;
+    const int64_t *off_w1;
+    const int64_t *off_w3;
+    const int64_t *off_w2;
+    const int32_t *perm;
+    const int32_t *k_gu;
+    const int32_t *k_d;
+    const uint16_t *w13_suh;
+    const uint16_t *w13_svh;
+    const uint16_t *w2_suh;
+    const uint16_t *w2_svh;
+} exl3_moe_bank;
+
+/*
+ * Router helper: per token, the topk largest logits (equal logits: lower
+ * expert id first) and their softmax weights over the selected topk.
+ *   logits fp32 [T][E]; ids int32 [T][topk]; w fp32 [T][topk].
+ * Requires 1 <= topk <= 32 and E <= 1024.
+ */
+exl3_status exl3_moe_topk_softmax(const float *logits, int32_t T, int32_t E, int32_t topk,
+                                  int32_t *ids, float *w, exl3_stream stream);
+
+/* Workspace bytes exl3_moe_grouped needs for T tokens of this geometry. */
+size_t exl3_moe_workspace_bytes(int32_t T, int32_t H, int32_t I, int32_t E, int32_t topk);
+
+/*
+ * Grouped SiLU-gated MoE layer over an EXL3 expert bank.  For token t and its
+ * routes k = 0..topk-1 (expert e = ids[t][k], slot p = bank->perm[e]):
+ *   g = Had(Had(x_t * w13_suh[p][0]) @ W1_p) * w13_svh[p][0]
+ *   u = Had(Had(x_t * w13_suh[p][1]) @ W3_p) * w13_svh[p][1]
+ *   d = Had(Had((silu(g) * u) * w2_suh[p]) @ W2_p) * w2_svh[p]
+ *   y_t = sum over k = 0..topk-1, in that order, of w[t][k] * d
+ *   x bf16 [T][H]; ids int32 [T][topk]; w fp32 [T][topk]; y bf16 [T][H].
+ * Ids outside [0, E) are an error the kernels record in the workspace error
+ * word (their rows contribute nothing).  Requires H, I multiples of 128,
+ * topk <= 32.  ws: exl3_moe_workspace_bytes(T, H, I, E, topk) bytes,
+ * prepared by exl3_workspace_init.
+ */
+exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
+                             int32_t E, int32_t topk, const int32_t *ids, const float *w,
+                             const exl3_moe_bank *bank, uint16_t *y,
+                             void *ws, size_t ws_bytes, exl3_stream stream);
+
+/* ------------------------------------------------------------- embedding */
+
+/*
+ * int8 embedding gather with per-row scale (vllm-quantpack exl3/embedding.py,
+ * embedding(): "dequantized on the GATHERED rows so the table itself stays
+ * int8"):  out[i][:] = bf16(q[ids[i]][:] * scale[ids[i]]), one rounding.
+ *   q int8 [V][H] (row-major), scale fp16 [V], ids int32 [N], out bf16 [N][H].
+ * An id outside [0, V) writes a row of zeros (the masking vLLM's vocab-parallel
+ * embedding applies, same file's module docstring) and, if n_bad (device
+ * int32, may be NULL) is given, is added to *n_bad.  Requires H % 16 == 0 and
+ * 16-byte aligned q and out.
+ */
+exl3_status exl3_embed_int8_gather(const int8_t *q, const uint16_t *scale, int64_t V,
+                                   int32_t H, const int32_t *ids, int64_t N,
+                                   uint16_t *out, int32_t *n_bad, exl3_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXL3_GB300_H */

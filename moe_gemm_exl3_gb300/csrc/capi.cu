@@ -1,0 +1,312 @@
+// capi.cu -- the extern "C" boundary: argument validation, workspace carving,
+// the decode/prefill choice by M, and error reporting.  No entry point
+// allocates device memory or synchronizes the caller's stream (except
+// exl3_workspace_error, which is documented to).
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/exl3.h"
+#include "internal.h"
+
+namespace exl3 {
+
+static thread_local char g_err[512] = "";
+
+exl3_status fail(exl3_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    if (std::getenv("EXL3_TRACE")) std::fprintf(stderr, "[exl3] error: %s\n", g_err);
+    return st;
+}
+
+exl3_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(EXL3_ECUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+void trace(const char *fmt, ...) {
+    if (!std::getenv("EXL3_TRACE")) return;
+    va_list ap;
+    va_start(ap, fmt);
+    std::fprintf(stderr, "[exl3] ");
+    std::vfprintf(stderr, fmt, ap);
+    std::fprintf(stderr, "\n");
+    va_end(ap);
+}
+
+const DeviceInfo &device_info() {
+    static DeviceInfo info[64];
+    static bool done[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+        cudaDeviceGetAttribute(&info[dev].sm_count, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&info[dev].max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (info[dev].sm_count <= 0) info[dev].sm_count = 1;
+        done[dev] = true;
+    }
+    return info[dev];
+}
+
+static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Fixed part of every workspace: error word, then the arrival counters.
+constexpr size_t kHeaderBytes = 256;
+constexpr size_t kCounterCount = 65536;
+constexpr size_t kFixedBytes = kHeaderBytes + kCounterCount * sizeof(int32_t);
+
+size_t fixed_workspace_bytes() { return kFixedBytes; }
+int32_t *workspace_err(void *base) { return reinterpret_cast<int32_t *>(base); }
+int32_t *workspace_counters(void *base) {
+    return reinterpret_cast<int32_t *>(static_cast<char *>(base) + kHeaderBytes);
+}
+
+// Rows above which the prefill (tensor-core) path is taken.
+int64_t prefill_threshold() {
+    static int64_t t = -1;
+    if (t < 0) {
+        const char *f = std::getenv("EXL3_FORCE_MODE");
+        t = kDecodeMaxRows;
+        if (f && !std::strcmp(f, "decode")) t = INT64_MAX;
+        if (f && !std::strcmp(f, "prefill")) t = 0;
+    }
+    return t;
+}
+
+size_t linear_workspace_layout(int64_t max_M, int32_t max_IC, int32_t max_OC, LinearWorkspace *ws,
+                               void *base) {
+    if (max_M < 0 || max_IC <= 0 || max_OC <= 0) return 0;
+    const int64_t NG = max_OC / 128;
+    const int64_t dec_rows = max_M < kDecodeMaxRows ? max_M : kDecodeMaxRows;
+    const int64_t nb = (dec_rows + 7) / 8;
+    size_t off = kFixedBytes;
+    const size_t u_elems = (size_t)max_M * max_IC;
+    const size_t u_off = off;
+    off = align256(off + u_elems * sizeof(uint16_t));
+    const size_t part_elems = (size_t)(kDecodeMaxCtas + NG) * (8 * nb * 4 * 32);
+    const size_t part_off = off;
+    off = align256(off + part_elems * sizeof(float));
+    size_t wt_elems = 0, wt_off = off;
+    if (max_M > prefill_threshold() && prefill_supported()) {
+        wt_elems = (size_t)max_OC * max_IC;
+        off = align256(off + wt_elems * sizeof(uint16_t));
+    }
+    if (ws) {
+        char *b = static_cast<char *>(base);
+        ws->err = workspace_err(base);
+        ws->counters = workspace_counters(base);
+        ws->counters_n = kCounterCount;
+        ws->u = reinterpret_cast<uint16_t *>(b + u_off);
+        ws->u_elems = u_elems;
+        ws->partials = reinterpret_cast<float *>(b + part_off);
+        ws->partial_elems = part_elems;
+        ws->wt = wt_elems ? reinterpret_cast<uint16_t *>(b + wt_off) : nullptr;
+        ws->wt_elems = wt_elems;
+    }
+    return off;
+}
+
+}  // namespace exl3
+
+using namespace exl3;
+
+static inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+extern "C" {
+
+const char *exl3_last_error(void) { return g_err; }
+
+const char *exl3_version(void) { return "exl3-gb300 0.1.0 (sm_103a)"; }
+
+size_t exl3_linear_workspace_bytes(int64_t max_M, int32_t max_IC, int32_t max_OC) {
+    if (max_M < 0 || max_IC <= 0 || max_OC <= 0 || max_IC % 128 || max_OC % 128 ||
+        (int64_t)max_OC / 128 > (int64_t)kCounterCount)
+        return 0;
+    return linear_workspace_layout(max_M, max_IC, max_OC, nullptr, nullptr);
+}
+
+exl3_status exl3_workspace_init(void *ws, size_t ws_bytes, exl3_stream stream) {
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u))
+        return fail(EXL3_EINVAL, "workspace_init: workspace pointer %p is null or not 256-byte aligned", ws);
+    if (ws_bytes < kFixedBytes)
+        return fail(EXL3_EWORKSPACE, "workspace_init: %zu bytes < the %zu-byte minimum", ws_bytes, kFixedBytes);
+    cudaError_t e = cudaMemsetAsync(ws, 0, kFixedBytes, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "workspace_init");
+    return EXL3_OK;
+}
+
+exl3_status exl3_workspace_error(const void *ws, size_t ws_bytes, int32_t *flag_host, exl3_stream stream) {
+    if (!ws || !flag_host || ws_bytes < kFixedBytes)
+        return fail(EXL3_EINVAL, "workspace_error: null pointer or workspace of %zu bytes", ws_bytes);
+    cudaError_t e = cudaMemcpyAsync(flag_host, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "workspace_error");
+    return EXL3_OK;
+}
+
+static exl3_status check_linear_args(const char *fn, const uint16_t *x, int64_t M, int32_t IC,
+                                     const int16_t *code, int32_t OC, int32_t K,
+                                     const uint16_t *s_in, const uint16_t *rin,
+                                     const uint16_t *rout, const uint16_t *s_out) {
+    if (M < 0) return fail(EXL3_EINVAL, "%s: M = %lld is negative", fn, (long long)M);
+    if (K < 2 || K > 4)
+        return fail(EXL3_EUNSUPPORTED, "%s: K = %d bits per weight; this build decodes K in {2, 3, 4}", fn, K);
+    if (IC <= 0 || OC <= 0 || IC % 128 || OC % 128)
+        return fail(EXL3_EINVAL, "%s: IC = %d and OC = %d must be positive multiples of 128 "
+                    "(the Hadamard transform is blocked at 128)", fn, IC, OC);
+    if ((int64_t)OC / 128 > (int64_t)kCounterCount)
+        return fail(EXL3_EINVAL, "%s: OC = %d exceeds %lld column groups", fn, OC, (long long)kCounterCount);
+    if (!code || !s_in || !rin || !rout || !s_out || (M > 0 && !x))
+        return fail(EXL3_EINVAL, "%s: null input pointer", fn);
+    if (!aligned16(code) || (M > 0 && !aligned16(x)))
+        return fail(EXL3_EINVAL, "%s: x (%p) and code (%p) must be 16-byte aligned", fn, x, code);
+    if (((uintptr_t)s_in | (uintptr_t)rin | (uintptr_t)rout | (uintptr_t)s_out) & 7u)
+        return fail(EXL3_EINVAL, "%s: scale vectors must be 8-byte aligned", fn);
+    return EXL3_OK;
+}
+
+exl3_status exl3_pretransform(const uint16_t *x, int64_t M, int32_t IC, const uint16_t *s_in,
+                              const uint16_t *rin, uint16_t *u, exl3_stream stream) {
+    if (M < 0 || IC <= 0 || IC % 128)
+        return fail(EXL3_EINVAL, "pretransform: M = %lld, IC = %d (IC must be a positive multiple of 128)",
+                    (long long)M, IC);
+    if (M == 0) return EXL3_OK;
+    if (!x || !s_in || !rin || !u) return fail(EXL3_EINVAL, "pretransform: null pointer");
+    if (((uintptr_t)x | (uintptr_t)u | (uintptr_t)s_in | (uintptr_t)rin) & 7u)
+        return fail(EXL3_EINVAL, "pretransform: pointers must be 8-byte aligned");
+    cudaError_t e = launch_pretransform(x, M, IC, s_in, rin, u, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "pretransform");
+    return EXL3_OK;
+}
+
+// Trellis GEMM + epilogue on pre-transformed activations u (fp16 [M][IC]).
+static exl3_status gemm_into_impl(const char *fn, const uint16_t *u, int64_t M, int32_t IC, const int16_t *code,
+                                  int32_t OC, int32_t K, const uint16_t *rout, const uint16_t *s_out,
+                                  uint16_t *dst, int64_t ldo, const LinearWorkspace &ws, cudaStream_t s) {
+    cudaError_t e;
+    if (M > prefill_threshold() && prefill_supported()) {
+        bool launched = false;
+        e = launch_reconstruct(code, IC, OC, K, ws.wt, /*transposed=*/true, s);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+        e = launch_prefill(u, ws.wt, M, IC, OC, rout, s_out, dst, ldo, ws.err, s, &launched);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+        trace("%s M=%lld IC=%d OC=%d K=%d mode=prefill", fn, (long long)M, IC, OC, K);
+        if (launched) return EXL3_OK;
+    }
+    // decode mode: passes of up to kDecodeMaxRows rows
+    for (int64_t r0 = 0; r0 < M; r0 += kDecodeMaxRows) {
+        DecodeGemmArgs a;
+        a.u = u + r0 * IC;
+        a.code = code;
+        a.IC = IC;
+        a.OC = OC;
+        a.K = K;
+        a.M = (int)((M - r0) < kDecodeMaxRows ? (M - r0) : kDecodeMaxRows);
+        a.rout = rout;
+        a.s_out = s_out;
+        a.out = dst + r0 * ldo;
+        a.ldo = ldo;
+        a.partials = ws.partials;
+        a.counters = ws.counters;
+        e = launch_decode_gemm(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+    }
+    trace("%s M=%lld IC=%d OC=%d K=%d mode=decode", fn, (long long)M, IC, OC, K);
+    return EXL3_OK;
+}
+
+static exl3_status check_out_ws(const char *fn, int64_t M, int32_t IC, int32_t OC, const uint16_t *out,
+                                int64_t ldo, int64_t col0, void *wsp, size_t ws_bytes) {
+    if (ldo < OC || col0 < 0 || col0 + OC > ldo)
+        return fail(EXL3_EINVAL, "%s: column slice [%lld, %lld) does not fit ldo = %lld", fn,
+                    (long long)col0, (long long)col0 + OC, (long long)ldo);
+    if (M == 0) return EXL3_OK;
+    if (!out) return fail(EXL3_EINVAL, "%s: null output", fn);
+    if ((ldo % 8) || (col0 % 8) || !aligned16(out))
+        return fail(EXL3_EINVAL, "%s: out (%p), ldo = %lld and col0 = %lld must give 16-byte "
+                    "aligned rows (ldo, col0 multiples of 8)", fn, out, (long long)ldo, (long long)col0);
+    const size_t need = exl3_linear_workspace_bytes(M, IC, OC);
+    if (!wsp || (reinterpret_cast<uintptr_t>(wsp) & 255u) || ws_bytes < need)
+        return fail(EXL3_EWORKSPACE, "%s: workspace %p of %zu bytes; this call needs %zu bytes, "
+                    "256-byte aligned (exl3_linear_workspace_bytes(%lld, %d, %d))", fn, wsp, ws_bytes, need,
+                    (long long)M, IC, OC);
+    return EXL3_OK;
+}
+
+exl3_status exl3_linear_into(const uint16_t *x, int64_t M, int32_t IC, const int16_t *code, int32_t OC,
+                             int32_t K, const uint16_t *s_in, const uint16_t *rin, const uint16_t *rout,
+                             const uint16_t *s_out, uint16_t *out, int64_t ldo, int64_t col0, void *wsp,
+                             size_t ws_bytes, exl3_stream stream) {
+    exl3_status st = check_linear_args("linear_into", x, M, IC, code, OC, K, s_in, rin, rout, s_out);
+    if (st == EXL3_OK) st = check_out_ws("linear_into", M, IC, OC, out, ldo, col0, wsp, ws_bytes);
+    if (st != EXL3_OK || M == 0) return st;
+    LinearWorkspace ws;
+    linear_workspace_layout(M, IC, OC, &ws, wsp);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_pretransform(x, M, IC, s_in, rin, ws.u, s);
+    if (e != cudaSuccess) return cuda_fail(e, "linear_into: pretransform");
+    return gemm_into_impl("linear_into", ws.u, M, IC, code, OC, K, rout, s_out, out + col0, ldo, ws, s);
+}
+
+exl3_status exl3_gemm_into(const uint16_t *u, int64_t M, int32_t IC, const int16_t *code, int32_t OC, int32_t K,
+                           const uint16_t *rout, const uint16_t *s_out, uint16_t *out, int64_t ldo, int64_t col0,
+                           void *wsp, size_t ws_bytes, exl3_stream stream) {
+    exl3_status st = check_linear_args("gemm_into", u, M, IC, code, OC, K, rout, rout, rout, s_out);
+    if (st == EXL3_OK) st = check_out_ws("gemm_into", M, IC, OC, out, ldo, col0, wsp, ws_bytes);
+    if (st != EXL3_OK || M == 0) return st;
+    LinearWorkspace ws;
+    linear_workspace_layout(M, IC, OC, &ws, wsp);
+    return gemm_into_impl("gemm_into", u, M, IC, code, OC, K, rout, s_out, out + col0, ldo, ws,
+                          (cudaStream_t)stream);
+}
+
+exl3_status exl3_linear(const uint16_t *x, int64_t M, int32_t IC, const int16_t *code, int32_t OC, int32_t K,
+                        const uint16_t *s_in, const uint16_t *rin, const uint16_t *rout, const uint16_t *s_out,
+                        uint16_t *y, void *ws, size_t ws_bytes, exl3_stream stream) {
+    return exl3_linear_into(x, M, IC, code, OC, K, s_in, rin, rout, s_out, y, OC, 0, ws, ws_bytes, stream);
+}
+
+exl3_status exl3_reconstruct(const int16_t *code, int32_t IC, int32_t OC, int32_t K, uint16_t *W,
+                             exl3_stream stream) {
+    if (K < 2 || K > 4) return fail(EXL3_EUNSUPPORTED, "reconstruct: K = %d; this build decodes K in {2, 3, 4}", K);
+    if (IC <= 0 || OC <= 0 || IC % 16 || OC % 16)
+        return fail(EXL3_EINVAL, "reconstruct: IC = %d, OC = %d must be positive multiples of 16", IC, OC);
+    if (!code || !W || !aligned16(code) || !aligned16(W) || (OC % 128 && OC % 8))
+        return fail(EXL3_EINVAL, "reconstruct: code and W must be non-null and 16-byte aligned");
+    cudaError_t e = launch_reconstruct(code, IC, OC, K, W, false, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reconstruct");
+    return EXL3_OK;
+}
+
+exl3_status exl3_codebook_table(uint16_t *table, exl3_stream stream) {
+    if (!table) return fail(EXL3_EINVAL, "codebook_table: null table");
+    cudaError_t e = launch_codebook_table(table, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "codebook_table");
+    return EXL3_OK;
+}
+
+exl3_status exl3_embed_int8_gather(const int8_t *q, const uint16_t *scale, int64_t V, int32_t H,
+                                   const int32_t *ids, int64_t N, uint16_t *out, int32_t *n_bad,
+                                   exl3_stream stream) {
+    if (V <= 0 || H <= 0 || H % 16 || N < 0)
+        return fail(EXL3_EINVAL, "embed_int8_gather: V = %lld, H = %d (multiple of 16), N = %lld",
+                    (long long)V, H, (long long)N);
+    if (N == 0) return EXL3_OK;
+    if (!q || !scale || !ids || !out) return fail(EXL3_EINVAL, "embed_int8_gather: null pointer");
+    if (!aligned16(q) || !aligned16(out))
+        return fail(EXL3_EINVAL, "embed_int8_gather: q (%p) and out (%p) must be 16-byte aligned", q, out);
+    cudaError_t e = launch_gather(q, scale, V, H, ids, N, out, n_bad, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "embed_int8_gather");
+    return EXL3_OK;
+}
+
+}  // extern "C"

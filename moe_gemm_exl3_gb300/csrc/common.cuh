@@ -1,0 +1,156 @@
+// common.cuh -- device helpers shared by the EXL3 kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/exl3.h"
+
+namespace exl3 {
+
+constexpr int kHad = 128;        // incoherence transform block
+constexpr int kTile = 16;        // weight tile edge
+constexpr unsigned kFull = 0xFFFFFFFFu;
+// 1/sqrt(128): the orthonormal Had128 scale, applied in fp32.
+constexpr float kHadNorm = 0.08838834764831845f;
+
+// Device error codes recorded in the workspace error word (first one wins).
+enum DeviceError : int32_t {
+    kErrNone = 0,
+    kErrWaitTimeout = 1,     // a bounded mbarrier wait gave up
+    kErrBadExpertId = 2,     // a MoE route named an expert outside [0, E)
+    kErrRouteOverflow = 3,   // more routed rows than the workspace was sized for
+};
+
+__device__ __forceinline__ void record_error(int32_t *err, int32_t code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// ---------------------------------------------------------------- formats
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) {
+    return __uint_as_float(b16 << 16);
+}
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float v) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t h) {
+    return __half2float(__ushort_as_half(h));
+}
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float v) {
+    return __half_as_ushort(__float2half_rn(v));
+}
+
+// ---------------------------------------------------------------- trellis
+// 3INST hash of a 16-bit trellis state: returns the two fp16 halves z' whose
+// sum is the decoded weight (low half in bits 0..15, high half in 16..31).
+__device__ __forceinline__ uint32_t trellis_hash(uint32_t state) {
+    uint32_t z = state * 89226354u + 64248484u;
+    return (z & 0x8FFF8FFFu) ^ 0x3B603B60u;
+}
+
+// The decoded fp16 weight of one hashed state: lo + hi, rounded once.
+__device__ __forceinline__ __half trellis_weight(uint32_t zp) {
+    __half2 h = *reinterpret_cast<const __half2 *>(&zp);
+    return __hadd(__low2half(h), __high2half(h));
+}
+
+// Pack the decoded weights of two hashed states into one half2 (a, b).
+__device__ __forceinline__ uint32_t trellis_weight_pair(uint32_t za, uint32_t zb) {
+    uint32_t lo = __byte_perm(za, zb, 0x5410);   // (lo_a, lo_b)
+    uint32_t hi = __byte_perm(za, zb, 0x7632);   // (hi_a, hi_b)
+    __half2 s = __hadd2(*reinterpret_cast<__half2 *>(&lo), *reinterpret_cast<__half2 *>(&hi));
+    return *reinterpret_cast<uint32_t *>(&s);
+}
+
+// A quarter of a tile: 4 tile rows x 16 columns = 64 weights, 64K stream bits
+// held as 2K little-endian uint32 words (int16 word 2j in bits 0..15 of word j).
+// `prev` is the uint32 word preceding the quarter in the circular tile stream;
+// only its high int16 (the stream word just before the quarter) is used.
+//
+// Builds E[0..2K], E[j] = stream bits [32j - 16, 32j + 16) relative to the
+// quarter start, as big-endian 32-bit values (E[0] starts with the preceding
+// 16 bits).  The state of quarter weight i (0..63) is then the 16 bits of E
+// starting at bit (i+1)K.
+template <int K>
+struct QuarterStream {
+    uint32_t E[2 * K + 1];
+
+    __device__ __forceinline__ void build(const uint32_t (&w)[2 * K], uint32_t prev) {
+        E[0] = __byte_perm(w[0], prev, 0x7610);
+#pragma unroll
+        for (int j = 1; j < 2 * K; j++) E[j] = __byte_perm(w[j], w[j - 1], 0x7610);
+        E[2 * K] = w[2 * K - 1] & 0xFFFF0000u;
+    }
+
+    // 16-bit trellis state of quarter weight i (compile-time i after unrolling).
+    __device__ __forceinline__ uint32_t state(int i) const {
+        const int p = (i + 1) * K;
+        const int j = p >> 5, o = p & 31;
+        if (o <= 16) return (E[j] >> (16 - o)) & 0xFFFFu;
+        return __funnelshift_r(E[j + 1], E[j], 48 - o) & 0xFFFFu;
+    }
+};
+
+// Word preceding a quarter inside its tile (tail-biting): lanes are laid out
+// as 4 consecutive quarters q = lane % 4 of one tile; quarter 0 takes the last
+// word of quarter 3.
+__device__ __forceinline__ uint32_t quarter_prev_word(uint32_t last_word, int lane) {
+    const int q = lane & 3;
+    const int src = q == 0 ? lane + 3 : lane - 1;
+    return __shfl_sync(kFull, last_word, src);
+}
+
+// Load one quarter (2K uint32 words) with loads as wide as its alignment allows.
+template <int K>
+__device__ __forceinline__ void load_quarter(uint32_t (&w)[2 * K], const uint32_t *p) {
+    if constexpr (K == 2) {
+        uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (K == 4) {
+        uint4 v0 = __ldg(reinterpret_cast<const uint4 *>(p));
+        uint4 v1 = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
+        w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+        w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < K; j++) {
+            uint2 v = __ldg(reinterpret_cast<const uint2 *>(p) + j);
+            w[2 * j] = v.x; w[2 * j + 1] = v.y;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- Hadamard
+// In-warp unnormalised Had128 of 128 values held 4 per lane as v[i] = value
+// (4*lane + i): two register stages (index bits 0, 1) then five shuffle stages
+// (index bits 2..6 = lane bits 0..4).  Sylvester order: H[i][j] = (-1)^popc(i&j).
+__device__ __forceinline__ void warp_fwht128(float (&v)[4], int lane) {
+    float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+    v[0] = a0 + a2; v[1] = a1 + a3; v[2] = a0 - a2; v[3] = a1 - a3;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = lane & m;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float p = __shfl_xor_sync(kFull, v[i], m);
+            v[i] = upper ? p - v[i] : v[i] + p;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- MMA
+// D += A * B, m16n8k16, fp16 operands, fp32 accumulate (legacy warp-level MMA).
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t dup_half_lo(uint32_t h2) { return __byte_perm(h2, 0, 0x1010); }
+__device__ __forceinline__ uint32_t dup_half_hi(uint32_t h2) { return __byte_perm(h2, 0, 0x3232); }
+
+}  // namespace exl3

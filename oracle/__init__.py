@@ -65,6 +65,9 @@ def lib():
             L.exl3o_reconstruct_cols.argtypes = [_P(i16)] + [ctypes.c_int] * 5 + [_P(u16)]
             L.exl3o_reconstruct_cols.restype = ctypes.c_int
             L.exl3o_hadamard128.argtypes = [_P(f64)]
+            L.exl3o_pretransform_f64.argtypes = [_P(u16), ctypes.c_long, ctypes.c_int, _P(u16),
+                                                 _P(u16), _P(f64)]
+            L.exl3o_pretransform_f64.restype = ctypes.c_int
             L.exl3o_linear_f64.argtypes = [_P(u16), ctypes.c_long, ctypes.c_int, _P(i16),
                                            ctypes.c_int, ctypes.c_int, _P(u16), _P(u16), _P(u16),
                                            _P(u16), ctypes.c_int, ctypes.c_int, _P(f64)]
@@ -177,6 +180,18 @@ def hadamard128() -> np.ndarray:
 
 
 # ---------------------------------------------------------------- linear
+def pretransform_f64(x, s_in, rin) -> np.ndarray:
+    """fp64 u[M][IC] = Had128((x * s_in) * rin) blockwise."""
+    x = _u16(x)
+    M, IC = x.shape
+    u = np.empty((M, IC), np.float64)
+    _check(lib().exl3o_pretransform_f64(_ptr(x, ctypes.c_uint16), M, IC,
+                                        _ptr(_u16(s_in), ctypes.c_uint16),
+                                        _ptr(_u16(rin), ctypes.c_uint16),
+                                        _ptr(u, ctypes.c_double)), "pretransform")
+    return u
+
+
 def linear_f64(x, code, K, s_in, rin, rout, s_out, blk0=0, nblk=None) -> np.ndarray:
     """fp64 y[M][nblk*128] of output blocks [blk0, blk0+nblk) (unrounded)."""
     x = _u16(x)

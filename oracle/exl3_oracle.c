@@ -250,6 +250,27 @@ static void had_blocks(const double *H, const double *v, double *y, long n)
 /* EXL3 linear                                                               */
 /* ------------------------------------------------------------------------ */
 
+/* [escha] THE FORWARD, first factor: u = Had128((x * s_in) * rin) per
+ * 128-channel block, fp64.  x bf16 [M][IC]; u [M][IC]. */
+int exl3o_pretransform_f64(const uint16_t *x, long M, int IC, const uint16_t *s_in,
+                           const uint16_t *rin, double *u)
+{
+    if (IC % 128 || M < 0)
+        return EXL3O_EINVAL;
+    double *H = malloc(sizeof(double) * 128 * 128);
+    double *xs = malloc(sizeof(double) * IC);
+    exl3o_hadamard128(H);
+    for (long m = 0; m < M; m++) {
+        for (int c = 0; c < IC; c++)
+            xs[c] = (exl3o_bf16_to_f64(x[m * IC + c]) * exl3o_f16_to_f64(s_in[c]))
+                    * exl3o_f16_to_f64(rin[c]);
+        had_blocks(H, xs, u + m * IC, IC);
+    }
+    free(H);
+    free(xs);
+    return EXL3O_OK;
+}
+
 /*
  * [escha] THE FORWARD, restated step by step:
  *   u = Had128((x * s_in) * rin)          rin is a pre-scale, before its Had

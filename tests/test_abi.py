@@ -1,0 +1,47 @@
+"""The C-ABI library loads and exports every symbol include/exl3.h declares
+(no compute call: this runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import moe_gemm_exl3_gb300 as m
+from moe_gemm_exl3_gb300 import build as b
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "exl3.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(exl3_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    b.build()
+    lib = ctypes.CDLL(m.LIB_PATH)
+    names = declared_symbols()
+    assert len(names) >= 14
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert sorted(m.EXPORTS) == names
+
+
+def test_host_side_queries_without_gpu():
+    b.build()
+    L = m.lib()
+    assert m.exl3_version().startswith("exl3-gb300")
+    # workspace sizes are pure host arithmetic
+    assert m.exl3_linear_workspace_bytes(8, 5120, 17408) > 0
+    assert m.exl3_linear_workspace_bytes(8, 5000, 17408) == 0      # IC not a multiple of 128
+    assert m.exl3_linear_workspace_bytes(8, 5120, 17400) == 0
+    assert m.exl3_linear_workspace_bytes(-1, 5120, 17408) == 0
+    # invalid sizes are rejected on the host before any CUDA call
+    st = L.exl3_linear_into(None, 4, 500, None, 512, 2, None, None, None, None, None, 512, 0,
+                            None, 0, None)
+    assert st == m.EXL3_EINVAL
+    assert b"multiples of 128" in L.exl3_last_error()
+    st = L.exl3_linear_into(None, 4, 512, None, 512, 5, None, None, None, None, None, 512, 0,
+                            None, 0, None)
+    assert st == m.EXL3_EUNSUPPORTED
+    st = L.exl3_embed_int8_gather(None, None, 10, 24, None, 3, None, None, None)
+    assert st == m.EXL3_EINVAL

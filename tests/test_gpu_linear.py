@@ -1,0 +1,196 @@
+"""GPU parity of the EXL3 linear path against the CPU oracle, through the C ABI.
+
+Decoded weights and the codebook must match the oracle bit for bit; outputs
+must satisfy max|y - y_ref| <= 2e-2 * rms(y_ref) per row (fp32 accumulation).
+Columns outside a shard's slice must keep their NaN poison (the vLLM PR #190
+trellis-MoE validation used NaN-poisoned scratch the same way).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+from tests._util import as_f64, assert_rows_close, bits, dev
+
+pytestmark = pytest.mark.gpu
+
+m = pytest.importorskip("moe_gemm_exl3_gb300")
+NAN_BF16 = 0x7FC1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_gemm_exl3_gb300 import build
+    build.build()
+    m.lib()
+
+
+def shard_dev(sh):
+    return (dev(sh.code, torch.int16), *(dev(v, torch.float16) for v in (sh.s_in, sh.rin, sh.rout, sh.s_out)))
+
+
+def test_codebook_table_exhaustive():
+    got = bits(m.exl3_codebook_table())
+    assert np.array_equal(got, oracle.codebook_table())
+
+
+@pytest.mark.parametrize("K", (2, 3, 4))
+def test_reconstruct_bit_exact_small(K):
+    g = syn.rng(40 + K)
+    code = syn.uniform_code(g, (32, 48, 16 * K))     # IC = 512, OC = 768
+    W = m.exl3_reconstruct(dev(code, torch.int16), K)
+    assert np.array_equal(bits(W), oracle.reconstruct(code, K))
+
+
+@pytest.mark.parametrize("K", (2, 3, 4))
+def test_reconstruct_single_bit_tiles(K):
+    # one tile per stream bit position class: pins the bit order, window and tail-biting on GPU
+    n = 256 * K
+    pos = list(range(0, n, max(1, n // 61))) + [0, 15, 16, n - 1]
+    code = np.zeros((1, len(pos), 16 * K), np.uint16)
+    for i, p in enumerate(pos):
+        code[0, i, p // 16] = 1 << (15 - p % 16)
+    code = code.view(np.int16)
+    pad = (-len(pos)) % 8                             # OC multiple of 128 is not needed here
+    code = np.concatenate([code, np.zeros((1, pad, 16 * K), np.int16)], axis=1)
+    W = m.exl3_reconstruct(dev(code, torch.int16), K)
+    assert np.array_equal(bits(W), oracle.reconstruct(code, K))
+
+
+@pytest.mark.parametrize("K", (2, 3))
+def test_reconstruct_bit_exact_full_gate_up_shards(K):
+    # every tile of a 5120 x 17408 shard
+    g = syn.rng(50 + K)
+    code = syn.uniform_code(g, (320, 1088, 16 * K))
+    W = bits(m.exl3_reconstruct(dev(code, torch.int16), K))
+    for b0 in range(0, 17408, 4352):                   # oracle in column chunks (memory)
+        assert np.array_equal(W[:, b0:b0 + 4352], oracle.reconstruct(code, K, b0, 4352))
+
+
+def test_pretransform_matches_oracle():
+    x, sh = syn.linear_case(60, 7, 1024, 128, 2, outlier_frac=0.01)
+    u = m.exl3_pretransform(dev(x, torch.bfloat16), dev(sh.s_in, torch.float16), dev(sh.rin, torch.float16))
+    ref = oracle.pretransform_f64(x, sh.s_in, sh.rin)
+    got = as_f64(u)
+    # fp16 output: within half an fp16 ulp of the fp64 value plus fp32 rounding
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -10 + 1e-6)
+
+
+def run_linear(x, sh, ws=None):
+    M = x.shape[0]
+    if ws is None:
+        ws = m.workspace(m.exl3_linear_workspace_bytes(M, sh.IC, sh.OC))
+    y = m.exl3_linear(dev(x, torch.bfloat16), *shard_dev(sh)[:1], sh.K, *shard_dev(sh)[1:], ws)
+    torch.cuda.synchronize()
+    return y
+
+
+@pytest.mark.parametrize("K", (2, 3, 4))
+@pytest.mark.parametrize("M", (1, 3, 8, 13, 32, 33, 70))
+def test_linear_parity_small(K, M):
+    x, sh = syn.linear_case(100 + M + K, M, 512, 640, K)
+    y = run_linear(x, sh)
+    ref = oracle.linear_f64(x, sh.code, K, sh.s_in, sh.rin, sh.rout, sh.s_out)
+    assert_rows_close(as_f64(y), ref)
+
+
+def test_single_linear_workload():
+    x, sh = syn.single_linear(0)
+    y = run_linear(x, sh)
+    ref = oracle.linear_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out)
+    assert_rows_close(as_f64(y), ref)
+
+
+@pytest.mark.parametrize("M", (1, 8, 64))
+def test_gate_up_full_size_sampled_blocks(M):
+    # the decode-shaped merged gate (K=2) / up (K=3) layer into one out[M, 34816];
+    # the oracle computes three 128-column blocks of each shard
+    x, shards = syn.gate_up(1, M=M)
+    OC = 17408
+    out = torch.full((M, 2 * OC), 0, dtype=torch.int16, device="cuda")
+    out.fill_(NAN_BF16)
+    out = out.view(torch.bfloat16)
+    ws = m.workspace(m.exl3_linear_workspace_bytes(M, 5120, OC))
+    xd = dev(x, torch.bfloat16)
+    for i, sh in enumerate(shards):
+        c, *sc = shard_dev(sh)
+        m.exl3_linear_into(xd, c, sh.K, *sc, out, i * OC, ws)
+    torch.cuda.synchronize()
+    got = as_f64(out)
+    assert np.all(np.isfinite(got)), "a column of the output was left unwritten"
+    for i, sh in enumerate(shards):
+        for blk in (0, 77, OC // 128 - 1):
+            ref = oracle.linear_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=blk, nblk=1)
+            assert_rows_close(got[:, i * OC + blk * 128:i * OC + (blk + 1) * 128], ref)
+
+
+def test_column_slice_isolation_and_merged_layer():
+    x, shards = syn.gate_up(7, M=5, IC=512, OC=384, Ks=(2, 3))
+    ldo = 2 * 384 + 64
+    out = torch.full((5, ldo), NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    ws = m.workspace(m.exl3_linear_workspace_bytes(5, 512, 384))
+    xd = dev(x, torch.bfloat16)
+    col = 32
+    for sh in shards:
+        c, *sc = shard_dev(sh)
+        m.exl3_linear_into(xd, c, sh.K, *sc, out, col, ws)
+        col += 384
+    torch.cuda.synchronize()
+    b = bits(out)
+    assert np.all(b[:, :32] == NAN_BF16) and np.all(b[:, col:] == NAN_BF16)
+    col = 32
+    for sh in shards:
+        ref = oracle.linear_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out)
+        assert_rows_close(as_f64(out)[:, col:col + 384], ref)
+        col += 384
+
+
+def test_deterministic_and_batch_invariant():
+    x, sh = syn.linear_case(8, 8, 1024, 1024, 3)
+    y8a = bits(run_linear(x, sh))
+    y8b = bits(run_linear(x, sh))
+    assert np.array_equal(y8a, y8b)
+    for r in (0, 5):
+        y1 = bits(run_linear(x[r:r + 1], sh))
+        assert np.array_equal(y1[0], y8a[r])
+
+
+def test_graph_replay_equals_eager():
+    x, sh = syn.linear_case(9, 4, 1024, 768, 2)
+    ws = m.workspace(m.exl3_linear_workspace_bytes(4, 1024, 768))
+    xd = dev(x, torch.bfloat16)
+    c, *sc = shard_dev(sh)
+    eager = bits(m.exl3_linear(xd, c, 2, *sc, ws))
+    out = torch.empty((4, 768), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            m.exl3_linear(xd, c, 2, *sc, ws, out=out)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(out), eager)
+
+
+def test_errors_are_reported_not_launched():
+    x, sh = syn.linear_case(10, 2, 256, 256, 2)
+    c, *sc = shard_dev(sh)
+    xd = dev(x, torch.bfloat16)
+    small = m.workspace(1 << 20)
+    with pytest.raises(m.Exl3Error) as e:
+        m.exl3_linear(xd, c, 2, *sc, small)
+    assert e.value.status == m.EXL3_EWORKSPACE
+    ws = m.workspace(m.exl3_linear_workspace_bytes(2, 256, 256))
+    out = torch.empty((2, 300), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(m.Exl3Error) as e:
+        m.exl3_linear_into(xd, c, 2, *sc, out, 100, ws)       # slice past ldo
+    assert e.value.status == m.EXL3_EINVAL
+    with pytest.raises(ValueError):
+        m.exl3_linear(xd, c, 3, *sc, ws)                       # K disagrees with the code's shape
+    # M == 0 is a no-op
+    m.exl3_linear(xd[:0], c, 2, *sc, ws)
+    assert m.exl3_workspace_error(ws) == 0

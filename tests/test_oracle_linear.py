@@ -138,3 +138,10 @@ def test_m_zero_is_a_no_op():
     out = np.full((0, 128), 0x7FC1, np.uint16)
     oracle.linear_into(out, np.zeros((0, 128), np.uint16), shard.code, 2, shard.s_in,
                        shard.rin, shard.rout, shard.s_out, 0)
+
+
+def test_pretransform_matches_dense_hadamard():
+    x, shard = syn.linear_case(18, 3, 384, 128, 2)
+    u = oracle.pretransform_f64(x, shard.s_in, shard.rin)
+    ref = (bf16(x) * f16(shard.s_in) * f16(shard.rin)) @ hblk(384)
+    assert np.max(np.abs(u - ref)) <= 1e-12 * np.max(np.abs(ref))
