@@ -140,6 +140,34 @@ exl3_status exl3_gemm_into(const uint16_t *u, int64_t M, int32_t IC,
                            uint16_t *out, int64_t ldo, int64_t col0,
                            void *ws, size_t ws_bytes, exl3_stream stream);
 
+/*
+ * exl3_linear_into without a workspace, for callers that cannot allocate
+ * device memory: code running where cudaMalloc is not allowed or not wanted
+ * (inside a host callback, under an allocator-owning framework or plugin host
+ * that hands out no spare buffer, or on a path that must never trigger an
+ * allocation or its implicit synchronization).  No page the library follows
+ * has a counterpart of this call.
+ *
+ * Same arguments and result as exl3_linear_into, minus the workspace; the
+ * caller still owns x, code, the scale vectors and out.  Scratch comes from one
+ * fixed array of about 6.8 MB that the library declares in device memory:
+ * every GPU that loads the library holds it until the process exits.  Limits:
+ * M <= 8, IC <= 32768, OC <= 65536; larger requests return EXL3_EINVAL and
+ * launch nothing.  The call allocates and frees nothing.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array and clears its counters on
+ * entry, so calls that overlap on the GPU (different streams, or other
+ * threads) race and give wrong results: serialize them.
+ */
+exl3_status exl3_linear_into_noalloc(const uint16_t *x, int64_t M, int32_t IC,
+                                     const int16_t *code, int32_t OC, int32_t K,
+                                     const uint16_t *s_in, const uint16_t *rin,
+                                     const uint16_t *rout, const uint16_t *s_out,
+                                     uint16_t *out, int64_t ldo, int64_t col0,
+                                     exl3_stream stream);
+
 /* exl3_linear_into with out = y [M][OC] contiguous (ldo = OC, col0 = 0). */
 exl3_status exl3_linear(const uint16_t *x, int64_t M, int32_t IC,
                         const int16_t *code, int32_t OC, int32_t K,

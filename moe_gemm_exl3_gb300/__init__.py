@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "EXL3_OK", 1: "EXL3_EINVAL", 2: "EXL3_EWORKSPACE", 3: "EXL3_E
 
 # Every symbol include/exl3.h declares.
 EXPORTS = ("exl3_last_error", "exl3_version", "exl3_linear_workspace_bytes", "exl3_workspace_init",
-           "exl3_workspace_error", "exl3_linear_into", "exl3_linear", "exl3_gemm_into", "exl3_pretransform",
+           "exl3_workspace_error", "exl3_linear_into", "exl3_linear", "exl3_gemm_into", "exl3_linear_into_noalloc", "exl3_pretransform",
            "exl3_reconstruct", "exl3_codebook_table", "exl3_moe_topk_softmax",
            "exl3_moe_workspace_bytes", "exl3_moe_grouped", "exl3_embed_int8_gather")
 
@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
                                       vp], ctypes.c_int),
                 "exl3_linear": ([vp, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp],
                                 ctypes.c_int),
+                "exl3_linear_into_noalloc": ([vp, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, i64, i64,
+                                              vp], ctypes.c_int),
                 "exl3_gemm_into": ([vp, i64, i32, vp, i32, i32, vp, vp, vp, i64, i64, vp, sz, vp],
                                    ctypes.c_int),
                 "exl3_pretransform": ([vp, i64, i32, vp, vp, vp, vp], ctypes.c_int),
@@ -163,6 +165,21 @@ def exl3_linear_into(x: torch.Tensor, code: torch.Tensor, K: int, s_in, rin, rou
         _ptr(rout, torch.float16, "rout"), _ptr(s_out, torch.float16, "s_out"),
         _ptr(out, torch.bfloat16, "out"), ldo, col0, _ptr(ws, torch.uint8, "ws"), ws.numel(),
         _stream(x.device)), "exl3_linear_into")
+
+
+def exl3_linear_into_noalloc(x: torch.Tensor, code: torch.Tensor, K: int, s_in, rin, rout, s_out,
+                             out: torch.Tensor, col0: int) -> None:
+    """exl3_linear_into with no workspace: scratch is the library's fixed device array
+    (M <= 8, IC <= 32768, OC <= 65536).  For callers that cannot allocate device memory;
+    calls that overlap on the GPU race on that array."""
+    IC, OC = _linear_shapes(x, code, K)
+    M = x.numel() // IC
+    _check(lib().exl3_linear_into_noalloc(
+        _ptr(x, torch.bfloat16, "x"), M, IC, _ptr(code, torch.int16, "code"), OC, K,
+        _ptr(s_in, torch.float16, "s_in"), _ptr(rin, torch.float16, "rin"),
+        _ptr(rout, torch.float16, "rout"), _ptr(s_out, torch.float16, "s_out"),
+        _ptr(out, torch.bfloat16, "out"), out.shape[-1], col0, _stream(x.device)),
+        "exl3_linear_into_noalloc")
 
 
 def exl3_linear(x, code, K, s_in, rin, rout, s_out, ws, out=None) -> torch.Tensor:
