@@ -168,6 +168,49 @@ exl3_status exl3_linear_into_noalloc(const uint16_t *x, int64_t M, int32_t IC,
                                      uint16_t *out, int64_t ldo, int64_t col0,
                                      exl3_stream stream);
 
+/*
+ * One merged layer (radiance_escha.py, EschaLinearMethod.apply: gate_up_proj
+ * = gate_proj + up_proj, qkv_proj = q/k/v, each source tensor its own EXL3
+ * tensor with its own K and scale vectors) in one call: the result equals
+ * calling exl3_linear_into once per shard, in order, on the same x and out.
+ * All shards share IC; each has its own code, K, OC, four scale vectors and
+ * column offset col0 (the caller advances col0 by each shard's OC, as
+ * EschaLinearMethod.apply does).  The shards run in one pre-transform launch
+ * and one grouped GEMM launch (for M <= 32 rows per pass), so the merged
+ * layer has one tail instead of one per shard.
+ *   shards   HOST array of n_shards descriptors, 1 <= n_shards <= 4
+ *   ws       exl3_linear_shards_workspace_bytes(M, IC, shards, n_shards) bytes
+ */
+typedef struct exl3_shard {
+    const int16_t *code;      /* [IC/16][OC/16][16*K] */
+    const uint16_t *s_in;     /* fp16 [IC] */
+    const uint16_t *rin;      /* fp16 [IC] */
+    const uint16_t *rout;     /* fp16 [OC] */
+    const uint16_t *s_out;    /* fp16 [OC] */
+    int32_t OC;
+    int32_t K;
+    int64_t col0;
+} exl3_shard;
+
+size_t exl3_linear_shards_workspace_bytes(int64_t max_M, int32_t IC, const exl3_shard *shards,
+                                          int32_t n_shards);
+
+exl3_status exl3_linear_into_shards(const uint16_t *x, int64_t M, int32_t IC,
+                                    const exl3_shard *shards, int32_t n_shards,
+                                    uint16_t *out, int64_t ldo,
+                                    void *ws, size_t ws_bytes, exl3_stream stream);
+
+/*
+ * exl3_linear_into_shards on activations already transformed per shard:
+ * u fp16 [n_shards][M][IC], u[i] = Had128((x * s_in_i) * rin_i) (as
+ * exl3_pretransform writes it); the shards' s_in / rin pointers are ignored.
+ * One grouped GEMM launch per 32 rows.
+ */
+exl3_status exl3_gemm_into_shards(const uint16_t *u, int64_t M, int32_t IC,
+                                  const exl3_shard *shards, int32_t n_shards,
+                                  uint16_t *out, int64_t ldo,
+                                  void *ws, size_t ws_bytes, exl3_stream stream);
+
 /* exl3_linear_into with out = y [M][OC] contiguous (ldo = OC, col0 = 0). */
 exl3_status exl3_linear(const uint16_t *x, int64_t M, int32_t IC,
                         const int16_t *code, int32_t OC, int32_t K,

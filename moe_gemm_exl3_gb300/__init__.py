@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "EXL3_OK", 1: "EXL3_EINVAL", 2: "EXL3_EWORKSPACE", 3: "EXL3_E
 
 # Every symbol include/exl3.h declares.
 EXPORTS = ("exl3_last_error", "exl3_version", "exl3_linear_workspace_bytes", "exl3_workspace_init",
-           "exl3_workspace_error", "exl3_linear_into", "exl3_linear", "exl3_gemm_into", "exl3_linear_into_noalloc", "exl3_pretransform",
+           "exl3_workspace_error", "exl3_linear_into", "exl3_linear", "exl3_gemm_into", "exl3_linear_into_noalloc",
+           "exl3_linear_shards_workspace_bytes", "exl3_linear_into_shards", "exl3_gemm_into_shards", "exl3_pretransform",
            "exl3_reconstruct", "exl3_codebook_table", "exl3_moe_topk_softmax",
            "exl3_moe_workspace_bytes", "exl3_moe_grouped", "exl3_embed_int8_gather")
 
@@ -33,6 +34,13 @@ class Exl3Error(RuntimeError):
     def __init__(self, status: int, fn: str, msg: str):
         super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)}: {msg}")
         self.status = status
+
+
+class Shard(ctypes.Structure):
+    """exl3_shard: one source tensor of a merged layer."""
+    _fields_ = [("code", ctypes.c_void_p), ("s_in", ctypes.c_void_p), ("rin", ctypes.c_void_p),
+                ("rout", ctypes.c_void_p), ("s_out", ctypes.c_void_p), ("OC", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("col0", ctypes.c_int64)]
 
 
 class MoeBank(ctypes.Structure):
@@ -67,6 +75,11 @@ def lib() -> ctypes.CDLL:
                                 ctypes.c_int),
                 "exl3_linear_into_noalloc": ([vp, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, i64, i64,
                                               vp], ctypes.c_int),
+                "exl3_linear_shards_workspace_bytes": ([i64, i32, ctypes.POINTER(Shard), i32], sz),
+                "exl3_linear_into_shards": ([vp, i64, i32, ctypes.POINTER(Shard), i32, vp, i64, vp, sz, vp],
+                                            ctypes.c_int),
+                "exl3_gemm_into_shards": ([vp, i64, i32, ctypes.POINTER(Shard), i32, vp, i64, vp, sz, vp],
+                                          ctypes.c_int),
                 "exl3_gemm_into": ([vp, i64, i32, vp, i32, i32, vp, vp, vp, i64, i64, vp, sz, vp],
                                    ctypes.c_int),
                 "exl3_pretransform": ([vp, i64, i32, vp, vp, vp, vp], ctypes.c_int),
@@ -180,6 +193,51 @@ def exl3_linear_into_noalloc(x: torch.Tensor, code: torch.Tensor, K: int, s_in, 
         _ptr(rout, torch.float16, "rout"), _ptr(s_out, torch.float16, "s_out"),
         _ptr(out, torch.bfloat16, "out"), out.shape[-1], col0, _stream(x.device)),
         "exl3_linear_into_noalloc")
+
+
+def _shard_array(shards, IC):
+    arr = (Shard * len(shards))()
+    col = 0
+    for i, sh in enumerate(shards):
+        code, K, s_in, rin, rout, s_out = sh[:6]
+        col0 = sh[6] if len(sh) > 6 else col
+        if code.dim() != 3 or code.shape[2] != 16 * K or code.shape[0] * 16 != IC:
+            raise ValueError(f"shard {i}: code {tuple(code.shape)} does not match K={K}, IC={IC}")
+        OC = code.shape[1] * 16
+        arr[i] = Shard(_ptr(code, torch.int16, "code"), _ptr(s_in, torch.float16, "s_in"),
+                       _ptr(rin, torch.float16, "rin"), _ptr(rout, torch.float16, "rout"),
+                       _ptr(s_out, torch.float16, "s_out"), OC, K, col0)
+        col = col0 + OC
+    return arr
+
+
+def exl3_linear_shards_workspace_bytes(max_M: int, IC: int, shards) -> int:
+    """shards: sequence of (code, K, s_in, rin, rout, s_out[, col0]) device tensors."""
+    arr = _shard_array(shards, IC)
+    return int(lib().exl3_linear_shards_workspace_bytes(max_M, IC, arr, len(shards)))
+
+
+def exl3_linear_into_shards(x: torch.Tensor, shards, out: torch.Tensor, ws: torch.Tensor) -> None:
+    """A merged layer in one call: shard i = (code, K, s_in, rin, rout, s_out[, col0]) writes
+    out[:, col0:col0+OC_i]; col0 defaults to the running sum of the previous shards' OC."""
+    IC = x.shape[-1]
+    M = x.numel() // IC
+    arr = _shard_array(shards, IC)
+    _check(lib().exl3_linear_into_shards(_ptr(x, torch.bfloat16, "x"), M, IC, arr, len(shards),
+                                         _ptr(out, torch.bfloat16, "out"), out.shape[-1],
+                                         _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(x.device)),
+           "exl3_linear_into_shards")
+
+
+def exl3_gemm_into_shards(u: torch.Tensor, shards, out: torch.Tensor, ws: torch.Tensor) -> None:
+    """Grouped trellis GEMM + output transform of per-shard pre-transformed u [n][M][IC]."""
+    IC = u.shape[-1]
+    M = u.shape[-2]
+    arr = _shard_array(shards, IC)
+    _check(lib().exl3_gemm_into_shards(_ptr(u, torch.float16, "u"), M, IC, arr, len(shards),
+                                       _ptr(out, torch.bfloat16, "out"), out.shape[-1],
+                                       _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(u.device)),
+           "exl3_gemm_into_shards")
 
 
 def exl3_linear(x, code, K, s_in, rin, rout, s_out, ws, out=None) -> torch.Tensor:

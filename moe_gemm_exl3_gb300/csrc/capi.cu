@@ -58,6 +58,8 @@ const DeviceInfo &device_info() {
 }
 
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+size_t linear_workspace_layout_n(int64_t max_M, int32_t IC, int n_shards, int total_groups, int32_t max_OC,
+                                 LinearWorkspace *ws, void *base);
 
 // Fixed part of every workspace: error word, then the arrival counters.
 constexpr size_t kHeaderBytes = 256;
@@ -84,20 +86,24 @@ int64_t prefill_threshold() {
 
 size_t linear_workspace_layout(int64_t max_M, int32_t max_IC, int32_t max_OC, LinearWorkspace *ws,
                                void *base) {
-    if (max_M < 0 || max_IC <= 0 || max_OC <= 0) return 0;
-    const int64_t NG = max_OC / 128;
+    return linear_workspace_layout_n(max_M, max_IC, 1, max_OC / 128, max_OC, ws, base);
+}
+
+size_t linear_workspace_layout_n(int64_t max_M, int32_t IC, int n_shards, int total_groups, int32_t max_OC,
+                                 LinearWorkspace *ws, void *base) {
+    if (max_M < 0 || IC <= 0 || max_OC <= 0 || n_shards <= 0) return 0;
     const int64_t dec_rows = max_M < kDecodeMaxRows ? max_M : kDecodeMaxRows;
-    const int64_t nb = (dec_rows + 7) / 8;
+    const int nb = (int)((dec_rows + 7) / 8 > 0 ? (dec_rows + 7) / 8 : 1);
     size_t off = kFixedBytes;
-    const size_t u_elems = (size_t)max_M * max_IC;
+    const size_t u_elems = (size_t)n_shards * max_M * IC;
     const size_t u_off = off;
     off = align256(off + u_elems * sizeof(uint16_t));
-    const size_t part_elems = (size_t)(kDecodeMaxCtas + NG) * (8 * nb * 4 * 32);
+    const size_t part_elems = group_slab_floats(total_groups, nb);
     const size_t part_off = off;
     off = align256(off + part_elems * sizeof(float));
     size_t wt_elems = 0, wt_off = off;
     if (max_M > prefill_threshold() && prefill_supported()) {
-        wt_elems = (size_t)max_OC * max_IC;
+        wt_elems = (size_t)max_OC * IC;
         off = align256(off + wt_elems * sizeof(uint16_t));
     }
     if (ws) {
@@ -188,44 +194,66 @@ exl3_status exl3_pretransform(const uint16_t *x, int64_t M, int32_t IC, const ui
     return EXL3_OK;
 }
 
-// Trellis GEMM + epilogue on pre-transformed activations u (fp16 [M][IC]).
-static exl3_status gemm_into_impl(const char *fn, const uint16_t *u, int64_t M, int32_t IC, const int16_t *code,
-                                  int32_t OC, int32_t K, const uint16_t *rout, const uint16_t *s_out,
-                                  uint16_t *dst, int64_t ldo, const LinearWorkspace &ws, cudaStream_t s) {
+struct ShardDesc {
+    const int16_t *code;
+    const uint16_t *s_in, *rin, *rout, *s_out;
+    int32_t OC, K;
+    int64_t col0;
+};
+
+// Trellis GEMM + epilogue for n shards whose pre-transformed activations sit
+// in u as [shard][M][IC] (fp16).
+static exl3_status run_gemm(const char *fn, const uint16_t *u, int64_t M, int32_t IC, const ShardDesc *sh, int n,
+                            uint16_t *out, int64_t ldo, const LinearWorkspace &ws, bool pdl, cudaStream_t s) {
     cudaError_t e;
     if (M > prefill_threshold() && prefill_supported()) {
-        bool launched = false;
-        e = launch_reconstruct(code, IC, OC, K, ws.wt, /*transposed=*/true, s);
-        if (e != cudaSuccess) return cuda_fail(e, fn);
-        e = launch_prefill(u, ws.wt, M, IC, OC, rout, s_out, dst, ldo, ws.err, s, &launched);
-        if (e != cudaSuccess) return cuda_fail(e, fn);
-        trace("%s M=%lld IC=%d OC=%d K=%d mode=prefill", fn, (long long)M, IC, OC, K);
-        if (launched) return EXL3_OK;
+        for (int i = 0; i < n; i++) {
+            bool launched = false;
+            e = launch_reconstruct(sh[i].code, IC, sh[i].OC, sh[i].K, ws.wt, /*transposed=*/true, s);
+            if (e != cudaSuccess) return cuda_fail(e, fn);
+            e = launch_prefill(u + (int64_t)i * M * IC, ws.wt, M, IC, sh[i].OC, sh[i].rout, sh[i].s_out,
+                               out + sh[i].col0, ldo, ws.err, s, &launched);
+            if (e != cudaSuccess) return cuda_fail(e, fn);
+            if (!launched) return fail(EXL3_EUNSUPPORTED, "%s: prefill path unavailable", fn);
+        }
+        trace("%s M=%lld IC=%d shards=%d mode=prefill", fn, (long long)M, IC, n);
+        return EXL3_OK;
     }
-    // decode mode: passes of up to kDecodeMaxRows rows
+    // decode mode: passes of up to kDecodeMaxRows rows, all shards in one launch per pass
     for (int64_t r0 = 0; r0 < M; r0 += kDecodeMaxRows) {
-        DecodeGemmArgs a;
-        a.u = u + r0 * IC;
-        a.code = code;
+        const int rows = (int)((M - r0) < kDecodeMaxRows ? (M - r0) : kDecodeMaxRows);
+        GroupGemmArgs a = {};
+        a.u = u;
         a.IC = IC;
-        a.OC = OC;
-        a.K = K;
-        a.M = (int)((M - r0) < kDecodeMaxRows ? (M - r0) : kDecodeMaxRows);
-        a.rout = rout;
-        a.s_out = s_out;
-        a.out = dst + r0 * ldo;
+        a.mode = kModeDense;
+        a.n_inline = n;
+        int g0 = 0;
+        for (int i = 0; i < n; i++) {
+            GroupEntry &ge = a.inline_e[i];
+            ge.code = sh[i].code;
+            ge.post = sh[i].rout;
+            ge.post2 = sh[i].s_out;
+            ge.out_off = sh[i].col0;
+            ge.K = sh[i].K;
+            ge.OC = sh[i].OC;
+            ge.u_row0 = (int32_t)((int64_t)i * M + r0);
+            ge.nrows = rows;
+            ge.g0 = g0;
+            g0 += sh[i].OC / 128;
+        }
+        a.out = out + r0 * ldo;
         a.ldo = ldo;
         a.partials = ws.partials;
         a.counters = ws.counters;
-        e = launch_decode_gemm(a, s);
+        e = launch_group_gemm(a, (rows + 7) / 8, pdl, s);
         if (e != cudaSuccess) return cuda_fail(e, fn);
     }
-    trace("%s M=%lld IC=%d OC=%d K=%d mode=decode", fn, (long long)M, IC, OC, K);
+    trace("%s M=%lld IC=%d shards=%d mode=decode", fn, (long long)M, IC, n);
     return EXL3_OK;
 }
 
-static exl3_status check_out_ws(const char *fn, int64_t M, int32_t IC, int32_t OC, const uint16_t *out,
-                                int64_t ldo, int64_t col0, void *wsp, size_t ws_bytes) {
+static exl3_status check_out_ws(const char *fn, int64_t M, int32_t OC, const uint16_t *out, int64_t ldo,
+                                int64_t col0, void *wsp, size_t ws_bytes, size_t need) {
     if (ldo < OC || col0 < 0 || col0 + OC > ldo)
         return fail(EXL3_EINVAL, "%s: column slice [%lld, %lld) does not fit ldo = %lld", fn,
                     (long long)col0, (long long)col0 + OC, (long long)ldo);
@@ -234,11 +262,9 @@ static exl3_status check_out_ws(const char *fn, int64_t M, int32_t IC, int32_t O
     if ((ldo % 8) || (col0 % 8) || !aligned16(out))
         return fail(EXL3_EINVAL, "%s: out (%p), ldo = %lld and col0 = %lld must give 16-byte "
                     "aligned rows (ldo, col0 multiples of 8)", fn, out, (long long)ldo, (long long)col0);
-    const size_t need = exl3_linear_workspace_bytes(M, IC, OC);
     if (!wsp || (reinterpret_cast<uintptr_t>(wsp) & 255u) || ws_bytes < need)
         return fail(EXL3_EWORKSPACE, "%s: workspace %p of %zu bytes; this call needs %zu bytes, "
-                    "256-byte aligned (exl3_linear_workspace_bytes(%lld, %d, %d))", fn, wsp, ws_bytes, need,
-                    (long long)M, IC, OC);
+                    "256-byte aligned", fn, wsp, ws_bytes, need);
     return EXL3_OK;
 }
 
@@ -247,26 +273,98 @@ exl3_status exl3_linear_into(const uint16_t *x, int64_t M, int32_t IC, const int
                              const uint16_t *s_out, uint16_t *out, int64_t ldo, int64_t col0, void *wsp,
                              size_t ws_bytes, exl3_stream stream) {
     exl3_status st = check_linear_args("linear_into", x, M, IC, code, OC, K, s_in, rin, rout, s_out);
-    if (st == EXL3_OK) st = check_out_ws("linear_into", M, IC, OC, out, ldo, col0, wsp, ws_bytes);
+    if (st == EXL3_OK)
+        st = check_out_ws("linear_into", M, OC, out, ldo, col0, wsp, ws_bytes, exl3_linear_workspace_bytes(M, IC, OC));
     if (st != EXL3_OK || M == 0) return st;
     LinearWorkspace ws;
     linear_workspace_layout(M, IC, OC, &ws, wsp);
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = launch_pretransform(x, M, IC, s_in, rin, ws.u, s);
     if (e != cudaSuccess) return cuda_fail(e, "linear_into: pretransform");
-    return gemm_into_impl("linear_into", ws.u, M, IC, code, OC, K, rout, s_out, out + col0, ldo, ws, s);
+    ShardDesc d = {code, s_in, rin, rout, s_out, OC, K, col0};
+    return run_gemm("linear_into", ws.u, M, IC, &d, 1, out, ldo, ws, true, s);
 }
 
 exl3_status exl3_gemm_into(const uint16_t *u, int64_t M, int32_t IC, const int16_t *code, int32_t OC, int32_t K,
                            const uint16_t *rout, const uint16_t *s_out, uint16_t *out, int64_t ldo, int64_t col0,
                            void *wsp, size_t ws_bytes, exl3_stream stream) {
     exl3_status st = check_linear_args("gemm_into", u, M, IC, code, OC, K, rout, rout, rout, s_out);
-    if (st == EXL3_OK) st = check_out_ws("gemm_into", M, IC, OC, out, ldo, col0, wsp, ws_bytes);
+    if (st == EXL3_OK)
+        st = check_out_ws("gemm_into", M, OC, out, ldo, col0, wsp, ws_bytes, exl3_linear_workspace_bytes(M, IC, OC));
     if (st != EXL3_OK || M == 0) return st;
     LinearWorkspace ws;
     linear_workspace_layout(M, IC, OC, &ws, wsp);
-    return gemm_into_impl("gemm_into", u, M, IC, code, OC, K, rout, s_out, out + col0, ldo, ws,
-                          (cudaStream_t)stream);
+    ShardDesc d = {code, nullptr, nullptr, rout, s_out, OC, K, col0};
+    return run_gemm("gemm_into", u, M, IC, &d, 1, out, ldo, ws, false, (cudaStream_t)stream);
+}
+
+static bool shards_shape(const exl3_shard *shards, int32_t n, int *groups, int32_t *max_oc) {
+    if (!shards || n < 1 || n > kMaxInlineEntries) return false;
+    *groups = 0;
+    *max_oc = 0;
+    for (int i = 0; i < n; i++) {
+        if (shards[i].OC <= 0 || shards[i].OC % 128) return false;
+        *groups += shards[i].OC / 128;
+        if (shards[i].OC > *max_oc) *max_oc = shards[i].OC;
+    }
+    return *groups <= (int)kCounterCount;
+}
+
+size_t exl3_linear_shards_workspace_bytes(int64_t max_M, int32_t IC, const exl3_shard *shards, int32_t n) {
+    int groups;
+    int32_t max_oc;
+    if (max_M < 0 || IC <= 0 || IC % 128 || !shards_shape(shards, n, &groups, &max_oc)) return 0;
+    return linear_workspace_layout_n(max_M, IC, n, groups, max_oc, nullptr, nullptr);
+}
+
+static exl3_status shards_prepare(const char *fn, const uint16_t *x, int64_t M, int32_t IC, const exl3_shard *shards,
+                                  int32_t n, uint16_t *out, int64_t ldo, void *wsp, size_t ws_bytes, bool need_in,
+                                  ShardDesc *d, LinearWorkspace *ws) {
+    int groups;
+    int32_t max_oc;
+    if (!shards_shape(shards, n, &groups, &max_oc))
+        return fail(EXL3_EINVAL, "%s: need 1..%d shard descriptors with OC a positive multiple of 128", fn,
+                    kMaxInlineEntries);
+    for (int i = 0; i < n; i++) {
+        const exl3_shard &h = shards[i];
+        const uint16_t *si = need_in ? h.s_in : h.rout, *ri = need_in ? h.rin : h.rout;
+        exl3_status st = check_linear_args(fn, x, M, IC, h.code, h.OC, h.K, si, ri, h.rout, h.s_out);
+        if (st == EXL3_OK)
+            st = check_out_ws(fn, M, h.OC, out, ldo, h.col0, wsp, ws_bytes,
+                              exl3_linear_shards_workspace_bytes(M, IC, shards, n));
+        if (st != EXL3_OK) return st;
+        d[i] = {h.code, h.s_in, h.rin, h.rout, h.s_out, h.OC, h.K, h.col0};
+    }
+    if (M > 0) linear_workspace_layout_n(M, IC, n, groups, max_oc, ws, wsp);
+    return EXL3_OK;
+}
+
+exl3_status exl3_linear_into_shards(const uint16_t *x, int64_t M, int32_t IC, const exl3_shard *shards,
+                                    int32_t n, uint16_t *out, int64_t ldo, void *wsp, size_t ws_bytes,
+                                    exl3_stream stream) {
+    ShardDesc d[kMaxInlineEntries];
+    LinearWorkspace ws;
+    exl3_status st = shards_prepare("linear_into_shards", x, M, IC, shards, n, out, ldo, wsp, ws_bytes, true, d, &ws);
+    if (st != EXL3_OK || M == 0) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    PretransformShards p = {};
+    p.n = n;
+    for (int i = 0; i < n; i++) {
+        p.s_in[i] = d[i].s_in;
+        p.rin[i] = d[i].rin;
+    }
+    cudaError_t e = launch_pretransform_shards(x, M, IC, p, ws.u, s);
+    if (e != cudaSuccess) return cuda_fail(e, "linear_into_shards: pretransform");
+    return run_gemm("linear_into_shards", ws.u, M, IC, d, n, out, ldo, ws, true, s);
+}
+
+exl3_status exl3_gemm_into_shards(const uint16_t *u, int64_t M, int32_t IC, const exl3_shard *shards, int32_t n,
+                                  uint16_t *out, int64_t ldo, void *wsp, size_t ws_bytes, exl3_stream stream) {
+    ShardDesc d[kMaxInlineEntries];
+    LinearWorkspace ws;
+    exl3_status st = shards_prepare("gemm_into_shards", u, M, IC, shards, n, out, ldo, wsp, ws_bytes, false, d, &ws);
+    if (st != EXL3_OK || M == 0) return st;
+    return run_gemm("gemm_into_shards", u, M, IC, d, n, out, ldo, ws, false, (cudaStream_t)stream);
 }
 
 exl3_status exl3_linear(const uint16_t *x, int64_t M, int32_t IC, const int16_t *code, int32_t OC, int32_t K,

@@ -44,9 +44,20 @@ __device__ __forceinline__ uint16_t f32_to_f16_bits(float v) {
 // ---------------------------------------------------------------- trellis
 // 3INST hash of a 16-bit trellis state: returns the two fp16 halves z' whose
 // sum is the decoded weight (low half in bits 0..15, high half in 16..31).
+constexpr uint32_t kHashMul = 89226354u, kHashAdd = 64248484u;
+constexpr uint32_t kHashMask = 0x8FFF8FFFu, kHashXor = 0x3B603B60u;
 __device__ __forceinline__ uint32_t trellis_hash(uint32_t state) {
-    uint32_t z = state * 89226354u + 64248484u;
-    return (z & 0x8FFF8FFFu) ^ 0x3B603B60u;
+    uint32_t z = state * kHashMul + kHashAdd;
+    return (z & kHashMask) ^ kHashXor;
+}
+
+// The same hash with the xor constant held in a register: one LOP3 instead of
+// two (a LOP3 takes at most one 32-bit immediate).  Hot loops pass kHashXor
+// through a kernel argument so the compiler cannot fold it back into an
+// immediate.
+__device__ __forceinline__ uint32_t trellis_hash_x(uint32_t state, uint32_t xor_reg) {
+    uint32_t z = state * kHashMul + kHashAdd;
+    return (z & kHashMask) ^ xor_reg;
 }
 
 // The decoded fp16 weight of one hashed state: lo + hi, rounded once.

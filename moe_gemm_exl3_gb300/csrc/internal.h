@@ -35,22 +35,61 @@ size_t linear_workspace_layout(int64_t max_M, int32_t max_IC, int32_t max_OC,
 
 cudaError_t launch_pretransform(const uint16_t *x, int64_t M, int IC, const uint16_t *s_in,
                                 const uint16_t *rin, uint16_t *u, cudaStream_t s);
+// Pre-transform of x once per shard: u[shard][m][:] with shard s using (s_in[s], rin[s]).
+struct PretransformShards {
+    const uint16_t *s_in[4];
+    const uint16_t *rin[4];
+    int n;
+};
+cudaError_t launch_pretransform_shards(const uint16_t *x, int64_t M, int IC, const PretransformShards &p,
+                                       uint16_t *u, cudaStream_t s);
 cudaError_t launch_reconstruct(const int16_t *code, int IC, int OC, int K, uint16_t *W,
                                bool transposed, cudaStream_t s);
 cudaError_t launch_codebook_table(uint16_t *table, cudaStream_t s);
 
-struct DecodeGemmArgs {
-    const uint16_t *u;        // fp16 [M][IC]
+// One problem of the grouped decode-mode GEMM: a code tensor [IC/16][OC/16][16K]
+// applied to rows [u_row0, u_row0 + nrows) of the activation matrix.
+struct GroupEntry {
     const int16_t *code;
-    int IC, OC, K;
-    int M;                    // rows in this pass (<= kDecodeMaxRows)
-    const uint16_t *rout, *s_out;
-    uint16_t *out;            // bf16, row stride ldo, already offset by col0
+    const uint16_t *post;     // dense: rout [OC]; rows mode: post-scale [OC]
+    const uint16_t *post2;    // dense: s_out [OC]; rows mode: unused
+    int64_t out_off;          // dense: column of out where this entry starts; rows: first output row
+    int32_t K;
+    int32_t OC;
+    int32_t u_row0;
+    int32_t nrows;            // <= 8 * NB of the launch
+    int32_t g0;               // first global column-group index of this entry
+    int32_t pad_;
+};
+
+enum GroupMode : int32_t {
+    kModeDense = 0,   // y = (Had128(v) * post) * post2 -> bf16 out[row][out_off + col], row stride ldo
+    kModeRows = 1,    // y = Had128(v) * post -> fp32 out_rows[(out_off + row) * OC + col]
+};
+
+struct GroupGemmArgs {
+    const uint16_t *u;            // fp16 activations, row stride IC
+    int IC;
+    int mode;
+    const GroupEntry *entries;    // device array (MoE) or nullptr (use inline)
+    const int32_t *n_entries_dev; // device entry count (MoE) or nullptr
+    int n_groups_per_entry;       // > 0: every entry has this many column groups (MoE)
+    int n_inline;
+    GroupEntry inline_e[4];       // dense: up to 4 shards passed by value
+    uint16_t *out;                // dense output base (bf16), row stride ldo
     int64_t ldo;
+    float *out_rows;              // rows-mode output (fp32)
     float *partials;
     int32_t *counters;
+    uint32_t hash_xor;            // the codebook's xor constant, kept in a register
+    int32_t max_rows;             // rows per entry the launch was sized for
 };
-cudaError_t launch_decode_gemm(const DecodeGemmArgs &a, cudaStream_t s);
+constexpr int kMaxInlineEntries = 4;
+
+// Launch the grouped decode-mode GEMM; `max_groups` bounds the total number of
+// column groups (for the partial slab), rows per entry <= 8 * nb.
+cudaError_t launch_group_gemm(const GroupGemmArgs &a, int nb, bool pdl, cudaStream_t s);
+size_t group_slab_floats(int max_groups, int nb);
 
 bool prefill_supported();
 cudaError_t launch_prefill(const uint16_t *u, const uint16_t *wt, int64_t M, int IC, int OC,

@@ -13,41 +13,53 @@ namespace exl3 {
 // One warp per (row, block); lane l holds channels 4l..4l+3 of the block.
 // --------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) pretransform_kernel(const uint16_t *__restrict__ x,
-                                                           int64_t M, int IC,
-                                                           const uint16_t *__restrict__ s_in,
-                                                           const uint16_t *__restrict__ rin,
+                                                           int64_t M, int IC, PretransformShards p,
                                                            uint16_t *__restrict__ u) {
+    // let a dependent launch (the GEMM that reads u) get scheduled early; it
+    // still waits for this grid to finish before touching u
+    asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int blocks = IC / kHad;
-    if (wid >= M * blocks) return;
-    const int64_t m = wid / blocks;
-    const int c0 = (int)(wid % blocks) * kHad + 4 * lane;
+    if (wid >= (int64_t)p.n * M * blocks) return;
+    const int sh = (int)(wid / (M * blocks));
+    const int64_t rem = wid % (M * blocks);
+    const int64_t m = rem / blocks;
+    const int c0 = (int)(rem % blocks) * kHad + 4 * lane;
     const uint2 xv = *reinterpret_cast<const uint2 *>(x + m * IC + c0);
-    const uint2 sv = __ldg(reinterpret_cast<const uint2 *>(s_in + c0));
-    const uint2 rv = __ldg(reinterpret_cast<const uint2 *>(rin + c0));
+    const uint2 sv = __ldg(reinterpret_cast<const uint2 *>(p.s_in[sh] + c0));
+    const uint2 rv = __ldg(reinterpret_cast<const uint2 *>(p.rin[sh] + c0));
     const uint32_t xs[2] = {xv.x, xv.y}, ss[2] = {sv.x, sv.y}, rs[2] = {rv.x, rv.y};
     float v[4];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
         const uint32_t xb = (xs[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
-        const float s = f16_bits_to_f32((uint16_t)(ss[i >> 1] >> (16 * (i & 1))));
+        const float sc = f16_bits_to_f32((uint16_t)(ss[i >> 1] >> (16 * (i & 1))));
         const float r = f16_bits_to_f32((uint16_t)(rs[i >> 1] >> (16 * (i & 1))));
-        v[i] = (bf16_bits_to_f32(xb) * s) * r;
+        v[i] = (bf16_bits_to_f32(xb) * sc) * r;
     }
     warp_fwht128(v, lane);
     uint2 o;
     o.x = (uint32_t)f32_to_f16_bits(v[0] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[1] * kHadNorm) << 16);
     o.y = (uint32_t)f32_to_f16_bits(v[2] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[3] * kHadNorm) << 16);
-    *reinterpret_cast<uint2 *>(u + m * IC + c0) = o;
+    *reinterpret_cast<uint2 *>(u + ((int64_t)sh * M + m) * IC + c0) = o;
+}
+
+cudaError_t launch_pretransform_shards(const uint16_t *x, int64_t M, int IC, const PretransformShards &p,
+                                       uint16_t *u, cudaStream_t s) {
+    const int64_t warps = (int64_t)p.n * M * (IC / kHad);
+    const int64_t grid = (warps + 7) / 8;
+    pretransform_kernel<<<(unsigned)grid, 256, 0, s>>>(x, M, IC, p, u);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_pretransform(const uint16_t *x, int64_t M, int IC, const uint16_t *s_in,
                                 const uint16_t *rin, uint16_t *u, cudaStream_t s) {
-    const int64_t warps = M * (IC / kHad);
-    const int64_t grid = (warps + 7) / 8;
-    pretransform_kernel<<<(unsigned)grid, 256, 0, s>>>(x, M, IC, s_in, rin, u);
-    return cudaGetLastError();
+    PretransformShards p = {};
+    p.s_in[0] = s_in;
+    p.rin[0] = rin;
+    p.n = 1;
+    return launch_pretransform_shards(x, M, IC, p, u, s);
 }
 
 // --------------------------------------------------------------------------
@@ -120,36 +132,34 @@ cudaError_t launch_codebook_table(uint16_t *table, cudaStream_t s) {
 }
 
 // --------------------------------------------------------------------------
-// Decode-mode fused trellis GEMM (M <= 32 rows per pass).
+// Grouped decode-mode fused trellis GEMM (rows per problem <= 8 * NB <= 32).
 //
-// v = u @ W with W decoded on the fly from the code words, then the epilogue
-// y = (Had128(v) * rout) * s_out written as bf16 into the caller's columns.
+// Each problem ("entry") is one code tensor applied to a block of activation
+// rows: v = u @ W with W decoded on the fly from the code words, followed by
+// the output transform.  The dense linear is one entry per shard; the MoE
+// layer is one entry per (expert, row block) with each expert's own K.
 //
 // Mapping.  A warp owns one column group G (8 tiles = 128 output columns) and
 // one tile row a (16 input channels) per step.  Lane (g, q) = (lane/4, lane%4)
 // loads quarter q (tile rows 4q..4q+3) of tile (a, 8G + g): the warp's 8 tiles
-// are contiguous in memory, so one step is one coalesced 512-byte (K=2) read.
+// are contiguous in memory, so one step is one coalesced read of 512 K bytes.
 // The decoded weights go straight into the A operand of m16n8k16 MMAs with the
-// roles swapped (A = W^T: output columns on the MMA's M, tokens on its N):
+// roles swapped (A = W^T: output columns on the MMA's M, rows on its N):
 // A row g <-> column 16(8G+g)+2j, row g+8 <-> the next column, and each A
 // register holds the two fp16 halves (lo, hi) of one weight's codebook sum
 // against a B register holding the same activation twice, so the tensor core
 // forms u*(lo+hi) and no per-weight add is issued on the ALUs.
 //
-// Split-K.  The (G, a) units are split evenly over a persistent grid; a CTA's
-// range covers parts of one or two column groups.  Warps reduce through shared
-// memory in fixed order; CTAs sharing a group write their partial to a slab
-// slot and bump the group's counter; the last to arrive sums the partials in
-// CTA order (deterministic), runs the epilogue and resets the counter.  No CTA
-// waits on another (radiance_escha.py: split-K partial slab + block counter).
+// Split-K.  The (group, a) units of all entries are split evenly over a
+// persistent grid; a CTA's range covers parts of one or two column groups.
+// Warps reduce through shared memory in fixed order; CTAs sharing a group write
+// their partial to a slab slot and bump the group's counter; the last to arrive
+// sums the partials in CTA order (deterministic), runs the epilogue and resets
+// the counter.  No CTA waits on another (radiance_escha.py: split-K partial slab
+// + block counter).
 // --------------------------------------------------------------------------
-template <int NB>
-struct DecodeSmem {
-    float red[8 * NB * 4 * 32];   // CTA partial in MMA fragment order
-    int last;
-};
 
-// Fragment-order index of (token n, group-local column oc).
+// Fragment-order index of (row n, group-local column oc).
 template <int NB>
 __device__ __forceinline__ int frag_index(int n, int oc) {
     const int g = oc >> 4, j = (oc & 15) >> 1, rrow = oc & 1;
@@ -157,24 +167,135 @@ __device__ __forceinline__ int frag_index(int n, int oc) {
     return ((j * NB + nb) * 4 + (2 * rrow + c)) * 32 + (4 * g + q);
 }
 
+// Registers per thread grow with NB (the accumulators); the bound keeps NB = 1
+// at three CTAs (24 warps) per SM.
+template <int NB>
+struct DecodeOcc { static constexpr int value = NB == 1 ? 3 : (NB == 2 ? 2 : 1); };
+
+template <int NB>
+constexpr size_t group_smem_bytes() {
+    return sizeof(float) * kDecodeWarps * 8 * NB * 4 * 32 + sizeof(GroupEntry) + 16;
+}
+
+// Accumulate tile rows [a_lo, a_hi) of one column group into acc (one warp,
+// rows a_lo + warp, a_lo + warp + 8, ...).
 template <int K, int NB>
-__global__ void __launch_bounds__(256) decode_gemm_kernel(const DecodeGemmArgs a) {
-    __shared__ DecodeSmem<NB> sm;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const GroupEntry &e, const uint16_t *u,
+                                                 int IC, int G, int a_lo, int a_hi, int lane, int warp,
+                                                 uint32_t hx) {
+    constexpr int PF = 2;   // tile rows of code words in flight per warp
     const int g = lane >> 2, q = lane & 3;
+    const int TO = e.OC / kTile;
+    const uint32_t *tile0 = reinterpret_cast<const uint32_t *>(e.code) + (int64_t)(8 * G + g) * 8 * K + q * 2 * K;
+    const int64_t row_words = (int64_t)TO * 8 * K;   // uint32 words per tile row
+    const uint16_t *ub = u + (int64_t)e.u_row0 * IC;
+    // activations of row 8nb+g, channels 16a + 4q .. +3 (zeros past the entry's rows)
+    auto load_u = [&](uint2 (&v)[NB], int ar) {
+#pragma unroll
+        for (int nb = 0; nb < NB; nb++) {
+            v[nb] = make_uint2(0u, 0u);
+            if (8 * nb + g < e.nrows && ar < a_hi)
+                v[nb] = __ldg(reinterpret_cast<const uint2 *>(ub + (int64_t)(8 * nb + g) * IC + 16 * ar + 4 * q));
+        }
+    };
+    int ar = a_lo + warp;
+    uint32_t wq[PF][2 * K];
+#pragma unroll
+    for (int d = 0; d < PF; d++)
+        if (ar + d * kDecodeWarps < a_hi) load_quarter<K>(wq[d], tile0 + (ar + d * kDecodeWarps) * row_words);
+    uint2 un[NB];
+    load_u(un, ar);
+    for (; ar < a_hi; ar += kDecodeWarps) {
+        uint32_t w[2 * K];
+#pragma unroll
+        for (int i = 0; i < 2 * K; i++) w[i] = wq[0][i];
+#pragma unroll
+        for (int d = 0; d + 1 < PF; d++)
+#pragma unroll
+            for (int i = 0; i < 2 * K; i++) wq[d][i] = wq[d + 1][i];
+        if (ar + PF * kDecodeWarps < a_hi) load_quarter<K>(wq[PF - 1], tile0 + (ar + PF * kDecodeWarps) * row_words);
+
+        // this row's activations, each duplicated into a half2; prefetch the next row's
+        uint32_t b[NB][4];
+#pragma unroll
+        for (int nb = 0; nb < NB; nb++) {
+            b[nb][0] = dup_half_lo(un[nb].x);
+            b[nb][1] = dup_half_hi(un[nb].x);
+            b[nb][2] = dup_half_lo(un[nb].y);
+            b[nb][3] = dup_half_hi(un[nb].y);
+        }
+        load_u(un, ar + kDecodeWarps);
+
+        QuarterStream<K> st;
+        st.build(w, quarter_prev_word(w[2 * K - 1], lane));
+#pragma unroll
+        for (int rp = 0; rp < 2; rp++) {
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const int i0 = 32 * rp + 2 * j;
+                const uint32_t z0 = trellis_hash_x(st.state(i0), hx);
+                const uint32_t z1 = trellis_hash_x(st.state(i0 + 1), hx);
+                const uint32_t z2 = trellis_hash_x(st.state(i0 + 16), hx);
+                const uint32_t z3 = trellis_hash_x(st.state(i0 + 17), hx);
+#pragma unroll
+                for (int nb = 0; nb < NB; nb++)
+                    mma_16816(acc[j][nb], z0, z1, z2, z3, b[nb][2 * rp], b[nb][2 * rp + 1]);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// KSET: bit k set = the launch may contain entries of bitrate k (2, 3, 4); only
+// those decode paths are compiled into the kernel, which keeps registers low.
+template <int NB, int KSET>
+__global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(const GroupGemmArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    constexpr int FRAG = 8 * NB * 4 * 32;
+    float *red = reinterpret_cast<float *>(smem_raw);                   // [warps][FRAG]
+    GroupEntry *s_ent = reinterpret_cast<GroupEntry *>(red + kDecodeWarps * FRAG);
+    int *s_last = reinterpret_cast<int *>(s_ent + 1);
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int A = a.IC / kTile;
-    const int NG = a.OC / kHad;
-    const int TO = a.OC / kTile;
-    const int64_t total = (int64_t)NG * A;
+
+    // everything below reads what the preceding kernel in the stream wrote
+    grid_dependency_wait();
+
+    int n_groups;
+    const int n_entries = a.n_entries_dev ? *a.n_entries_dev : a.n_inline;
+    if (a.n_groups_per_entry > 0) {
+        n_groups = n_entries * a.n_groups_per_entry;
+    } else {
+        n_groups = 0;
+        for (int i = 0; i < n_entries; i++) n_groups += a.inline_e[i].OC / kHad;
+    }
+    const int64_t total = (int64_t)n_groups * A;
     const int nCTA = gridDim.x, c = blockIdx.x;
     int64_t f = (int64_t)c * total / nCTA;
     const int64_t f_end = (int64_t)(c + 1) * total / nCTA;
-    constexpr int FRAG = 8 * NB * 4 * 32;
+    const uint32_t hx = a.hash_xor;
 
     while (f < f_end) {
-        const int G = (int)(f / A);
+        const int gi = (int)(f / A);                 // global column-group index
         const int a_lo = (int)(f % A);
         const int a_hi = (int)((int64_t)A < a_lo + (f_end - f) ? (int64_t)A : a_lo + (f_end - f));
+        // the entry owning group gi
+        if (threadIdx.x == 0) {
+            if (a.n_groups_per_entry > 0) {
+                *s_ent = a.entries ? a.entries[gi / a.n_groups_per_entry] : a.inline_e[gi / a.n_groups_per_entry];
+            } else {
+                int i = 0;
+                while (i + 1 < n_entries && a.inline_e[i + 1].g0 <= gi) i++;
+                *s_ent = a.inline_e[i];
+            }
+        }
+        __syncthreads();
+        const GroupEntry e = *s_ent;
+        const int G = a.n_groups_per_entry > 0 ? gi % a.n_groups_per_entry : gi - e.g0;
 
         float acc[8][NB][4];
 #pragma unroll
@@ -183,158 +304,152 @@ __global__ void __launch_bounds__(256) decode_gemm_kernel(const DecodeGemmArgs a
             for (int nb = 0; nb < NB; nb++)
 #pragma unroll
                 for (int r = 0; r < 4; r++) acc[j][nb][r] = 0.f;
+        if ((KSET & 4) && e.K == 2) group_accumulate<2, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx);
+        if ((KSET & 8) && e.K == 3) group_accumulate<3, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx);
+        if ((KSET & 16) && e.K == 4) group_accumulate<4, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx);
 
-        const uint32_t *tile0 = reinterpret_cast<const uint32_t *>(a.code) +
-                                ((int64_t)(8 * G + g) * 16 * K) / 2 + q * 2 * K;
-        const int64_t row_words = (int64_t)TO * 8 * K;   // uint32 words per tile row
-        int ar = a_lo + warp;
-        uint32_t w[2 * K];
-        if (ar < a_hi) load_quarter<K>(w, tile0 + ar * row_words);
-        for (; ar < a_hi; ar += kDecodeWarps) {
-            uint32_t wn[2 * K];
-            const int an = ar + kDecodeWarps;
-            if (an < a_hi) load_quarter<K>(wn, tile0 + an * row_words);
-
-            // activations for k = 16a + 4q + 0..3, each duplicated into a half2
-            uint32_t b[NB][4];
+        // ---- CTA reduction in fixed warp order (fragment order, one barrier)
 #pragma unroll
-            for (int nb = 0; nb < NB; nb++) {
-                const int n = 8 * nb + g;
-                uint2 v = make_uint2(0u, 0u);
-                if (n < a.M)
-                    v = __ldg(reinterpret_cast<const uint2 *>(a.u + (int64_t)n * a.IC + 16 * ar + 4 * q));
-                b[nb][0] = dup_half_lo(v.x);
-                b[nb][1] = dup_half_hi(v.x);
-                b[nb][2] = dup_half_lo(v.y);
-                b[nb][3] = dup_half_hi(v.y);
-            }
-
-            QuarterStream<K> st;
-            st.build(w, quarter_prev_word(w[2 * K - 1], lane));
+        for (int j = 0; j < 8; j++)
 #pragma unroll
-            for (int rp = 0; rp < 2; rp++) {
+            for (int nb = 0; nb < NB; nb++)
 #pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const int i0 = 32 * rp + 2 * j;
-                    const uint32_t z0 = trellis_hash(st.state(i0));
-                    const uint32_t z1 = trellis_hash(st.state(i0 + 1));
-                    const uint32_t z2 = trellis_hash(st.state(i0 + 16));
-                    const uint32_t z3 = trellis_hash(st.state(i0 + 17));
+                for (int r = 0; r < 4; r++) red[warp * FRAG + ((j * NB + nb) * 4 + r) * 32 + lane] = acc[j][nb][r];
+        __syncthreads();
+        for (int i = threadIdx.x; i < FRAG; i += blockDim.x) {
+            float sum = red[i];
 #pragma unroll
-                    for (int nb = 0; nb < NB; nb++)
-                        mma_16816(acc[j][nb], z0, z1, z2, z3, b[nb][2 * rp], b[nb][2 * rp + 1]);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 2 * K; i++) w[i] = wn[i];
+            for (int wv = 1; wv < kDecodeWarps; wv++) sum += red[wv * FRAG + i];
+            red[i] = sum;
         }
-
-        // ---- CTA reduction in fixed warp order (fragment order, conflict-free)
-        for (int wv = 0; wv < kDecodeWarps; wv++) {
-            if (warp == wv) {
-#pragma unroll
-                for (int j = 0; j < 8; j++)
-#pragma unroll
-                    for (int nb = 0; nb < NB; nb++)
-#pragma unroll
-                        for (int r = 0; r < 4; r++) {
-                            float &dst = sm.red[((j * NB + nb) * 4 + r) * 32 + lane];
-                            dst = (wv == 0) ? acc[j][nb][r] : dst + acc[j][nb][r];
-                        }
-            }
-            __syncthreads();
-        }
+        __syncthreads();
 
         // ---- split-K across CTAs
-        const int64_t x0 = (int64_t)G * A, x1 = (int64_t)(G + 1) * A - 1;
+        const int64_t x0 = (int64_t)gi * A, x1 = (int64_t)(gi + 1) * A - 1;
         const int c_first = (int)(((x0 + 1) * nCTA - 1) / total);
         const int c_last = (int)(((x1 + 1) * nCTA - 1) / total);
         bool do_epilogue = true;
         if (c_first != c_last) {
-            float *slot = a.partials + (int64_t)(c + G) * FRAG;
-            for (int i = threadIdx.x; i < FRAG; i += blockDim.x) slot[i] = sm.red[i];
+            float *slot = a.partials + (int64_t)(c + gi) * FRAG;
+            for (int i = threadIdx.x; i < FRAG; i += blockDim.x) slot[i] = red[i];
             __threadfence();
             __syncthreads();
             if (threadIdx.x == 0) {
-                const int prev = atomicAdd(a.counters + G, 1);
-                sm.last = (prev == c_last - c_first);
+                const int prev = atomicAdd(a.counters + gi, 1);
+                *s_last = (prev == c_last - c_first);
             }
             __syncthreads();
-            do_epilogue = sm.last;
+            do_epilogue = *s_last;
             if (do_epilogue) {
                 __threadfence();
                 for (int i = threadIdx.x; i < FRAG; i += blockDim.x) {
-                    float s = 0.f;
+                    float sum = 0.f;
                     for (int cc = c_first; cc <= c_last; cc++)
-                        s += __ldcg(a.partials + (int64_t)(cc + G) * FRAG + i);
-                    sm.red[i] = s;
+                        sum += __ldcg(a.partials + (int64_t)(cc + gi) * FRAG + i);
+                    red[i] = sum;
                 }
-                if (threadIdx.x == 0) a.counters[G] = 0;
+                if (threadIdx.x == 0) a.counters[gi] = 0;
                 __syncthreads();
             }
         }
 
-        // ---- epilogue: y = (Had128(v) * rout) * s_out -> bf16, one warp per token
+        // ---- epilogue: Had128 of each row's 128 columns, then the post-scales
         if (do_epilogue) {
             const int oc0 = G * kHad + 4 * lane;
-            const uint2 rv = __ldg(reinterpret_cast<const uint2 *>(a.rout + oc0));
-            const uint2 sv = __ldg(reinterpret_cast<const uint2 *>(a.s_out + oc0));
+            const uint2 rv = __ldg(reinterpret_cast<const uint2 *>(e.post + oc0));
+            uint2 sv = make_uint2(0x3C003C00u, 0x3C003C00u);
+            if (a.mode == kModeDense) sv = __ldg(reinterpret_cast<const uint2 *>(e.post2 + oc0));
             const uint32_t rs[2] = {rv.x, rv.y}, ss[2] = {sv.x, sv.y};
-            for (int n = warp; n < a.M; n += kDecodeWarps) {
+            for (int n = warp; n < e.nrows; n += kDecodeWarps) {
                 float v[4];
 #pragma unroll
-                for (int i = 0; i < 4; i++) v[i] = sm.red[frag_index<NB>(n, 4 * lane + i)];
+                for (int i = 0; i < 4; i++) v[i] = red[frag_index<NB>(n, 4 * lane + i)];
                 warp_fwht128(v, lane);
-                uint32_t o[2];
+                float y[4];
 #pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    float y0 = (v[2 * h] * kHadNorm) * f16_bits_to_f32((uint16_t)(rs[h] & 0xFFFFu));
-                    float y1 = (v[2 * h + 1] * kHadNorm) * f16_bits_to_f32((uint16_t)(rs[h] >> 16));
-                    y0 *= f16_bits_to_f32((uint16_t)(ss[h] & 0xFFFFu));
-                    y1 *= f16_bits_to_f32((uint16_t)(ss[h] >> 16));
-                    o[h] = (uint32_t)f32_to_bf16_bits(y0) | ((uint32_t)f32_to_bf16_bits(y1) << 16);
+                for (int i = 0; i < 4; i++) {
+                    const int h = i >> 1, sh = 16 * (i & 1);
+                    y[i] = (v[i] * kHadNorm) * f16_bits_to_f32((uint16_t)(rs[h] >> sh));
+                    if (a.mode == kModeDense) y[i] *= f16_bits_to_f32((uint16_t)(ss[h] >> sh));
                 }
-                *reinterpret_cast<uint2 *>(a.out + (int64_t)n * a.ldo + oc0) = make_uint2(o[0], o[1]);
+                if (a.mode == kModeDense) {
+                    const uint32_t o0 = (uint32_t)f32_to_bf16_bits(y[0]) | ((uint32_t)f32_to_bf16_bits(y[1]) << 16);
+                    const uint32_t o1 = (uint32_t)f32_to_bf16_bits(y[2]) | ((uint32_t)f32_to_bf16_bits(y[3]) << 16);
+                    *reinterpret_cast<uint2 *>(a.out + (int64_t)n * a.ldo + e.out_off + oc0) = make_uint2(o0, o1);
+                } else {
+                    *reinterpret_cast<float4 *>(a.out_rows + (e.out_off + n) * (int64_t)e.OC + oc0) =
+                        make_float4(y[0], y[1], y[2], y[3]);
+                }
             }
         }
-        __syncthreads();   // sm.red is reused by the next segment
+        __syncthreads();   // red and s_ent are reused by the next segment
         f += a_hi - a_lo;
     }
 }
 
-template <int K, int NB>
-static cudaError_t launch_decode_t(const DecodeGemmArgs &a, cudaStream_t s) {
+template <int NB, int KSET>
+static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t total_hint, cudaStream_t s) {
     static int occ = -1;
+    constexpr size_t smem = group_smem_bytes<NB>();
     if (occ < 0) {
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_gemm_kernel<K, NB>, 256, 0);
+        cudaError_t e = cudaFuncSetAttribute(group_gemm_kernel<NB, KSET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, group_gemm_kernel<NB, KSET>, 256, smem);
         if (e != cudaSuccess) return e;
         if (occ < 1) occ = 1;
     }
-    const int64_t total = (int64_t)(a.OC / kHad) * (a.IC / kTile);
+    GroupGemmArgs a = a0;
+    a.hash_xor = kHashXor;
     int64_t grid = (int64_t)device_info().sm_count * occ;
     if (grid > kDecodeMaxCtas) grid = kDecodeMaxCtas;
-    if (grid > total) grid = total;
-    decode_gemm_kernel<K, NB><<<(unsigned)grid, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    if (total_hint > 0 && grid > total_hint) grid = total_hint;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, group_gemm_kernel<NB, KSET>, a);
 }
 
-template <int K>
-static cudaError_t launch_decode_k(const DecodeGemmArgs &a, cudaStream_t s) {
-    const int nb = (a.M + 7) / 8;
-    switch (nb) {
-        case 1: return launch_decode_t<K, 1>(a, s);
-        case 2: return launch_decode_t<K, 2>(a, s);
-        case 3: return launch_decode_t<K, 3>(a, s);
-        case 4: return launch_decode_t<K, 4>(a, s);
-        default: return cudaErrorInvalidValue;
+template <int NB>
+static cudaError_t launch_group_nb(const GroupGemmArgs &a, int kset, bool pdl, int64_t total, cudaStream_t s) {
+    switch (kset) {
+        case 4: return launch_group_t<NB, 4>(a, pdl, total, s);
+        case 8: return launch_group_t<NB, 8>(a, pdl, total, s);
+        case 16: return launch_group_t<NB, 16>(a, pdl, total, s);
+        case 12: return launch_group_t<NB, 12>(a, pdl, total, s);
+        default: return launch_group_t<NB, 28>(a, pdl, total, s);
     }
 }
 
-cudaError_t launch_decode_gemm(const DecodeGemmArgs &a, cudaStream_t s) {
-    switch (a.K) {
-        case 2: return launch_decode_k<2>(a, s);
-        case 3: return launch_decode_k<3>(a, s);
-        case 4: return launch_decode_k<4>(a, s);
+size_t group_slab_floats(int max_groups, int nb) {
+    return (size_t)(kDecodeMaxCtas + max_groups) * (8 * nb * 4 * 32);
+}
+
+cudaError_t launch_group_gemm(const GroupGemmArgs &a, int nb, bool pdl, cudaStream_t s) {
+    // total units when known on the host (dense): never launch more CTAs than units
+    int64_t total = -1;
+    int kset = 28;
+    if (!a.n_entries_dev) {
+        int64_t groups = 0;
+        kset = 0;
+        for (int i = 0; i < a.n_inline; i++) {
+            groups += a.inline_e[i].OC / kHad;
+            kset |= 1 << a.inline_e[i].K;
+        }
+        total = groups * (a.IC / kTile);
+    }
+    if (nb == 3) nb = 4;
+    switch (nb) {
+        case 1: return launch_group_nb<1>(a, kset, pdl, total, s);
+        case 2: return launch_group_nb<2>(a, kset, pdl, total, s);
+        case 4: return launch_group_nb<4>(a, kset, pdl, total, s);
         default: return cudaErrorInvalidValue;
     }
 }

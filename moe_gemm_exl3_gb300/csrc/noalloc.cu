@@ -34,7 +34,7 @@ constexpr int32_t kNaMaxGroups = kNaMaxOC / 128;
 constexpr size_t kNaHeader = 256;
 constexpr size_t kNaCounters = (size_t)kNaMaxGroups * sizeof(int32_t);
 constexpr size_t kNaU = (size_t)kNaMaxM * kNaMaxIC * sizeof(uint16_t);
-constexpr size_t kNaSlab = (size_t)(kDecodeMaxCtas + kNaMaxGroups) * (8 * 1 * 4 * 32) * sizeof(float);
+constexpr size_t kNaSlab = (size_t)(kDecodeMaxCtas + kNaMaxGroups) * (8 * 1 * 4 * 32) * sizeof(float);  // NB = 1
 constexpr size_t kNaBytes = kNaHeader + kNaCounters + kNaU + kNaSlab;   // 6.8 MB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaBytes];
@@ -99,20 +99,26 @@ extern "C" exl3_status exl3_linear_into_noalloc(const uint16_t *x, int64_t M, in
     if (e != cudaSuccess) return cuda_fail(e, "linear_into_noalloc: clear counters");
     e = launch_pretransform(x, M, IC, s_in, rin, u, s);
     if (e != cudaSuccess) return cuda_fail(e, "linear_into_noalloc: pretransform");
-    DecodeGemmArgs a;
+    GroupGemmArgs a = {};
     a.u = u;
-    a.code = code;
     a.IC = IC;
-    a.OC = OC;
-    a.K = K;
-    a.M = (int)M;
-    a.rout = rout;
-    a.s_out = s_out;
-    a.out = out + col0;
+    a.mode = kModeDense;
+    a.n_inline = 1;
+    GroupEntry &ge = a.inline_e[0];
+    ge.code = code;
+    ge.post = rout;
+    ge.post2 = s_out;
+    ge.out_off = col0;
+    ge.K = K;
+    ge.OC = OC;
+    ge.u_row0 = 0;
+    ge.nrows = (int32_t)M;
+    ge.g0 = 0;
+    a.out = out;
     a.ldo = ldo;
     a.partials = slab;
     a.counters = counters;
-    e = launch_decode_gemm(a, s);
+    e = launch_group_gemm(a, 1, false, s);
     if (e != cudaSuccess) return cuda_fail(e, "linear_into_noalloc: decode gemm");
     return EXL3_OK;
 }

@@ -194,3 +194,26 @@ def test_errors_are_reported_not_launched():
     # M == 0 is a no-op
     m.exl3_linear(xd[:0], c, 2, *sc, ws)
     assert m.exl3_workspace_error(ws) == 0
+
+
+@pytest.mark.parametrize("M", (1, 8, 20, 40))
+def test_shards_call_equals_per_shard_calls(M):
+    # a merged layer in one call gives the per-shard result (three shards, different K and OC)
+    g = syn.rng(70 + M)
+    IC = 1024
+    shards = [syn.make_shard(g, IC, OC, K) for OC, K in ((384, 2), (640, 3), (256, 4))]
+    x = syn.normal_bf16(g, M, IC)
+    ldo = sum(s.OC for s in shards) + 64
+    xd = dev(x, torch.bfloat16)
+    dsh = [(*shard_dev(s)[:1], s.K, *shard_dev(s)[1:]) for s in shards]
+    ws = m.workspace(m.exl3_linear_shards_workspace_bytes(M, IC, dsh))
+    got = torch.full((M, ldo), NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    m.exl3_linear_into_shards(xd, dsh, got, ws)
+    torch.cuda.synchronize()
+    b = bits(got)
+    assert np.all(b[:, ldo - 64:] == NAN_BF16)
+    col = 0
+    for s in shards:
+        ref = oracle.linear_f64(x, s.code, s.K, s.s_in, s.rin, s.rout, s.s_out)
+        assert_rows_close(as_f64(got)[:, col:col + s.OC], ref)
+        col += s.OC
