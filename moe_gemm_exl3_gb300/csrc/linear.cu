@@ -274,7 +274,11 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
         for (int i = 0; i < n_entries; i++) n_groups += a.inline_e[i].OC / kHad;
     }
     const int64_t total = (int64_t)n_groups * A;
-    const int nCTA = gridDim.x, c = blockIdx.x;
+    // every CTA of the partition must own at least one unit (an empty range would
+    // never arrive at its group's counter): with fewer units than CTAs the extra
+    // CTAs leave
+    const int nCTA = (int64_t)gridDim.x < total ? (int)gridDim.x : (int)total, c = blockIdx.x;
+    if (c >= nCTA) return;
     int64_t f = (int64_t)c * total / nCTA;
     const int64_t f_end = (int64_t)(c + 1) * total / nCTA;
     const uint32_t hx = a.hash_xor;

@@ -1,25 +1,414 @@
-// moe.cu -- grouped MoE over an EXL3 expert bank (bank.py layout).
+// moe.cu -- grouped SiLU-gated MoE over an EXL3 expert bank (bank.py layout:
+// w13 = [w1 | w3] per K-sorted slot, w2, fp16 suh/svh vectors [E, ...]).
+//
+// Launch chain, all on the caller's stream, no host synchronization:
+//   route     ids -> expert-sorted rows (stable counting sort), per-row slot,
+//             per-pair row position, and the grouped-GEMM entry lists
+//   rotate    u1[r] = Had(x_t * w13_suh[p][0]), u3[r] = Had(x_t * w13_suh[p][1])
+//   FC1       grouped trellis GEMM over (slot, row block) x {w1, w3}, epilogue
+//             Had(v) * w13_svh -> fp32 rows
+//   act       h = silu(g) * u, then FC2's input transform Had(h * w2_suh[p])
+//   FC2       grouped trellis GEMM over (slot, row block), epilogue
+//             Had(v) * w2_svh -> fp32 rows
+//   combine   y_t = sum over k (in order) of w[t][k] * d[pos(t,k)] -> bf16
 #include <cuda_runtime.h>
 
 #include "../../include/exl3.h"
+#include "common.cuh"
 #include "internal.h"
 
 namespace exl3 {
 exl3_status fail(exl3_status st, const char *fmt, ...);
-}
+exl3_status cuda_fail(cudaError_t e, const char *where);
+void trace(const char *fmt, ...);
+size_t fixed_workspace_bytes();
+int32_t *workspace_err(void *base);
+int32_t *workspace_counters(void *base);
+}  // namespace exl3
+
 using namespace exl3;
+
+namespace {
+
+constexpr int kMoeMaxE = 1024;
+constexpr int kMoeMaxTopk = 32;
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Rows per grouped-GEMM entry: an expert gets at most T rows (a token routes to
+// an expert at most once), so small batches need only small row blocks.
+int moe_nb(int T) { return T <= 8 ? 1 : (T <= 16 ? 2 : 4); }
+
+struct MoeLayout {
+    size_t pos, row_pair, row_slot, counts, ent1, ent2, u13, st1, h2, st2, slab, total;
+    int R, chunk, max_entries, nb;
+};
+
+MoeLayout moe_layout(int T, int H, int I, int E, int topk) {
+    MoeLayout L = {};
+    L.R = T * topk;
+    L.nb = moe_nb(T);
+    L.chunk = 8 * L.nb;
+    const int active = E < L.R ? E : L.R;
+    L.max_entries = (L.R + L.chunk - 1) / L.chunk + active;
+    size_t off = fixed_workspace_bytes();
+    auto take = [&](size_t bytes) { size_t o = off; off = align256(off + bytes); return o; };
+    L.pos = take(sizeof(int32_t) * L.R);
+    L.row_pair = take(sizeof(int32_t) * L.R);
+    L.row_slot = take(sizeof(int32_t) * L.R);
+    L.counts = take(sizeof(int32_t) * 4);                     // rows, entries FC1, entries FC2
+    L.ent1 = take(sizeof(GroupEntry) * 2 * L.max_entries);
+    L.ent2 = take(sizeof(GroupEntry) * L.max_entries);
+    L.u13 = take(sizeof(uint16_t) * 2 * (size_t)L.R * H);
+    L.st1 = take(sizeof(float) * 2 * (size_t)L.R * I);
+    L.h2 = take(sizeof(uint16_t) * (size_t)L.R * I);
+    L.st2 = take(sizeof(float) * (size_t)L.R * H);
+    const int groups1 = 2 * L.max_entries * (I / kHad), groups2 = L.max_entries * (H / kHad);
+    L.slab = take(sizeof(float) * group_slab_floats(groups1 > groups2 ? groups1 : groups2, L.nb));
+    L.total = off;
+    return L;
+}
+
+// ------------------------------------------------------------------ top-k
+// One thread per token: the topk largest logits (ties: lower expert id), then
+// softmax over the selected logits.
+__global__ void topk_softmax_kernel(const float *__restrict__ logits, int T, int E, int topk,
+                                    int32_t *__restrict__ ids, float *__restrict__ w) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    const float *l = logits + (int64_t)t * E;
+    uint32_t used[kMoeMaxE / 32];
+    for (int i = 0; i < (E + 31) / 32; i++) used[i] = 0;
+    float sel[kMoeMaxTopk];
+    for (int k = 0; k < topk; k++) {
+        int best = -1;
+        float bv = 0.f;
+        for (int e = 0; e < E; e++) {
+            if (used[e >> 5] & (1u << (e & 31))) continue;
+            const float v = __ldg(l + e);
+            if (best < 0 || v > bv) { best = e; bv = v; }
+        }
+        used[best >> 5] |= 1u << (best & 31);
+        ids[(int64_t)t * topk + k] = best;
+        sel[k] = bv;
+    }
+    float den = 0.f;
+    for (int k = 0; k < topk; k++) den += expf(sel[k] - sel[0]);
+    for (int k = 0; k < topk; k++) w[(int64_t)t * topk + k] = expf(sel[k] - sel[0]) / den;
+}
+
+// ------------------------------------------------------------------ route
+struct RouteArgs {
+    const int32_t *ids;
+    int R, topk, E, H, I, chunk;
+    exl3_moe_bank bank;
+    int32_t *pos, *row_pair, *row_slot, *counts;
+    GroupEntry *ent1, *ent2;
+    int32_t *err;
+};
+
+// One CTA of 1024 threads.  Rows of one slot are ordered by pair index (stable),
+// so the row -> entry assignment, and with it every partial sum, is the same on
+// every run.
+__global__ void __launch_bounds__(1024) route_kernel(const RouteArgs a) {
+    __shared__ int cnt[kMoeMaxE], base[kMoeMaxE], ebase[kMoeMaxE], cursor[kMoeMaxE];
+    const int tid = threadIdx.x;
+    for (int p = tid; p < a.E; p += blockDim.x) { cnt[p] = 0; cursor[p] = 0; }
+    __syncthreads();
+    for (int i = tid; i < a.R; i += blockDim.x) {
+        const int e = a.ids[i];
+        int p = -1;
+        if (e >= 0 && e < a.E) p = a.bank.perm[e];
+        if (p >= 0 && p < a.E) {
+            const int kg = a.bank.k_gu[p], kd = a.bank.k_d[p];
+            if (kg < 2 || kg > 4 || kd < 2 || kd > 4) p = -1;
+        } else {
+            p = -1;
+        }
+        if (p < 0) record_error(a.err, kErrBadExpertId);
+        else atomicAdd(&cnt[p], 1);
+        a.row_slot[i] = p;   // scratch: slot per pair (overwritten below with slot per row)
+    }
+    __syncthreads();
+    if (tid == 0) {   // E <= 1024 slots: a serial scan is a few microseconds at most
+        int rows = 0, chunks = 0;
+        for (int p = 0; p < a.E; p++) {
+            base[p] = rows;
+            ebase[p] = chunks;
+            rows += cnt[p];
+            chunks += (cnt[p] + a.chunk - 1) / a.chunk;
+        }
+        a.counts[0] = rows;
+        a.counts[1] = 2 * chunks;
+        a.counts[2] = chunks;
+    }
+    __syncthreads();
+    // stable positions: warp 0 walks the pairs 32 at a time
+    if (tid < 32) {
+        const unsigned lt = (1u << tid) - 1u;
+        for (int i0 = 0; i0 < a.R; i0 += 32) {
+            const int i = i0 + tid;
+            const int p = i < a.R ? a.row_slot[i] : -2;
+            const unsigned peers = __match_any_sync(kFull, p);
+            const int rank = __popc(peers & lt);
+            int position = -1;
+            if (p >= 0) position = base[p] + cursor[p] + rank;
+            __syncwarp();
+            if (p >= 0 && (peers & lt) == 0) cursor[p] += __popc(peers);
+            __syncwarp();
+            if (i < a.R) a.pos[i] = position;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < a.R; i += blockDim.x) {
+        const int r = a.pos[i];
+        if (r >= 0) a.row_pair[r] = i;
+    }
+    __syncthreads();
+    // slot per row (after every pair read its slot above)
+    for (int i = tid; i < a.R; i += blockDim.x) {
+        const int r = a.pos[i];
+        const int e = a.ids[i];
+        if (r >= 0) a.row_slot[r] = a.bank.perm[e];
+    }
+    // grouped-GEMM entries: one per (slot, block of `chunk` rows); FC1 has a w1 and a w3 entry
+    for (int p = tid; p < a.E; p += blockDim.x) {
+        const int n = cnt[p];
+        for (int c = 0; c * a.chunk < n; c++) {
+            const int r0 = base[p] + c * a.chunk;
+            const int nr = n - c * a.chunk < a.chunk ? n - c * a.chunk : a.chunk;
+            const int idx = ebase[p] + c;
+            for (int j = 0; j < 2; j++) {
+                GroupEntry ge = {};
+                ge.code = a.bank.w13 + (j == 0 ? a.bank.off_w1[p] : a.bank.off_w3[p]);
+                ge.post = a.bank.w13_svh + ((int64_t)p * 2 + j) * a.I;
+                ge.post2 = nullptr;
+                ge.K = a.bank.k_gu[p];
+                ge.OC = a.I;
+                ge.u_row0 = j * a.R + r0;
+                ge.out_off = j * a.R + r0;
+                ge.nrows = nr;
+                a.ent1[2 * idx + j] = ge;
+            }
+            GroupEntry ge = {};
+            ge.code = a.bank.w2 + a.bank.off_w2[p];
+            ge.post = a.bank.w2_svh + (int64_t)p * a.H;
+            ge.post2 = nullptr;
+            ge.K = a.bank.k_d[p];
+            ge.OC = a.H;
+            ge.u_row0 = r0;
+            ge.out_off = r0;
+            ge.nrows = nr;
+            a.ent2[idx] = ge;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ rotate
+// One warp per (row, projection j, 128-block): u[j*R + r] = Had(x_t * suh[p][j]).
+__global__ void __launch_bounds__(256) rotate_kernel(const uint16_t *__restrict__ x, int H, int R, int topk,
+                                                     const uint16_t *__restrict__ suh,
+                                                     const int32_t *__restrict__ row_pair,
+                                                     const int32_t *__restrict__ row_slot,
+                                                     const int32_t *__restrict__ counts,
+                                                     uint16_t *__restrict__ u) {
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int lane = threadIdx.x & 31;
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int blocks = H / kHad;
+    const int rows = counts[0];
+    if (wid >= (int64_t)2 * R * blocks) return;
+    const int j = (int)(wid / ((int64_t)R * blocks));
+    const int64_t rem = wid % ((int64_t)R * blocks);
+    const int r = (int)(rem / blocks);
+    if (r >= rows) return;
+    const int c0 = (int)(rem % blocks) * kHad + 4 * lane;
+    const int t = row_pair[r] / topk;
+    const int p = row_slot[r];
+    const uint2 xv = *reinterpret_cast<const uint2 *>(x + (int64_t)t * H + c0);
+    const uint2 sv = __ldg(reinterpret_cast<const uint2 *>(suh + ((int64_t)p * 2 + j) * H + c0));
+    const uint32_t xs[2] = {xv.x, xv.y}, ss[2] = {sv.x, sv.y};
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+        v[i] = bf16_bits_to_f32((xs[i >> 1] >> (16 * (i & 1))) & 0xFFFFu) *
+               f16_bits_to_f32((uint16_t)(ss[i >> 1] >> (16 * (i & 1))));
+    warp_fwht128(v, lane);
+    uint2 o;
+    o.x = (uint32_t)f32_to_f16_bits(v[0] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[1] * kHadNorm) << 16);
+    o.y = (uint32_t)f32_to_f16_bits(v[2] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[3] * kHadNorm) << 16);
+    *reinterpret_cast<uint2 *>(u + ((int64_t)j * R + r) * H + c0) = o;
+}
+
+// ------------------------------------------------------------------ act
+// One warp per (row, 128-block of I): h = silu(g) * u, then FC2's input
+// transform h2 = Had(h * w2_suh[p]).  g and u already carry their output Had
+// and svh scale (FC1 epilogue).
+__global__ void __launch_bounds__(256) act_kernel(const float *__restrict__ st1, int I, int R,
+                                                  const uint16_t *__restrict__ w2_suh,
+                                                  const int32_t *__restrict__ row_slot,
+                                                  const int32_t *__restrict__ counts,
+                                                  uint16_t *__restrict__ h2) {
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int lane = threadIdx.x & 31;
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int blocks = I / kHad;
+    const int rows = counts[0];
+    const int r = (int)(wid / blocks);
+    if (r >= rows || r >= R) return;
+    const int c0 = (int)(wid % blocks) * kHad + 4 * lane;
+    const int p = row_slot[r];
+    const float4 g = *reinterpret_cast<const float4 *>(st1 + (int64_t)r * I + c0);
+    const float4 uu = *reinterpret_cast<const float4 *>(st1 + ((int64_t)R + r) * I + c0);
+    const uint2 sv = __ldg(reinterpret_cast<const uint2 *>(w2_suh + (int64_t)p * I + c0));
+    const float gv[4] = {g.x, g.y, g.z, g.w}, uv[4] = {uu.x, uu.y, uu.z, uu.w};
+    const uint32_t ss[2] = {sv.x, sv.y};
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float silu = gv[i] / (1.0f + __expf(-gv[i]));
+        v[i] = (silu * uv[i]) * f16_bits_to_f32((uint16_t)(ss[i >> 1] >> (16 * (i & 1))));
+    }
+    warp_fwht128(v, lane);
+    uint2 o;
+    o.x = (uint32_t)f32_to_f16_bits(v[0] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[1] * kHadNorm) << 16);
+    o.y = (uint32_t)f32_to_f16_bits(v[2] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[3] * kHadNorm) << 16);
+    *reinterpret_cast<uint2 *>(h2 + (int64_t)r * I + c0) = o;
+}
+
+// ------------------------------------------------------------------ combine
+// One warp per (token, 128-block of H): y_t = sum_k w[t][k] * d[pos(t, k)],
+// k in order; routes whose expert id was invalid contribute nothing.
+__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ st2, int H, int T, int topk,
+                                                      const float *__restrict__ w,
+                                                      const int32_t *__restrict__ pos,
+                                                      uint16_t *__restrict__ y) {
+    const int lane = threadIdx.x & 31;
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int blocks = H / kHad;
+    const int t = (int)(wid / blocks);
+    if (t >= T) return;
+    const int c0 = (int)(wid % blocks) * kHad + 4 * lane;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < topk; k++) {
+        const int r = pos[(int64_t)t * topk + k];
+        if (r < 0) continue;
+        const float wk = w[(int64_t)t * topk + k];
+        const float4 d = *reinterpret_cast<const float4 *>(st2 + (int64_t)r * H + c0);
+        acc[0] += wk * d.x;
+        acc[1] += wk * d.y;
+        acc[2] += wk * d.z;
+        acc[3] += wk * d.w;
+    }
+    uint2 o;
+    o.x = (uint32_t)f32_to_bf16_bits(acc[0]) | ((uint32_t)f32_to_bf16_bits(acc[1]) << 16);
+    o.y = (uint32_t)f32_to_bf16_bits(acc[2]) | ((uint32_t)f32_to_bf16_bits(acc[3]) << 16);
+    *reinterpret_cast<uint2 *>(y + (int64_t)t * H + c0) = o;
+}
+
+inline unsigned warp_grid(int64_t warps) { return (unsigned)((warps + 7) / 8); }
+
+}  // namespace
 
 extern "C" {
 
-exl3_status exl3_moe_topk_softmax(const float *, int32_t, int32_t, int32_t, int32_t *, float *, exl3_stream) {
-    return fail(EXL3_EUNSUPPORTED, "moe_topk_softmax: not built yet");
+exl3_status exl3_moe_topk_softmax(const float *logits, int32_t T, int32_t E, int32_t topk, int32_t *ids, float *w,
+                                  exl3_stream stream) {
+    if (T < 0 || E < 1 || E > kMoeMaxE || topk < 1 || topk > kMoeMaxTopk || topk > E)
+        return fail(EXL3_EINVAL, "moe_topk_softmax: T = %d, E = %d (1..%d), topk = %d (1..%d, <= E)", T, E,
+                    kMoeMaxE, topk, kMoeMaxTopk);
+    if (T == 0) return EXL3_OK;
+    if (!logits || !ids || !w) return fail(EXL3_EINVAL, "moe_topk_softmax: null pointer");
+    topk_softmax_kernel<<<(T + 127) / 128, 128, 0, (cudaStream_t)stream>>>(logits, T, E, topk, ids, w);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "moe_topk_softmax");
+    return EXL3_OK;
 }
 
-size_t exl3_moe_workspace_bytes(int32_t, int32_t, int32_t, int32_t, int32_t) { return 0; }
+size_t exl3_moe_workspace_bytes(int32_t T, int32_t H, int32_t I, int32_t E, int32_t topk) {
+    if (T < 0 || H <= 0 || I <= 0 || H % 128 || I % 128 || E < 1 || E > kMoeMaxE || topk < 1 ||
+        topk > kMoeMaxTopk)
+        return 0;
+    return moe_layout(T, H, I, E, topk).total;
+}
 
-exl3_status exl3_moe_grouped(const uint16_t *, int32_t, int32_t, int32_t, int32_t, int32_t, const int32_t *,
-                             const float *, const exl3_moe_bank *, uint16_t *, void *, size_t, exl3_stream) {
-    return fail(EXL3_EUNSUPPORTED, "moe_grouped: not built yet");
+exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I, int32_t E, int32_t topk,
+                             const int32_t *ids, const float *w, const exl3_moe_bank *bank, uint16_t *y, void *wsp,
+                             size_t ws_bytes, exl3_stream stream) {
+    const char *fn = "moe_grouped";
+    if (T < 0 || H <= 0 || I <= 0 || H % 128 || I % 128)
+        return fail(EXL3_EINVAL, "%s: T = %d, H = %d, I = %d (H and I positive multiples of 128)", fn, T, H, I);
+    if (E < 1 || E > kMoeMaxE || topk < 1 || topk > kMoeMaxTopk)
+        return fail(EXL3_EINVAL, "%s: E = %d (1..%d), topk = %d (1..%d)", fn, E, kMoeMaxE, topk, kMoeMaxTopk);
+    if ((int64_t)T * topk > (1 << 24)) return fail(EXL3_EINVAL, "%s: T * topk = %lld routes is too many", fn,
+                                                   (long long)T * topk);
+    if (T == 0) return EXL3_OK;
+    if (!x || !ids || !w || !y || !bank) return fail(EXL3_EINVAL, "%s: null pointer", fn);
+    const exl3_moe_bank &b = *bank;
+    if (!b.w13 || !b.w2 || !b.off_w1 || !b.off_w3 || !b.off_w2 || !b.perm || !b.k_gu || !b.k_d || !b.w13_suh ||
+        !b.w13_svh || !b.w2_suh || !b.w2_svh)
+        return fail(EXL3_EINVAL, "%s: null pointer in the expert bank", fn);
+    if ((((uintptr_t)x | (uintptr_t)y | (uintptr_t)b.w13 | (uintptr_t)b.w2) & 15u) ||
+        (((uintptr_t)b.w13_suh | (uintptr_t)b.w13_svh | (uintptr_t)b.w2_suh | (uintptr_t)b.w2_svh) & 7u))
+        return fail(EXL3_EINVAL, "%s: x, y and the code banks must be 16-byte aligned, scale vectors 8-byte", fn);
+    const MoeLayout L = moe_layout(T, H, I, E, topk);
+    if (!wsp || (reinterpret_cast<uintptr_t>(wsp) & 255u) || ws_bytes < L.total)
+        return fail(EXL3_EWORKSPACE, "%s: workspace %p of %zu bytes; this call needs %zu bytes, 256-byte aligned",
+                    fn, wsp, ws_bytes, L.total);
+    char *base = static_cast<char *>(wsp);
+    int32_t *err = workspace_err(wsp);
+    int32_t *counters = workspace_counters(wsp);
+    int32_t *pos = reinterpret_cast<int32_t *>(base + L.pos);
+    int32_t *row_pair = reinterpret_cast<int32_t *>(base + L.row_pair);
+    int32_t *row_slot = reinterpret_cast<int32_t *>(base + L.row_slot);
+    int32_t *counts = reinterpret_cast<int32_t *>(base + L.counts);
+    GroupEntry *ent1 = reinterpret_cast<GroupEntry *>(base + L.ent1);
+    GroupEntry *ent2 = reinterpret_cast<GroupEntry *>(base + L.ent2);
+    uint16_t *u13 = reinterpret_cast<uint16_t *>(base + L.u13);
+    float *st1 = reinterpret_cast<float *>(base + L.st1);
+    uint16_t *h2 = reinterpret_cast<uint16_t *>(base + L.h2);
+    float *st2 = reinterpret_cast<float *>(base + L.st2);
+    float *slab = reinterpret_cast<float *>(base + L.slab);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int R = L.R;
+
+    RouteArgs ra = {ids, R, topk, E, H, I, L.chunk, b, pos, row_pair, row_slot, counts, ent1, ent2, err};
+    route_kernel<<<1, 1024, 0, s>>>(ra);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "moe_grouped: route");
+
+    rotate_kernel<<<warp_grid((int64_t)2 * R * (H / kHad)), 256, 0, s>>>(x, H, R, topk, b.w13_suh, row_pair,
+                                                                         row_slot, counts, u13);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "moe_grouped: rotate");
+
+    GroupGemmArgs g1 = {};
+    g1.u = u13;
+    g1.IC = H;
+    g1.mode = kModeRows;
+    g1.entries = ent1;
+    g1.n_entries_dev = counts + 1;
+    g1.n_groups_per_entry = I / kHad;
+    g1.out_rows = st1;
+    g1.partials = slab;
+    g1.counters = counters;
+    if ((e = launch_group_gemm(g1, L.nb, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC1");
+
+    act_kernel<<<warp_grid((int64_t)R * (I / kHad)), 256, 0, s>>>(st1, I, R, b.w2_suh, row_slot, counts, h2);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "moe_grouped: act");
+
+    GroupGemmArgs g2 = g1;
+    g2.u = h2;
+    g2.IC = I;
+    g2.entries = ent2;
+    g2.n_entries_dev = counts + 2;
+    g2.n_groups_per_entry = H / kHad;
+    g2.out_rows = st2;
+    if ((e = launch_group_gemm(g2, L.nb, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC2");
+
+    combine_kernel<<<warp_grid((int64_t)T * (H / kHad)), 256, 0, s>>>(st2, H, T, topk, w, pos, y);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "moe_grouped: combine");
+    trace("moe_grouped T=%d H=%d I=%d E=%d topk=%d rows<=%d nb=%d", T, H, I, E, topk, R, L.nb);
+    return EXL3_OK;
 }
 
 }  // extern "C"

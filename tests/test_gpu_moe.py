@@ -1,0 +1,128 @@
+"""GPU parity of the grouped EXL3 MoE layer against the CPU oracle, through the C ABI.
+
+Expert bank layout from bank.py (w13 = [w1 | w3] per K-sorted slot, w2, fp16
+suh/svh vectors); SiLU-gated FFN; top-k routing with softmax weights.  Outputs
+must satisfy max|y - y_ref| <= 2e-2 * rms(y_ref) per token.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+from tests._util import as_f64, assert_rows_close, bits, dev
+
+pytestmark = pytest.mark.gpu
+m = pytest.importorskip("moe_gemm_exl3_gb300")
+
+_DT = dict(w13=torch.int16, w2=torch.int16, off_w1=torch.int64, off_w3=torch.int64, off_w2=torch.int64,
+           perm=torch.int32, k_gu=torch.int32, k_d=torch.int32, w13_suh=torch.float16,
+           w13_svh=torch.float16, w2_suh=torch.float16, w2_svh=torch.float16)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_gemm_exl3_gb300 import build
+    build.build()
+
+
+def bank_dev(bank):
+    return {k: dev(v, _DT[k]) for k, v in bank.items()}
+
+
+def run_moe(x, ids, w, bank_d, E, H, I, ws=None):
+    T, topk = ids.shape
+    if ws is None:
+        ws = m.workspace(m.exl3_moe_workspace_bytes(T, H, I, E, topk))
+    y = m.exl3_moe_grouped(dev(x, torch.bfloat16), dev(ids, torch.int32), dev(w, torch.float32), bank_d, ws)
+    torch.cuda.synchronize()
+    return y, ws
+
+
+def test_topk_softmax_matches_oracle():
+    g = np.random.default_rng(3)
+    logits = g.standard_normal((300, 128)).astype(np.float32)
+    logits[7, [3, 90, 17]] = 9.0                 # ties: lower expert id first
+    ids, w = m.exl3_moe_topk_softmax(dev(logits, torch.float32), 8)
+    torch.cuda.synchronize()
+    rid, rw = oracle.topk_softmax(logits, 8)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("T", (1, 5, 20, 40))
+def test_moe_small_bank_mixed_k(T):
+    E, H, I, topk = 6, 256, 128, 3
+    bank = syn.moe_bank(11, E=E, H=H, I=I, distinct_down_k=True)
+    x, logits = syn.moe_tokens(12 + T, T, H=H, E=E)
+    ids, w = oracle.topk_softmax(logits, topk)
+    y, ws = run_moe(x, ids, w, bank_dev(bank), E, H, I)
+    assert_rows_close(as_f64(y), oracle.moe_f64(x, ids, w, bank))
+    assert m.exl3_workspace_error(ws) == 0
+
+
+@pytest.fixture(scope="module")
+def full_bank():
+    bank = syn.moe_bank(3)           # E = 128, H = 2048, I = 768, K per expert in {2, 3, 4}
+    return bank, bank_dev(bank)
+
+
+@pytest.mark.parametrize("T", (1, 16))
+def test_moe_full_geometry(full_bank, T):
+    bank, bank_d = full_bank
+    x, logits = syn.moe_tokens(20 + T, T)
+    ids, w = m.exl3_moe_topk_softmax(dev(logits, torch.float32), 8)
+    ids, w = ids.cpu().numpy(), w.cpu().numpy()
+    y, ws = run_moe(x, ids, w, bank_d, 128, 2048, 768)
+    assert_rows_close(as_f64(y), oracle.moe_f64(x, ids, w, bank))
+    assert m.exl3_workspace_error(ws) == 0
+
+
+def test_moe_full_geometry_512_tokens_sampled(full_bank):
+    bank, bank_d = full_bank
+    T = 512
+    x, logits = syn.moe_tokens(40, T)
+    ids, w = oracle.topk_softmax(logits, 8)
+    y, ws = run_moe(x, ids, w, bank_d, 128, 2048, 768)
+    got = as_f64(y)
+    assert np.all(np.isfinite(got))
+    sample = np.array([0, 1, 77, 200, 311, 450, 510, 511])
+    ref = oracle.moe_f64(np.ascontiguousarray(x[sample]), np.ascontiguousarray(ids[sample]),
+                         np.ascontiguousarray(w[sample]), bank)
+    assert_rows_close(got[sample], ref)
+
+
+def test_moe_deterministic(full_bank):
+    bank, bank_d = full_bank
+    x, logits = syn.moe_tokens(41, 37)
+    ids, w = oracle.topk_softmax(logits, 8)
+    y1, ws = run_moe(x, ids, w, bank_d, 128, 2048, 768)
+    y2, _ = run_moe(x, ids, w, bank_d, 128, 2048, 768, ws)
+    assert np.array_equal(bits(y1), bits(y2))
+
+
+def test_moe_invalid_expert_id_is_recorded_and_skipped():
+    E, H, I, topk = 6, 256, 128, 2
+    bank = syn.moe_bank(13, E=E, H=H, I=I)
+    x, logits = syn.moe_tokens(14, 4, H=H, E=E)
+    ids, w = oracle.topk_softmax(logits, topk)
+    bad = ids.copy()
+    bad[2, 1] = 99
+    y, ws = run_moe(x, bad, w, bank_dev(bank), E, H, I)
+    assert m.exl3_workspace_error(ws) == 2            # an expert id outside [0, E)
+    # the invalid route contributes nothing: same as a valid id with weight 0
+    w0 = w.copy()
+    w0[2, 1] = 0.0
+    assert_rows_close(as_f64(y), oracle.moe_f64(x, ids, w0, bank))
+
+
+def test_moe_zero_tokens_is_a_no_op():
+    E, H, I = 6, 256, 128
+    bank = syn.moe_bank(15, E=E, H=H, I=I)
+    ws = m.workspace(1 << 20)
+    y = torch.empty((0, H), dtype=torch.bfloat16, device="cuda")
+    m.exl3_moe_grouped(torch.empty((0, H), dtype=torch.bfloat16, device="cuda"),
+                       torch.empty((0, 2), dtype=torch.int32, device="cuda"),
+                       torch.empty((0, 2), dtype=torch.float32, device="cuda"), bank_dev(bank), ws, y=y)
