@@ -1,17 +1,327 @@
-// prefill.cu -- large-M (prefill) path.  Placeholder until the tensor-core kernel lands:
-// reports "not launched" so the caller keeps the decode-mode passes.
+// prefill.cu -- large-M (prefill) path of the EXL3 linear on the 5th-generation
+// tensor cores: y = (Had128(u @ W) * rout) * s_out for u fp16 [M][IC] and the
+// decoded weights W^T fp16 [OC][IC] (K-major), with a 128 x 256 output tile per
+// CTA accumulated in tensor memory.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: u and W^T tiles (64-element K slices, 128-byte
+//               swizzle) into a 4-stage shared-memory ring
+//   warp 1      TMEM allocation; one elected lane issues tcgen05.mma
+//               (M=128, N=256, K=16, fp16 in, fp32 accumulate)
+//   warps 2..5  epilogue: tcgen05.ld of one row per thread, in-register
+//               128-point Hadamard, rout then s_out, bf16 stores into the slice
+// Every mbarrier wait is bounded: on timeout the kernel records an error in the
+// workspace error word, drains what it issued (again bounded), frees its tensor
+// memory and returns.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
+#include "common.cuh"
 #include "internal.h"
 
 namespace exl3 {
 
-bool prefill_supported() { return false; }
+namespace {
 
-cudaError_t launch_prefill(const uint16_t *, const uint16_t *, int64_t, int, int, const uint16_t *,
-                           const uint16_t *, uint16_t *, int64_t, int32_t *, cudaStream_t, bool *launched) {
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;                 // 16 KB
+constexpr int B_BYTES = BN * BK * 2;                 // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* alignment */ + 256 /* barriers */;
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait: false (and the error recorded, abort raised) if the phase never completes.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t *err, volatile int *abort) {
+    for (uint32_t i = 0; i < kWaitLimit; i++) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+    }
+    record_error(err, kErrWaitTimeout);
+    *abort = 1;
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)(16 >> 4) << 16;                   // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                           // descriptor version
+    d |= (uint64_t)2 << 61;                           // swizzle: 128 B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M = 128, N = 256.
+constexpr uint32_t kIdesc = (1u << 4)                 // D format: f32
+                            | (0u << 7) | (0u << 10)  // A, B format: f16
+                            | ((uint32_t)(BN >> 3) << 17)
+                            | ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(da), "l"(db), "r"(kIdesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// ------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(192, 1)
+prefill_gemm_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_w,
+                    int M, int IC, int OC, const uint16_t *__restrict__ rout, const uint16_t *__restrict__ s_out,
+                    uint16_t *__restrict__ out, int64_t ldo, int32_t *err) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 1024-byte alignment for the swizzled tiles
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *sbase = smem_raw + (base - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + STAGES * STAGE_BYTES);
+    // bars[0..S) full, bars[S..2S) empty, bars[2S] accumulator ready
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 1);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+    int *s_issued = const_cast<int *>(reinterpret_cast<volatile int *>(s_tmem + 2));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+    const int nk = IC / BK;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; i++) {
+            mbar_init(smem_u32(&bars[i]), 1);
+            mbar_init(smem_u32(&bars[STAGES + i]), 1);
+        }
+        mbar_init(smem_u32(&bars[2 * STAGES]), 1);
+        *s_abort = 0;
+        *s_issued = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_tmem)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer
+        int kb = 0;
+        for (; kb < nk; kb++) {
+            const int s = kb % STAGES;
+            const uint32_t ph = (kb / STAGES) & 1;
+            if (!mbar_wait(smem_u32(&bars[STAGES + s]), ph ^ 1, err, s_abort)) break;
+            const uint32_t full = smem_u32(&bars[s]);
+            mbar_expect_tx(full, STAGE_BYTES);
+            const uint32_t sa = base + s * STAGE_BYTES;
+            tma_load_2d(sa, &tm_u, kb * BK, m0, full);
+            tma_load_2d(sa + A_BYTES, &tm_w, kb * BK, n0, full);
+        }
+        *s_issued = kb;
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        for (int kb = 0; kb < nk; kb++) {
+            const int s = kb % STAGES;
+            const uint32_t ph = (kb / STAGES) & 1;
+            if (!mbar_wait(smem_u32(&bars[s]), ph, err, s_abort)) break;
+            tc_fence_after();
+            const uint32_t sa = base + s * STAGE_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / 16; k++) {
+                const uint64_t da = smem_desc_sw128(sa + k * 32);
+                const uint64_t db = smem_desc_sw128(sa + A_BYTES + k * 32);
+                umma_f16(tmem, da, db, (kb | k) != 0);
+            }
+            umma_commit(smem_u32(&bars[STAGES + s]));   // frees the stage when these MMAs finish
+        }
+        umma_commit(smem_u32(&bars[2 * STAGES]));       // accumulator complete (or drained on abort)
+    } else if (warp >= 2) {
+        // ---------------- epilogue: one output row per thread
+        const int quarter = warp & 3;                    // TMEM lanes this warp may access
+        const int row = quarter * 32 + lane;
+        const bool ok = mbar_wait(smem_u32(&bars[2 * STAGES]), 0, err, s_abort);
+        tc_fence_after();
+        const int m = m0 + row;
+        for (int h = 0; h < BN / kHad; h++) {
+            const int col = n0 + h * kHad;
+            if (col >= OC) break;
+            float v[128];
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                float t[32];
+                tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + h * kHad + c * 32, t);
+#pragma unroll
+                for (int i = 0; i < 32; i++) v[c * 32 + i] = t[i];
+            }
+            tmem_ld_wait();
+            if (!ok || *s_abort || m >= M) continue;
+#pragma unroll
+            for (int hs = 1; hs < 128; hs <<= 1) {
+#pragma unroll
+                for (int i = 0; i < 128; i++) {
+                    if (i & hs) continue;
+                    const float a = v[i], b = v[i + hs];
+                    v[i] = a + b;
+                    v[i + hs] = a - b;
+                }
+            }
+            uint16_t *dst = out + (int64_t)m * ldo + col;
+#pragma unroll
+            for (int c8 = 0; c8 < 16; c8++) {
+                // scale vectors are only 8-byte aligned
+                const uint2 r0 = __ldg(reinterpret_cast<const uint2 *>(rout + col) + 2 * c8);
+                const uint2 r1 = __ldg(reinterpret_cast<const uint2 *>(rout + col) + 2 * c8 + 1);
+                const uint2 q0 = __ldg(reinterpret_cast<const uint2 *>(s_out + col) + 2 * c8);
+                const uint2 q1 = __ldg(reinterpret_cast<const uint2 *>(s_out + col) + 2 * c8 + 1);
+                const uint32_t rw[4] = {r0.x, r0.y, r1.x, r1.y}, sw[4] = {q0.x, q0.y, q1.x, q1.y};
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int c = c8 * 8 + 2 * i;
+                    float y0 = (v[c] * kHadNorm) * f16_bits_to_f32((uint16_t)(rw[i] & 0xFFFFu));
+                    float y1 = (v[c + 1] * kHadNorm) * f16_bits_to_f32((uint16_t)(rw[i] >> 16));
+                    y0 *= f16_bits_to_f32((uint16_t)(sw[i] & 0xFFFFu));
+                    y1 *= f16_bits_to_f32((uint16_t)(sw[i] >> 16));
+                    o[i] = (uint32_t)f32_to_bf16_bits(y0) | ((uint32_t)f32_to_bf16_bits(y1) << 16);
+                }
+                reinterpret_cast<uint4 *>(dst)[c8] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0 && lane == 0 && *s_abort) {
+        // drain: wait (bounded) for the copies this CTA issued into stages nobody consumed
+        const int issued = *s_issued;
+        for (int kb = issued - STAGES > 0 ? issued - STAGES : 0; kb < issued; kb++) {
+            const uint32_t bar = smem_u32(&bars[kb % STAGES]);
+            for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(bar, (kb / STAGES) & 1); i++) {
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+    }
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D fp16 tensor [rows][cols] (cols contiguous), box [box_rows][64 cols], 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool prefill_supported() { return encode_fn() != nullptr; }
+
+cudaError_t launch_prefill(const uint16_t *u, const uint16_t *wt, int64_t M, int IC, int OC, const uint16_t *rout,
+                           const uint16_t *s_out, uint16_t *out, int64_t ldo, int32_t *err, cudaStream_t s,
+                           bool *launched) {
     *launched = false;
-    return cudaSuccess;
+    if (M <= 0 || IC % BK || OC % kHad || M > INT32_MAX) return cudaErrorInvalidValue;
+    if ((reinterpret_cast<uintptr_t>(u) | reinterpret_cast<uintptr_t>(wt)) & 15u) return cudaErrorInvalidValue;
+    CUtensorMap tm_u, tm_w;
+    if (!make_map(&tm_u, u, M, IC, BM) || !make_map(&tm_w, wt, OC, IC, BN)) return cudaErrorInvalidValue;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    dim3 grid((unsigned)((M + BM - 1) / BM), (unsigned)((OC + BN - 1) / BN));
+    prefill_gemm_kernel<<<grid, 192, SMEM_BYTES, s>>>(tm_u, tm_w, (int)M, IC, OC, rout, s_out, out, ldo, err);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) *launched = true;
+    return e;
 }
 
 }  // namespace exl3
