@@ -1,20 +1,25 @@
-"""Benchmark of the EXL3 trellis linear hot path on one GB300 (or N replicas).
+"""Benchmark of the EXL3 trellis hot path on one GB300 (or N replicas).
 
-Workload: the decode-shaped merged gate/up projection, hidden 5120 -> 2 x 17408,
-gate coded at K=2 and up at K=3, written into two column slices of one bf16
-out[M, 34816], M = 8 tokens (seeded synthetic data, uniform int16 code words).
-A step = both shards through the C ABI (pre-transform, fused trellis GEMM,
-output transform into the slice).  Metric: tokens/s (M per step); the roofline
-object reports the decode GEMM kernel's HBM bandwidth on code bytes.
+Default workload (the headline): the decode-shaped merged gate/up projection,
+hidden 5120 -> 2 x 17408, gate coded at K=2 and up at K=3, written into two
+column slices of one bf16 out[M, 34816], M = 8 tokens, seeded synthetic data.
+A step = one merged-layer call through the C ABI (pre-transform, grouped fused
+trellis GEMM, output transform into the slices).  Metric: tokens/s.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--m M] [--impl ours|reference]
+Other workloads (--workload): prefill (5120 -> 17408 at M = 8192, K per
+--k), moe (128 experts, H 2048, I 768, top-8, T tokens per --t), gather
+(8192 ids from a 248,320 x 5120 int8 table), layer (the five projections of a
+hidden-5120 decoder layer at --m rows).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload W] [--impl ours|reference]
 
 Under torchrun each rank runs an independent replica on its own GPU (the path
-shards without a data-path collective); value = all ranks' tokens / max time.
+shards without a data-path collective); value = all ranks' units / max time.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -28,18 +33,7 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-IC, OC, KS = 5120, 17408, (2, 3)
-METRIC = "EXL3 linear tokens/s (decode-shaped gate_up, M<=8)"
 L2_BYTES = 129 * 2 ** 20
-
-
-def code_bytes(K, ic=IC, oc=OC):
-    return ic * oc * K // 8
-
-
-def algorithmic_bytes(M, K, ic=IC, oc=OC):
-    """Bytes one decode GEMM launch must move: code words, activations in, bf16 out, scales."""
-    return code_bytes(K, ic, oc) + 2 * M * ic + 2 * M * oc + 2 * 2 * oc
 
 
 def peaks():
@@ -51,12 +45,14 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-# ------------------------------------------------------------------ dist
 def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def omp_threads():
+    n = os.environ.get("OMP_NUM_THREADS")
+    return int(n) if n else os.cpu_count()
 
 
 class Clocks:
@@ -66,9 +62,7 @@ class Clocks:
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
-        self.index = index
-        self.proc = None
-        self.lines = []
+        self.index, self.proc, self.lines = index, None, []
 
     def __enter__(self):
         try:
@@ -76,8 +70,7 @@ class Clocks:
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
+            threading.Thread(target=self._read, daemon=True).start()
         except OSError:
             self.proc = None
         return self
@@ -113,7 +106,409 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ------------------------------------------------------------------ ours
+def kernel_time_ms(torch, stream, fn, n):
+    """Mean duration of fn(j) (the launches of one call) from CUDA events on `stream`;
+    the stream is kept busy first so that no launch gap is measured."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(50_000_000)
+        for j in range(n):
+            evs[j][0].record(stream)
+            fn(j)
+            evs[j][1].record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs[n // 4:])
+
+
+def profile_traffic(name, src_files):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current sources."""
+    p = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    h = hashlib.sha256()
+    for s in src_files:
+        with open(os.path.join(ROOT, "moe_gemm_exl3_gb300", "csrc", s), "rb") as f:
+            h.update(f.read())
+    if d.get("source_sha256_16") != h.hexdigest()[:16]:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def t16(torch, a, dev, dtype):
+    a = np.ascontiguousarray(a)
+    if dtype in (torch.bfloat16, torch.float16):
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(dev).view(dtype)
+
+
+# ------------------------------------------------------------------ workloads
+class GateUp:
+    """Decode-shaped merged gate (K=2) / up (K=3) projection, 5120 -> 2 x 17408."""
+    IC, OC, KS = 5120, 17408, (2, 3)
+
+    def __init__(self, args):
+        self.M = args.m
+        self.metric = "EXL3 linear tokens/s (decode-shaped gate_up, M<=8)"
+        self.unit = "tokens/s"
+        self.units_per_step = self.M
+
+    def config(self):
+        return {"workload": f"gate_up 5120->2x17408, K=2|K=3, M={self.M}, out[M,34816]", "M": self.M,
+                "IC": self.IC, "OC_per_shard": self.OC, "K": list(self.KS)}
+
+    def code_bytes(self, K):
+        return self.IC * self.OC * K // 8
+
+    def setup(self, torch, m, syn, dev):
+        M, IC, OC = self.M, self.IC, self.OC
+        self.x, shards = syn.gate_up(1, M=M)
+        per_step = sum(self.code_bytes(K) for K in self.KS)
+        self.R = R = max(4, int(np.ceil(4 * L2_BYTES / per_step)))
+        codes = [[t16(torch, s.code, dev, torch.int16) for s in shards]]
+        for _ in range(R - 1):
+            codes.append([c.clone() for c in codes[0]])
+        scal = [[t16(torch, v, dev, torch.float16) for v in (s.s_in, s.rin, s.rout, s.s_out)] for s in shards]
+        self.sets = [[(codes[r][i], s.K, *scal[i], i * OC) for i, s in enumerate(shards)] for r in range(R)]
+        self.xd = t16(torch, self.x, dev, torch.bfloat16)
+        self.out = torch.empty((M, 2 * OC), dtype=torch.bfloat16, device=dev)
+        self.ws = m.workspace(m.exl3_linear_shards_workspace_bytes(M, IC, self.sets[0]), dev)
+        self.u = torch.empty((len(shards), M, IC), dtype=torch.float16, device=dev)
+        for i in range(len(shards)):
+            m.exl3_pretransform(self.xd, *scal[i][:2], u=self.u[i])
+        self.m = m
+        self.l2 = f"inputs larger than L2: {R} rotating code copies ({R * per_step / 1e6:.0f} MB)"
+        self.launches_per_step = 1 + (M + 31) // 32
+
+    def step(self, r, x=None):
+        self.m.exl3_linear_into_shards(self.xd if x is None else x, self.sets[r], self.out, self.ws)
+
+    def roofline(self, torch, stream):
+        R, m = self.R, self.m
+        ms = kernel_time_ms(torch, stream,
+                            lambda j: m.exl3_gemm_into_shards(self.u, self.sets[j % R], self.out, self.ws), 4 * R)
+        hbm, _, src = peaks()
+        alg = sum(self.code_bytes(K) + 2 * self.M * self.IC + 2 * self.M * self.OC + 2 * 2 * self.OC
+                  for K in self.KS)
+        a = alg / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "kernel": "group_gemm_kernel (gate K=2 + up K=3 in one launch)",
+                "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
+                "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
+                "traffic": profile_traffic("decode_gemm_gate_up_m8.json", ["linear.cu", "common.cuh"]),
+                "per_launch_us": round(ms * 1e3, 2), "algorithmic_bytes_per_launch": alg,
+                "code_GBps": round(sum(self.code_bytes(K) for K in self.KS) / (ms * 1e-3) / 1e9, 1)}
+
+    def e2e_io(self, torch, dev):
+        xh = torch.from_numpy(self.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+        oh = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        return xh, torch.empty_like(self.xd), oh, self.out
+
+    def cpu_sample(self, budget):
+        import oracle
+        import synthetic as syn
+        x, shards = syn.gate_up(1, M=self.M)
+        nblk_total = self.OC // 128
+        oracle.lib()
+        t0 = time.perf_counter()
+        for sh in shards:
+            oracle.linear_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=0, nblk=1)
+        per_blk = (time.perf_counter() - t0) / 2
+        nblk = int(min(nblk_total, max(1, budget / max(per_blk, 1e-6) / 2)))
+        t0 = time.perf_counter()
+        for sh in shards:
+            oracle.linear_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=0, nblk=nblk)
+        t = (time.perf_counter() - t0) * nblk_total / nblk
+        return self.M / t, (f"M={self.M}, output blocks 0..{nblk - 1} of {nblk_total} (128 columns each) of both "
+                            f"shards, scaled linearly to all {nblk_total} blocks")
+
+
+class Prefill:
+    """Prefill-shaped linear 5120 -> 17408 at M = 8192 (1 % outlier channels)."""
+    IC, OC = 5120, 17408
+
+    def __init__(self, args):
+        self.M, self.K = 8192, args.k
+        self.metric = "EXL3 linear TFLOP/s (prefill-shaped, M=8192)"
+        self.unit = "TFLOP/s"
+        self.units_per_step = 2.0 * self.M * self.IC * self.OC / 1e12
+
+    def config(self):
+        return {"workload": f"prefill 5120->17408, K={self.K}, M=8192, 1% outlier channels", "M": self.M,
+                "IC": self.IC, "OC": self.OC, "K": self.K}
+
+    def setup(self, torch, m, syn, dev):
+        self.x, sh = syn.prefill(2, M=self.M, K=self.K)
+        self.code = t16(torch, sh.code, dev, torch.int16)
+        self.sc = [t16(torch, v, dev, torch.float16) for v in (sh.s_in, sh.rin, sh.rout, sh.s_out)]
+        self.xd = t16(torch, self.x, dev, torch.bfloat16)
+        self.out = torch.empty((self.M, self.OC), dtype=torch.bfloat16, device=dev)
+        self.ws = m.workspace(m.exl3_linear_workspace_bytes(self.M, self.IC, self.OC), dev)
+        self.u = m.exl3_pretransform(self.xd, self.sc[0], self.sc[1])
+        self.m, self.R = m, 1
+        self.l2 = "inputs larger than L2 (u 84 MB, decoded weights 178 MB, out 285 MB)"
+        self.launches_per_step = 3      # pre-transform, reconstruct, tcgen05 GEMM
+
+    def step(self, r, x=None):
+        self.m.exl3_linear_into(self.xd if x is None else x, self.code, self.K, *self.sc, self.out, 0, self.ws)
+
+    def roofline(self, torch, stream):
+        m = self.m
+        W = torch.empty((self.IC, self.OC), dtype=torch.float16, device=self.out.device)
+        ms_all = kernel_time_ms(torch, stream, lambda j: m.exl3_gemm_into(self.u, self.code, self.K, *self.sc[2:],
+                                                                           self.out, 0, self.ws), 8)
+        ms_rec = kernel_time_ms(torch, stream, lambda j: m.exl3_reconstruct(self.code, self.K, W), 8)
+        ms = ms_all - ms_rec
+        _, tf, src = peaks()
+        fl = 2.0 * self.M * self.IC * self.OC
+        a = fl / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": "prefill_gemm_kernel (tcgen05 128x256 tiles)",
+                "achieved": round(a, 1), "peak": tf, "unit": "TFLOP/s", "frac": round(a / tf, 4),
+                "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops; fp16 has the same dense rate)",
+                "traffic": profile_traffic("prefill_gemm_m8192.json", ["prefill.cu"]),
+                "per_launch_us": round(ms * 1e3, 1), "reconstruct_us": round(ms_rec * 1e3, 1),
+                "algorithmic_flops_per_launch": fl}
+
+    def e2e_io(self, torch, dev):
+        xh = torch.from_numpy(self.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+        oh = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        return xh, torch.empty_like(self.xd), oh, self.out
+
+    def cpu_sample(self, budget):
+        import oracle
+        import synthetic as syn
+        x, sh = syn.prefill(2, M=self.M, K=self.K)
+        rows = 8
+        t0 = time.perf_counter()
+        oracle.linear_f64(np.ascontiguousarray(x[:rows]), sh.code, self.K, sh.s_in, sh.rin, sh.rout, sh.s_out)
+        t = time.perf_counter() - t0
+        flops = 2.0 * rows * self.IC * self.OC
+        return flops / t / 1e12, (f"{rows} of 8192 rows, all 17408 columns (the weights decoded once), "
+                                  f"TFLOP/s of the sample")
+
+
+class Moe:
+    """Grouped MoE: 128 experts, H 2048, I 768, top-8, per-expert K in {2, 3, 4}."""
+    H, I, E, TOPK = 2048, 768, 128, 8
+
+    def __init__(self, args):
+        self.T = args.t
+        self.metric = f"EXL3 grouped MoE tokens/s (T={self.T})"
+        self.unit = "tokens/s"
+        self.units_per_step = self.T
+
+    def config(self):
+        return {"workload": f"moe E=128 H=2048 I=768 top-8, T={self.T}, K per expert in {{2,3,4}}", "T": self.T}
+
+    def setup(self, torch, m, syn, dev):
+        import oracle
+        self.bank_np = syn.moe_bank(3)
+        dt = dict(w13=torch.int16, w2=torch.int16, off_w1=torch.int64, off_w3=torch.int64, off_w2=torch.int64,
+                  perm=torch.int32, k_gu=torch.int32, k_d=torch.int32, w13_suh=torch.float16,
+                  w13_svh=torch.float16, w2_suh=torch.float16, w2_svh=torch.float16)
+        self.bank = {k: t16(torch, v, dev, dt[k]) for k, v in self.bank_np.items()}
+        # rotating token batches route to different experts every step (defeats L2 reuse)
+        self.R = R = 8
+        self.xs, self.ls = [], []
+        for r in range(R):
+            x, logits = syn.moe_tokens(100 + r, self.T)
+            self.xs.append(t16(torch, x, dev, torch.bfloat16))
+            self.ls.append(torch.from_numpy(logits).to(dev))
+            if r == 0:
+                self.x0 = x
+        self.ids = torch.empty((self.T, self.TOPK), dtype=torch.int32, device=dev)
+        self.w = torch.empty((self.T, self.TOPK), dtype=torch.float32, device=dev)
+        self.y = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=dev)
+        self.ws = m.workspace(m.exl3_moe_workspace_bytes(self.T, self.H, self.I, self.E, self.TOPK), dev)
+        self.m = m
+        kk = self.bank_np["k_gu"].astype(np.int64)
+        per_slot = 3 * self.H * self.I * kk // 8
+        self.touched = []
+        for r in range(R):
+            ids, _ = oracle.topk_softmax(self.ls[r].cpu().numpy(), self.TOPK)
+            slots = np.unique(self.bank_np["perm"][ids.ravel()])
+            self.touched.append(int(per_slot[slots].sum()))
+        bank_mb = (self.bank["w13"].numel() + self.bank["w2"].numel()) * 2 / 1e6
+        self.l2 = f"{R} rotating token batches (different experts per step; bank {bank_mb:.0f} MB)"
+        self.launches_per_step = 7      # top-k, route, rotate, FC1, act, FC2, combine
+
+    def step(self, r, x=None):
+        m = self.m
+        m.exl3_moe_topk_softmax(self.ls[r], self.TOPK, self.ids, self.w)
+        m.exl3_moe_grouped(self.xs[r] if x is None else x, self.ids, self.w, self.bank, self.ws, y=self.y)
+
+    def roofline(self, torch, stream):
+        # the layer's launch chain: code bytes of the touched experts / layer time
+        ms = kernel_time_ms(torch, stream, lambda j: self.step(j % self.R), 4 * self.R)
+        hbm, _, src = peaks()
+        code = statistics.mean(self.touched)
+        a = code / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "kernel": "grouped MoE launch chain (top-k .. combine)",
+                "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
+                "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)", "traffic": None,
+                "per_layer_us": round(ms * 1e3, 2), "touched_code_bytes": int(code)}
+
+    def e2e_io(self, torch, dev):
+        xh = torch.from_numpy(self.x0.view(np.int16)).view(torch.bfloat16).pin_memory()
+        oh = torch.empty(self.y.shape, dtype=torch.bfloat16).pin_memory()
+        return xh, torch.empty_like(self.xs[0]), oh, self.y
+
+    def cpu_sample(self, budget):
+        import oracle
+        import synthetic as syn
+        x, logits = syn.moe_tokens(100, self.T)
+        ids, w = oracle.topk_softmax(logits, self.TOPK)
+        n = min(self.T, 4)
+        t0 = time.perf_counter()
+        oracle.moe_f64(np.ascontiguousarray(x[:n]), np.ascontiguousarray(ids[:n]), np.ascontiguousarray(w[:n]),
+                       self.bank_np)
+        t = time.perf_counter() - t0
+        return n / t, f"{n} of {self.T} tokens (their experts decoded), tokens/s of the sample"
+
+
+class Gather:
+    """int8 embedding gather: 8192 ids from a 248,320 x 5120 int8 table."""
+    V, H, N = 248320, 5120, 8192
+
+    def __init__(self, args):
+        self.metric = "int8 embedding gather tokens/s (8192 ids, 248320 x 5120)"
+        self.unit = "tokens/s"
+        self.units_per_step = self.N
+
+    def config(self):
+        return {"workload": "gather 8192 ids from int8 [248320, 5120] + fp16 row scale -> bf16"}
+
+    def setup(self, torch, m, syn, dev):
+        q, s, _ = syn.embedding(5)
+        self.q = t16(torch, q, dev, torch.int8)
+        self.s = t16(torch, s, dev, torch.float16)
+        self.R = R = 8
+        g = syn.rng(77)
+        self.idss = [torch.from_numpy(g.integers(0, self.V, self.N, dtype=np.int32)).to(dev) for _ in range(R)]
+        self.ids0 = self.idss[0].cpu().numpy()
+        self.out = torch.empty((self.N, self.H), dtype=torch.bfloat16, device=dev)
+        self.m = m
+        self.l2 = "table 1.27 GB >> L2; 8 rotating id sets"
+        self.launches_per_step = 1
+
+    def step(self, r, ids=None):
+        self.m.exl3_embed_int8_gather(self.q, self.s, self.idss[r] if ids is None else ids, out=self.out)
+
+    def roofline(self, torch, stream):
+        ms = kernel_time_ms(torch, stream, lambda j: self.step(j % self.R), 4 * self.R)
+        hbm, _, src = peaks()
+        alg = self.N * self.H + 2 * self.N + 4 * self.N + 2 * self.N * self.H
+        a = alg / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "kernel": "gather_kernel", "achieved": round(a, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(a / hbm, 4), "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
+                "traffic": profile_traffic("gather_8192.json", ["gather.cu"]), "per_launch_us": round(ms * 1e3, 2),
+                "algorithmic_bytes_per_launch": alg}
+
+    def e2e_io(self, torch, dev):
+        xh = torch.from_numpy(self.ids0).pin_memory()
+        oh = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        return xh, torch.empty_like(self.idss[0]), oh, self.out
+
+    def cpu_sample(self, budget):
+        import oracle
+        import synthetic as syn
+        q, s, ids = syn.embedding(5)
+        t0 = time.perf_counter()
+        oracle.gather(q, s, ids)
+        t = time.perf_counter() - t0
+        return self.N / t, "all 8192 ids"
+
+
+class Layer:
+    """The five projections of a hidden-5120 decoder layer (qkv K4, o K3, gate K2 + up K3, down K3)."""
+
+    def __init__(self, args):
+        self.M = args.m
+        self.metric = f"EXL3 decoder-layer projections tokens/s (M={self.M})"
+        self.unit = "tokens/s"
+        self.units_per_step = self.M
+
+    def config(self):
+        return {"workload": f"layer qkv 5120->7168 K4, o 5120->5120 K3, gate|up 5120->2x17408 K2|K3, "
+                            f"down 17408->5120 K3; M={self.M}", "M": self.M}
+
+    def setup(self, torch, m, syn, dev):
+        projs = syn.decoder_layer(4, M=self.M)
+        self.projs = projs
+        self.m = m
+        self.code_bytes = sum(sh.IC * sh.OC * sh.K // 8 for _, _, sh in projs)
+        self.R = R = max(2, int(np.ceil(4 * L2_BYTES / self.code_bytes))) if self.M <= 32 else 1
+        self.xs = {n: t16(torch, x, dev, torch.bfloat16) for n, x, _ in projs}
+        self.x0 = self.xs["qkv"]
+        self.dsh = {}
+        for n, _, sh in projs:
+            c = [t16(torch, sh.code, dev, torch.int16)]
+            for _ in range(R - 1):
+                c.append(c[0].clone())
+            self.dsh[n] = (c, sh.K, [t16(torch, v, dev, torch.float16) for v in (sh.s_in, sh.rin, sh.rout, sh.s_out)])
+        self.outs = {"qkv": torch.empty((self.M, 7168), dtype=torch.bfloat16, device=dev),
+                     "o": torch.empty((self.M, 5120), dtype=torch.bfloat16, device=dev),
+                     "gu": torch.empty((self.M, 34816), dtype=torch.bfloat16, device=dev),
+                     "down": torch.empty((self.M, 5120), dtype=torch.bfloat16, device=dev)}
+        self.ws = m.workspace(max(m.exl3_linear_workspace_bytes(self.M, 17408, 17408),
+                                  m.exl3_linear_shards_workspace_bytes(
+                                      self.M, 5120, [self._sh("gate", 0), self._sh("up", 0)])), dev)
+        self.l2 = (f"{R} rotating code copies ({R * self.code_bytes / 1e6:.0f} MB)" if R > 1
+                   else "inputs larger than L2")
+        self.launches_per_step = 8 if self.M <= 32 else 15
+
+    def _sh(self, n, r, col0=None):
+        c, K, sc = self.dsh[n]
+        t = (c[r], K, *sc)
+        return t + ((col0,) if col0 is not None else ())
+
+    def step(self, r, x=None):
+        m = self.m
+        c, K, sc = self.dsh["qkv"]
+        m.exl3_linear_into(self.x0 if x is None else x, c[r], K, *sc, self.outs["qkv"], 0, self.ws)
+        c, K, sc = self.dsh["o"]
+        m.exl3_linear_into(self.xs["o"], c[r], K, *sc, self.outs["o"], 0, self.ws)
+        m.exl3_linear_into_shards(self.xs["gate"], [self._sh("gate", r, 0), self._sh("up", r, 17408)],
+                                  self.outs["gu"], self.ws)
+        c, K, sc = self.dsh["down"]
+        m.exl3_linear_into(self.xs["down"], c[r], K, *sc, self.outs["down"], 0, self.ws)
+
+    def roofline(self, torch, stream):
+        ms = kernel_time_ms(torch, stream, lambda j: self.step(j % self.R), 4 * self.R)
+        hbm, tf, src = peaks()
+        if self.M <= 32:
+            a = self.code_bytes / (ms * 1e-3) / 1e9
+            return {"bound": "hbm", "kernel": "the layer's launches (code bytes / layer time)",
+                    "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
+                    "peak_source": src, "traffic": None, "per_layer_us": round(ms * 1e3, 2),
+                    "code_bytes": self.code_bytes}
+        fl = sum(2.0 * self.M * sh.IC * sh.OC for _, _, sh in self.projs)
+        a = fl / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": "the layer's launches (flops / layer time)", "achieved": round(a, 1),
+                "peak": tf, "unit": "TFLOP/s", "frac": round(a / tf, 4), "peak_source": src, "traffic": None,
+                "per_layer_us": round(ms * 1e3, 1)}
+
+    def e2e_io(self, torch, dev):
+        xh = torch.from_numpy(np.ascontiguousarray(self.projs[0][1]).view(np.int16)).view(torch.bfloat16).pin_memory()
+        oh = torch.empty(self.outs["down"].shape, dtype=torch.bfloat16).pin_memory()
+        return xh, torch.empty_like(self.x0), oh, self.outs["down"]
+
+    def cpu_sample(self, budget):
+        import oracle
+        t = 0.0
+        for _, x, sh in self.projs:
+            nb, rows = 2, min(self.M, 8)
+            t0 = time.perf_counter()
+            oracle.linear_f64(np.ascontiguousarray(x[:rows]), sh.code, sh.K, sh.s_in, sh.rin, sh.rout,
+                              sh.s_out, blk0=0, nblk=nb)
+            t += (time.perf_counter() - t0) * (sh.OC // 128) / nb * (self.M / rows)
+        return self.M / t, "2 output blocks of each projection (<= 8 rows), scaled to all blocks and rows"
+
+
+WORKLOADS = {"gate_up": GateUp, "prefill": Prefill, "moe": Moe, "gather": Gather, "layer": Layer}
+
+
+# ------------------------------------------------------------------ our arm
 def run_ours(args):
     import torch
     import moe_gemm_exl3_gb300 as m
@@ -123,46 +518,24 @@ def run_ours(args):
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    dist = None
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
     b.build()
-    M = args.m
+    wl = WORKLOADS[args.workload](args)
+    wl.setup(torch, m, syn, dev)
+    R = wl.R
 
-    x, shards = syn.gate_up(1, M=M)
-    # rotate through enough copies of the code words that every step streams from HBM
-    per_step_code = sum(code_bytes(K) for K in KS)
-    R = max(4, int(np.ceil(4 * L2_BYTES / per_step_code)))
-    codes = [[torch.from_numpy(s.code).to(dev) for s in shards]]
-    for _ in range(R - 1):
-        codes.append([c.clone() for c in codes[0]])
-    scal = [[torch.from_numpy(v.view(np.int16)).to(dev).view(torch.float16)
-             for v in (s.s_in, s.rin, s.rout, s.s_out)] for s in shards]
-    xd = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
-    out = torch.empty((M, 2 * OC), dtype=torch.bfloat16, device=dev)
-
-    # one merged-layer call per step: both shards, each with its own K and scales
-    shard_sets = [[(codes[r][i], sh.K, *scal[i], i * OC) for i, sh in enumerate(shards)] for r in range(R)]
-    ws = m.workspace(m.exl3_linear_shards_workspace_bytes(M, IC, shard_sets[0]), dev)
-
-    def step(r, xin=None, o=None):
-        xin = xd if xin is None else xin
-        o = out if o is None else o
-        m.exl3_linear_into_shards(xin, shard_sets[r], o, ws)
-
-    # pre-transform + one grouped GEMM per 32 rows
-    launches_per_step = 1 + (M + 31) // 32
-
-    # capture R steps (one per code copy) in one CUDA graph
     stream = torch.cuda.Stream(dev)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for r in range(R):
-            step(r)                          # eager warm-up of every path
+            wl.step(r)                       # eager warm-up of every path
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for r in range(R):
-                step(r)
+                wl.step(r)
     torch.cuda.synchronize()
 
     steps = max(R, (args.steps // R) * R)
@@ -172,8 +545,7 @@ def run_ours(args):
         for _ in range(warm):
             g.replay()
     torch.cuda.synchronize()
-    if world > 1:
-        import torch.distributed as dist
+    if dist:
         dist.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -184,149 +556,78 @@ def run_ours(args):
                 g.replay()
             e1.record(stream)
         torch.cuda.synchronize()
-    if world > 1:
+    if dist:
         dist.barrier()
     ms = e0.elapsed_time(e1)
-    if world > 1:
+    if dist:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    ms_step = ms / steps
-    value = world * M * steps / (ms / 1e3)
+    value = world * wl.units_per_step * steps / (ms / 1e3)
 
-    # ---- roofline: the step's grouped trellis GEMM kernel alone (exl3_gemm_into_shards is
-    # that one launch for M <= 32), timed with events on its stream; the stream is kept
-    # busy so no launch gap is measured
-    u = torch.empty((len(shards), M, IC), dtype=torch.float16, device=dev)
-    for i in range(len(shards)):
-        m.exl3_pretransform(xd, *scal[i][:2], u=u[i])
-    n_k = 4 * R
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(50_000_000)
-        for j in range(n_k):
-            evs[j][0].record(stream)
-            m.exl3_gemm_into_shards(u, shard_sets[j % R], out, ws)
-            evs[j][1].record(stream)
-    torch.cuda.synchronize()
-    dur_ms = statistics.mean(a.elapsed_time(b2) for a, b2 in evs[n_k // 4:])
-    hbm_peak, bf16_peak, peak_src = peaks()
-    alg = sum(algorithmic_bytes(M, K) for K in KS)
-    achieved = alg / (dur_ms * 1e-3) / 1e9
-    roof = {"bound": "hbm", "kernel": "group_gemm_kernel (gate K=2 + up K=3 in one launch)",
-            "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-            "frac": round(achieved / hbm_peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-            "traffic": traffic_from_profile(), "per_launch_us": round(dur_ms * 1e3, 2),
-            "algorithmic_bytes_per_launch": alg,
-            "code_GBps": round(sum(code_bytes(K) for K in KS) / (dur_ms * 1e-3) / 1e9, 1)}
+    roof = wl.roofline(torch, stream)
 
-    # ---- end to end through the public API with host buffers
-    xh = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
-    oh = torch.empty((M, 2 * OC), dtype=torch.bfloat16).pin_memory()
-    xdev = torch.empty_like(xd)
+    # ---- end to end through the public API with host buffers (pinned), eager launches
+    xh, xdev, oh, out = wl.e2e_io(torch, dev)
     e2e_steps = max(R, min(steps, 20 * R))
     with torch.cuda.stream(stream):
         for r in range(R):
             xdev.copy_(xh, non_blocking=True)
-            step(r, xdev)
+            wl.step(r, xdev)
             oh.copy_(out, non_blocking=True)
         torch.cuda.synchronize()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
         for i in range(e2e_steps):
             xdev.copy_(xh, non_blocking=True)
-            step(i % R, xdev)
+            wl.step(i % R, xdev)
             oh.copy_(out, non_blocking=True)
         a1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = a0.elapsed_time(a1)
-    e2e_val = M * e2e_steps / (e2e_ms / 1e3)
-    if world > 1:
-        t = torch.tensor([e2e_ms / e2e_steps], device=dev)
+    e2e_ms = a0.elapsed_time(a1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_val = world * M / (float(t.item()) / 1e3)
+        e2e_ms = float(t.item())
+    e2e_val = world * wl.units_per_step / (e2e_ms / 1e3)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-            "steps": steps, "warmup": warm * R, "ms_per_step": round(ms_step, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f16",
-            "data": "synthetic (seeded; uniform int16 code words, x ~ N(0,1))",
-            "config": {"workload": "gate_up 5120->2x17408, K=2|K=3, M=%d, out[M,34816]" % M,
-                       "M": M, "IC": IC, "OC_per_shard": OC, "K": list(KS),
-                       "l2": f"inputs larger than L2: {R} rotating code copies "
-                             f"({R * per_step_code / 1e6:.0f} MB)",
-                       "timing": "CUDA graph of %d steps, replayed; CUDA events" % R,
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
-            "gpu_launches": launches_per_step * steps,
+            "metric": wl.metric, "value": round(value, 3), "unit": wl.unit, "n_gpus": world,
+            "steps": steps, "warmup": warm * R, "ms_per_step": round(ms / steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic (seeded; uniform int16 code words, N(0,1) activations)",
+            "config": dict(wl.config(), l2=wl.l2, timing=f"CUDA graph of {R} steps, replayed; CUDA events",
+                           parallelism="replicas" if world > 1 else "single GPU"),
+            "gpu_launches": wl.launches_per_step * steps,
             "roofline": roof,
-            "e2e": {"value": round(e2e_val, 1), "unit": "tokens/s",
-                    "h2d_bytes_per_step": int(xh.numel() * 2), "d2h_bytes_per_step": int(oh.numel() * 2),
-                    "note": "exl3_linear_into_shards (one call for both shards), x copied from pinned host "
-                            "memory and out read back every step, eager launches"},
+            "e2e": {"value": round(e2e_val, 3), "unit": wl.unit,
+                    "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
+                    "d2h_bytes_per_step": int(oh.numel() * oh.element_size()),
+                    "note": "public API with pinned host input copied in and the result read back every step, "
+                            "eager launches"},
             "clocks": clk.summary(),
         }
         if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_baseline(M, budget_s=args.cpu_budget)
+            v, sample = wl.cpu_sample(args.cpu_budget)
+            line["cpu_baseline"] = {"value": round(v, 4), "unit": wl.unit, "cores": omp_threads(), "kind": "oracle",
+                                    "sample": sample}
         print(json.dumps(line), flush=True)
-    if world > 1:
+    if dist:
         dist.destroy_process_group()
 
 
-def traffic_from_profile():
-    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel."""
-    import hashlib
-    p = os.path.join(ROOT, "profiles", "decode_gemm_gate_up_m8.json")
-    src = os.path.join(ROOT, "moe_gemm_exl3_gb300", "csrc", "linear.cu")
-    if not os.path.exists(p):
-        return None
-    with open(p) as f:
-        d = json.load(f)
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
-    if d.get("source_sha256_16") != h:
-        return None
-    return d.get("dram_bytes_per_launch")
-
-
-# ------------------------------------------------------------------ oracle
-def cpu_baseline(M, budget_s=15.0, seed=1):
-    """The CPU oracle on a bounded sample of the workload, scaled to tokens/s."""
-    import oracle
-    import synthetic as syn
-    x, shards = syn.gate_up(seed, M=M)
-    nblk_total = OC // 128
-    oracle.lib()
-    # time one block per shard, then size the sample to the budget
-    t0 = time.perf_counter()
-    for sh in shards:
-        oracle.linear_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=0, nblk=1)
-    per_blk = (time.perf_counter() - t0) / 2
-    nblk = int(min(nblk_total, max(1, budget_s / max(per_blk, 1e-6) / 2)))
-    t0 = time.perf_counter()
-    for sh in shards:
-        oracle.linear_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=0, nblk=nblk)
-    t = time.perf_counter() - t0
-    full = t * nblk_total / nblk
-    return {"value": round(M / full, 3), "unit": "tokens/s", "cores": _omp_threads(),
-            "kind": "oracle",
-            "sample": f"M={M}, output blocks 0..{nblk - 1} of {nblk_total} (128 columns each) of both "
-                      f"shards in {t:.1f} s, scaled linearly to all {nblk_total} blocks"}
-
-
-def _omp_threads():
-    n = os.environ.get("OMP_NUM_THREADS")
-    return int(n) if n else os.cpu_count()
-
-
+# ------------------------------------------------------------------ reference arm
 def run_reference(args):
-    """The oracle as the reference arm: same metric and workload, each step a bounded
+    """The CPU oracle as the reference arm: same metric and workload, each step a bounded
     sample (whole 128-column output blocks of both shards), scaled to the full step."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    M = args.m
+    if args.workload != "gate_up":
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm covers the headline workload only"}))
+        return
+    M, OC = args.m, GateUp.OC
     import oracle
     import synthetic as syn
     x, shards = syn.gate_up(1, M=M)
@@ -353,17 +654,15 @@ def run_reference(args):
         one(nblk)
     t = (time.perf_counter() - t0) / run_steps * nblk_total / nblk
     v = M / t
-    line = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "tokens/s",
+    wl = GateUp(args)
+    line = {"impl": "reference", "metric": wl.metric, "value": round(v, 3), "unit": "tokens/s",
             "n_gpus": 1, "steps": run_steps, "steps_requested": K, "warmup": min(W, 1),
             "ms_per_step": round(t * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": "gate_up 5120->2x17408, K=2|K=3, M=%d, out[M,34816]" % M, "M": M},
-            "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": _omp_threads(),
-                             "kind": "oracle",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)", "config": wl.config(),
+            "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": omp_threads(), "kind": "oracle",
                              "sample": f"each step: output blocks 0..{nblk - 1} of {nblk_total} (128 columns) "
                                        f"of both shards, scaled linearly to the full step"},
-            "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
-                    "d2h_bytes_per_step": 0}}
+            "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -372,16 +671,21 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--m", type=int, default=8)
+    ap.add_argument("--workload", default="gate_up", choices=sorted(WORKLOADS))
+    ap.add_argument("--m", type=int, default=8, help="rows (gate_up, layer)")
+    ap.add_argument("--k", type=int, default=2, help="bits per weight (prefill)")
+    ap.add_argument("--t", type=int, default=16, help="tokens (moe)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of oracle work")
+    ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of oracle work (reference arm)")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = 50000
+        args.steps = {"gate_up": 50000, "prefill": 300, "moe": 4000, "gather": 5000, "layer": 4000}[args.workload]
+        if args.workload == "layer" and args.m > 32:
+            args.steps = 100
     if args.warmup is None:
-        args.warmup = 200
+        args.warmup = 200 if args.workload == "gate_up" else 20
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         run_reference(args)
