@@ -228,13 +228,13 @@ class Prefill:
     IC, OC = 5120, 17408
 
     def __init__(self, args):
-        self.M, self.K = 8192, args.k
-        self.metric = "EXL3 linear TFLOP/s (prefill-shaped, M=8192)"
+        self.M, self.K = (args.m if args.m > 32 else 8192), args.k
+        self.metric = f"EXL3 linear TFLOP/s (prefill-shaped, M={self.M})"
         self.unit = "TFLOP/s"
         self.units_per_step = 2.0 * self.M * self.IC * self.OC / 1e12
 
     def config(self):
-        return {"workload": f"prefill 5120->17408, K={self.K}, M=8192, 1% outlier channels", "M": self.M,
+        return {"workload": f"prefill 5120->17408, K={self.K}, M={self.M}, 1% outlier channels", "M": self.M,
                 "IC": self.IC, "OC": self.OC, "K": self.K}
 
     def setup(self, torch, m, syn, dev):
@@ -246,7 +246,7 @@ class Prefill:
         self.ws = m.workspace(m.exl3_linear_workspace_bytes(self.M, self.IC, self.OC), dev)
         self.u = m.exl3_pretransform(self.xd, self.sc[0], self.sc[1])
         self.m, self.R = m, 1
-        self.l2 = "inputs larger than L2 (u 84 MB, decoded weights 178 MB, out 285 MB)"
+        self.l2 = "inputs larger than L2 (decoded weights 178 MB, activations and output M x 10 KB / 34 KB)"
         self.launches_per_step = 3      # pre-transform, reconstruct, tcgen05 GEMM
 
     def step(self, r, x=None):
@@ -279,11 +279,12 @@ class Prefill:
         import synthetic as syn
         x, sh = syn.prefill(2, M=self.M, K=self.K)
         rows = 8
+        self_M = self.M
         t0 = time.perf_counter()
         oracle.linear_f64(np.ascontiguousarray(x[:rows]), sh.code, self.K, sh.s_in, sh.rin, sh.rout, sh.s_out)
         t = time.perf_counter() - t0
         flops = 2.0 * rows * self.IC * self.OC
-        return flops / t / 1e12, (f"{rows} of 8192 rows, all 17408 columns (the weights decoded once), "
+        return flops / t / 1e12, (f"{rows} of {self_M} rows, all 17408 columns (the weights decoded once), "
                                   f"TFLOP/s of the sample")
 
 

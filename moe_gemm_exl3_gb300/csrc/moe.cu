@@ -70,31 +70,52 @@ MoeLayout moe_layout(int T, int H, int I, int E, int topk) {
 }
 
 // ------------------------------------------------------------------ top-k
-// One thread per token: the topk largest logits (ties: lower expert id), then
-// softmax over the selected logits.
-__global__ void topk_softmax_kernel(const float *__restrict__ logits, int T, int E, int topk,
-                                    int32_t *__restrict__ ids, float *__restrict__ w) {
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+// One warp per token: each lane holds the logits e = lane, lane + 32, ...; each
+// of the topk rounds is a warp arg-max (largest logit, ties to the lower expert
+// id); then softmax over the selected logits.
+__global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restrict__ logits, int T, int E, int topk,
+                                                           int32_t *__restrict__ ids, float *__restrict__ w) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     const float *l = logits + (int64_t)t * E;
-    uint32_t used[kMoeMaxE / 32];
-    for (int i = 0; i < (E + 31) / 32; i++) used[i] = 0;
-    float sel[kMoeMaxTopk];
-    for (int k = 0; k < topk; k++) {
-        int best = -1;
-        float bv = 0.f;
-        for (int e = 0; e < E; e++) {
-            if (used[e >> 5] & (1u << (e & 31))) continue;
-            const float v = __ldg(l + e);
-            if (best < 0 || v > bv) { best = e; bv = v; }
-        }
-        used[best >> 5] |= 1u << (best & 31);
-        ids[(int64_t)t * topk + k] = best;
-        sel[k] = bv;
+    constexpr int PER = kMoeMaxE / 32;
+    float v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; i++) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? __ldg(l + e) : -INFINITY;
     }
-    float den = 0.f;
-    for (int k = 0; k < topk; k++) den += expf(sel[k] - sel[0]);
-    for (int k = 0; k < topk; k++) w[(int64_t)t * topk + k] = expf(sel[k] - sel[0]) / den;
+    uint32_t taken = 0;     // bit i: logit lane + 32 i already selected
+    float sel0 = 0.f, den = 0.f, my_sel = 0.f;
+    for (int k = 0; k < topk; k++) {
+        float bv = -INFINITY;
+        int be = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < PER; i++) {
+            const int e = lane + 32 * i;
+            if (e < E && !(taken & (1u << i)) && (v[i] > bv || be == 0x7FFFFFFF)) {
+                bv = v[i];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(kFull, bv, off);
+            const int oe = __shfl_xor_sync(kFull, be, off);
+            if (oe != 0x7FFFFFFF && (be == 0x7FFFFFFF || ov > bv || (ov == bv && oe < be))) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (k == 0) sel0 = bv;
+        const float ex = expf(bv - sel0);
+        den += ex;
+        if (lane == k) my_sel = ex;
+        if (lane == 0) ids[(int64_t)t * topk + k] = be;
+    }
+    if (lane < topk) w[(int64_t)t * topk + lane] = my_sel / den;
 }
 
 // ------------------------------------------------------------------ route
@@ -319,7 +340,7 @@ exl3_status exl3_moe_topk_softmax(const float *logits, int32_t T, int32_t E, int
                     kMoeMaxE, topk, kMoeMaxTopk);
     if (T == 0) return EXL3_OK;
     if (!logits || !ids || !w) return fail(EXL3_EINVAL, "moe_topk_softmax: null pointer");
-    topk_softmax_kernel<<<(T + 127) / 128, 128, 0, (cudaStream_t)stream>>>(logits, T, E, topk, ids, w);
+    topk_softmax_kernel<<<(T + 7) / 8, 256, 0, (cudaStream_t)stream>>>(logits, T, E, topk, ids, w);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "moe_topk_softmax");
     return EXL3_OK;
