@@ -136,6 +136,20 @@ def profile_traffic(name, src_files):
     return d.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(torch, dist, value, device):
+    """The largest value over all ranks (every rank gets it); the value itself without a group."""
+    if dist is None:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, units_per_step, steps, max_ms):
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_step * steps / (max_ms / 1e3)
+
+
 def t16(torch, a, dev, dtype):
     a = np.ascontiguousarray(a)
     if dtype in (torch.bfloat16, torch.float16):
@@ -559,12 +573,8 @@ def run_ours(args):
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * wl.units_per_step * steps / (ms / 1e3)
+    ms = max_over_ranks(torch, dist, e0.elapsed_time(e1), dev)
+    value = job_throughput(world, wl.units_per_step, steps, ms)
 
     roof = wl.roofline(torch, stream)
 
@@ -585,12 +595,8 @@ def run_ours(args):
             oh.copy_(out, non_blocking=True)
         a1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = a0.elapsed_time(a1) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = world * wl.units_per_step / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(torch, dist, a0.elapsed_time(a1) / e2e_steps, dev)
+    e2e_val = job_throughput(world, wl.units_per_step, 1, e2e_ms)
 
     if rank == 0:
         line = {
