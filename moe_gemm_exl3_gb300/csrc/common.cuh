@@ -74,32 +74,54 @@ __device__ __forceinline__ uint32_t trellis_weight_pair(uint32_t za, uint32_t zb
     return *reinterpret_cast<uint32_t *>(&s);
 }
 
+// Multipliers 1 << o for the state extraction, passed to kernels by value.
+struct Pow2Table {
+    uint32_t v[17];
+};
+inline Pow2Table make_pow2_table() {
+    Pow2Table t;
+    for (int i = 0; i < 17; i++) t.v[i] = 1u << i;
+    return t;
+}
+
 // A quarter of a tile: 4 tile rows x 16 columns = 64 weights, 64K stream bits
 // held as 2K little-endian uint32 words (int16 word 2j in bits 0..15 of word j).
 // `prev` is the uint32 word preceding the quarter in the circular tile stream;
 // only its high int16 (the stream word just before the quarter) is used.
 //
-// Builds E[0..2K], E[j] = stream bits [32j - 16, 32j + 16) relative to the
-// quarter start, as big-endian 32-bit values (E[0] starts with the preceding
-// 16 bits).  The state of quarter weight i (0..63) is then the 16 bits of E
-// starting at bit (i+1)K.
+// Let S be the quarter's bits preceded by those 16 bits.  E[j] = S bits
+// [32j, 32j + 32) and F[j] = S bits [32j + 16, 32j + 48), as big-endian 32-bit
+// values; the state of quarter weight i (0..63) is the 16 bits of S starting
+// at bit (i+1)K, which always lie within one E or one F word at an offset
+// o in [0, 16] from its top.
 template <int K>
 struct QuarterStream {
     uint32_t E[2 * K + 1];
+    uint32_t F[2 * K];
 
     __device__ __forceinline__ void build(const uint32_t (&w)[2 * K], uint32_t prev) {
         E[0] = __byte_perm(w[0], prev, 0x7610);
 #pragma unroll
         for (int j = 1; j < 2 * K; j++) E[j] = __byte_perm(w[j], w[j - 1], 0x7610);
         E[2 * K] = w[2 * K - 1] & 0xFFFF0000u;
+#pragma unroll
+        for (int j = 0; j < 2 * K; j++) F[j] = __byte_perm(w[j], 0, 0x1032);
     }
 
     // 16-bit trellis state of quarter weight i (compile-time i after unrolling).
-    __device__ __forceinline__ uint32_t state(int i) const {
+    // The general case shifts the window to the top of the word with a multiply
+    // by 2^o and then down by 16: the multiply runs on the FMA pipe, which
+    // balances the integer ALU pipe that the hash's LOP3 and the shift occupy.
+    // pow2[o] must hold 1 << o; it is read from a kernel argument so that the
+    // compiler cannot turn the multiply back into an ALU shift.
+    __device__ __forceinline__ uint32_t state(int i, const uint32_t *pow2) const {
         const int p = (i + 1) * K;
         const int j = p >> 5, o = p & 31;
-        if (o <= 16) return (E[j] >> (16 - o)) & 0xFFFFu;
-        return __funnelshift_r(E[j + 1], E[j], 48 - o) & 0xFFFFu;
+        const uint32_t R = o <= 16 ? E[j] : F[j];
+        const int oo = o <= 16 ? o : o - 16;
+        if (oo == 0) return R >> 16;
+        if (oo == 16) return R & 0xFFFFu;
+        return (R * pow2[oo]) >> 16;
     }
 };
 

@@ -82,6 +82,7 @@ struct GroupGemmArgs {
     float *partials;
     int32_t *counters;
     uint32_t hash_xor;            // the codebook's xor constant, kept in a register
+    uint32_t pow2[17];            // pow2[o] = 1 << o (multipliers of the state extraction)
     int32_t max_rows;             // rows per entry the launch was sized for
 };
 constexpr int kMaxInlineEntries = 4;

@@ -71,7 +71,7 @@ template <int K>
 __global__ void __launch_bounds__(256) reconstruct_kernel(const int16_t *__restrict__ code,
                                                           int IC, int OC,
                                                           uint16_t *__restrict__ W,
-                                                          bool transposed) {
+                                                          bool transposed, const Pow2Table p2) {
     const int lane = threadIdx.x & 31;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int TO = OC / kTile;
@@ -92,8 +92,8 @@ __global__ void __launch_bounds__(256) reconstruct_kernel(const int16_t *__restr
             uint32_t pk[8];
 #pragma unroll
             for (int c = 0; c < 16; c += 2)
-                pk[c / 2] = trellis_weight_pair(trellis_hash(st.state(16 * r + c)),
-                                                trellis_hash(st.state(16 * r + c + 1)));
+                pk[c / 2] = trellis_weight_pair(trellis_hash(st.state(16 * r + c, p2.v)),
+                                                trellis_hash(st.state(16 * r + c + 1, p2.v)));
             uint4 *dst = reinterpret_cast<uint4 *>(W + (int64_t)(16 * a + 4 * q + r) * OC + 16 * b);
             dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(256) reconstruct_kernel(const int16_t *__restr
     } else {
 #pragma unroll
         for (int c = 0; c < 16; c++) {
-            uint32_t p0 = trellis_weight_pair(trellis_hash(st.state(c)), trellis_hash(st.state(16 + c)));
-            uint32_t p1 = trellis_weight_pair(trellis_hash(st.state(32 + c)), trellis_hash(st.state(48 + c)));
+            uint32_t p0 = trellis_weight_pair(trellis_hash(st.state(c, p2.v)), trellis_hash(st.state(16 + c, p2.v)));
+            uint32_t p1 = trellis_weight_pair(trellis_hash(st.state(32 + c, p2.v)), trellis_hash(st.state(48 + c, p2.v)));
             *reinterpret_cast<uint2 *>(W + (int64_t)(16 * b + c) * IC + 16 * a + 4 * q) = make_uint2(p0, p1);
         }
     }
@@ -112,10 +112,11 @@ cudaError_t launch_reconstruct(const int16_t *code, int IC, int OC, int K, uint1
                                bool transposed, cudaStream_t s) {
     const int64_t quarters = (int64_t)(IC / kTile) * (OC / kTile) * 4;
     const unsigned grid = (unsigned)((quarters + 255) / 256);
+    const Pow2Table p2 = make_pow2_table();
     switch (K) {
-        case 2: reconstruct_kernel<2><<<grid, 256, 0, s>>>(code, IC, OC, W, transposed); break;
-        case 3: reconstruct_kernel<3><<<grid, 256, 0, s>>>(code, IC, OC, W, transposed); break;
-        case 4: reconstruct_kernel<4><<<grid, 256, 0, s>>>(code, IC, OC, W, transposed); break;
+        case 2: reconstruct_kernel<2><<<grid, 256, 0, s>>>(code, IC, OC, W, transposed, p2); break;
+        case 3: reconstruct_kernel<3><<<grid, 256, 0, s>>>(code, IC, OC, W, transposed, p2); break;
+        case 4: reconstruct_kernel<4><<<grid, 256, 0, s>>>(code, IC, OC, W, transposed, p2); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -167,10 +168,11 @@ __device__ __forceinline__ int frag_index(int n, int oc) {
     return ((j * NB + nb) * 4 + (2 * rrow + c)) * 32 + (4 * g + q);
 }
 
-// Registers per thread grow with NB (the accumulators); the bound keeps NB = 1
-// at three CTAs (24 warps) per SM.
+// CTAs per SM the register budget is sized for.  NB = 1 runs two CTAs (16 warps)
+// of up to 128 registers: measured faster than three CTAs at 80 registers (the
+// extra registers buy prefetch depth and instruction-level parallelism).
 template <int NB>
-struct DecodeOcc { static constexpr int value = NB == 1 ? 3 : (NB == 2 ? 2 : 1); };
+struct DecodeOcc { static constexpr int value = NB <= 2 ? 2 : 1; };
 
 template <int NB>
 constexpr size_t group_smem_bytes() {
@@ -182,7 +184,7 @@ constexpr size_t group_smem_bytes() {
 template <int K, int NB>
 __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const GroupEntry &e, const uint16_t *u,
                                                  int IC, int G, int a_lo, int a_hi, int lane, int warp,
-                                                 uint32_t hx) {
+                                                 uint32_t hx, const uint32_t *pow2) {
     constexpr int PF = 2;   // tile rows of code words in flight per warp
     const int g = lane >> 2, q = lane & 3;
     const int TO = e.OC / kTile;
@@ -233,10 +235,10 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
 #pragma unroll
             for (int j = 0; j < 8; j++) {
                 const int i0 = 32 * rp + 2 * j;
-                const uint32_t z0 = trellis_hash_x(st.state(i0), hx);
-                const uint32_t z1 = trellis_hash_x(st.state(i0 + 1), hx);
-                const uint32_t z2 = trellis_hash_x(st.state(i0 + 16), hx);
-                const uint32_t z3 = trellis_hash_x(st.state(i0 + 17), hx);
+                const uint32_t z0 = trellis_hash_x(st.state(i0, pow2), hx);
+                const uint32_t z1 = trellis_hash_x(st.state(i0 + 1, pow2), hx);
+                const uint32_t z2 = trellis_hash_x(st.state(i0 + 16, pow2), hx);
+                const uint32_t z3 = trellis_hash_x(st.state(i0 + 17, pow2), hx);
 #pragma unroll
                 for (int nb = 0; nb < NB; nb++)
                     mma_16816(acc[j][nb], z0, z1, z2, z3, b[nb][2 * rp], b[nb][2 * rp + 1]);
@@ -308,9 +310,9 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
             for (int nb = 0; nb < NB; nb++)
 #pragma unroll
                 for (int r = 0; r < 4; r++) acc[j][nb][r] = 0.f;
-        if ((KSET & 4) && e.K == 2) group_accumulate<2, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx);
-        if ((KSET & 8) && e.K == 3) group_accumulate<3, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx);
-        if ((KSET & 16) && e.K == 4) group_accumulate<4, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx);
+        if ((KSET & 4) && e.K == 2) group_accumulate<2, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2);
+        if ((KSET & 8) && e.K == 3) group_accumulate<3, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2);
+        if ((KSET & 16) && e.K == 4) group_accumulate<4, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2);
 
         // ---- CTA reduction in fixed warp order (fragment order, one barrier)
 #pragma unroll
@@ -405,6 +407,7 @@ static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t tot
     }
     GroupGemmArgs a = a0;
     a.hash_xor = kHashXor;
+    for (int i = 0; i < 17; i++) a.pow2[i] = 1u << i;
     int64_t grid = (int64_t)device_info().sm_count * occ;
     if (grid > kDecodeMaxCtas) grid = kDecodeMaxCtas;
     if (total_hint > 0 && grid > total_hint) grid = total_hint;
