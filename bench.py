@@ -158,6 +158,16 @@ def t16(torch, a, dev, dtype):
 
 
 # ------------------------------------------------------------------ workloads
+def gemm_path(M):
+    """The GEMM path the library takes for M rows (the C-ABI's default choice)."""
+    return "decode" if M <= 32 else ("fused" if M <= 128 else "prefill")
+
+
+def linear_launches(M, n_shards):
+    """Kernel launches of one linear call: the pre-transform plus the GEMM path's."""
+    return 1 + (2 * n_shards if gemm_path(M) == "prefill" else 1)
+
+
 class GateUp:
     """Decode-shaped merged gate (K=2) / up (K=3) projection, 5120 -> 2 x 17408."""
     IC, OC, KS = 5120, 17408, (2, 3)
@@ -193,7 +203,7 @@ class GateUp:
             m.exl3_pretransform(self.xd, *scal[i][:2], u=self.u[i])
         self.m = m
         self.l2 = f"inputs larger than L2: {R} rotating code copies ({R * per_step / 1e6:.0f} MB)"
-        self.launches_per_step = 1 + (M + 31) // 32
+        self.launches_per_step = linear_launches(M, 2)
 
     def step(self, r, x=None):
         self.m.exl3_linear_into_shards(self.xd if x is None else x, self.sets[r], self.out, self.ws)
@@ -206,10 +216,13 @@ class GateUp:
         alg = sum(self.code_bytes(K) + 2 * self.M * self.IC + 2 * self.M * self.OC + 2 * 2 * self.OC
                   for K in self.KS)
         a = alg / (ms * 1e-3) / 1e9
-        return {"bound": "hbm", "kernel": "group_gemm_kernel (gate K=2 + up K=3 in one launch)",
+        kernel = {"decode": "group_gemm_kernel", "fused": "fused_tc_kernel",
+                  "prefill": "reconstruct + prefill_gemm_kernel"}[gemm_path(self.M)]
+        return {"bound": "hbm", "kernel": kernel + " (gate K=2 + up K=3 in one call)",
                 "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
-                "traffic": profile_traffic("decode_gemm_gate_up_m8.json", ["linear.cu", "common.cuh"]),
+                "traffic": (profile_traffic("decode_gemm_gate_up_m8.json", ["linear.cu", "common.cuh"])
+                            if gemm_path(self.M) == "decode" else None),
                 "per_launch_us": round(ms * 1e3, 2), "algorithmic_bytes_per_launch": alg,
                 "code_GBps": round(sum(self.code_bytes(K) for K in self.KS) / (ms * 1e-3) / 1e9, 1)}
 
@@ -452,7 +465,7 @@ class Layer:
         self.projs = projs
         self.m = m
         self.code_bytes = sum(sh.IC * sh.OC * sh.K // 8 for _, _, sh in projs)
-        self.R = R = max(2, int(np.ceil(4 * L2_BYTES / self.code_bytes))) if self.M <= 32 else 1
+        self.R = R = max(2, int(np.ceil(4 * L2_BYTES / self.code_bytes))) if self.M <= 128 else 1
         self.xs = {n: t16(torch, x, dev, torch.bfloat16) for n, x, _ in projs}
         self.x0 = self.xs["qkv"]
         self.dsh = {}
@@ -470,7 +483,7 @@ class Layer:
                                       self.M, 5120, [self._sh("gate", 0), self._sh("up", 0)])), dev)
         self.l2 = (f"{R} rotating code copies ({R * self.code_bytes / 1e6:.0f} MB)" if R > 1
                    else "inputs larger than L2")
-        self.launches_per_step = 8 if self.M <= 32 else 15
+        self.launches_per_step = sum(linear_launches(self.M, n) for n in (1, 1, 2, 1))
 
     def _sh(self, n, r, col0=None):
         c, K, sc = self.dsh[n]
@@ -491,7 +504,7 @@ class Layer:
     def roofline(self, torch, stream):
         ms = kernel_time_ms(torch, stream, lambda j: self.step(j % self.R), 4 * self.R)
         hbm, tf, src = peaks()
-        if self.M <= 32:
+        if gemm_path(self.M) != "prefill":
             a = self.code_bytes / (ms * 1e-3) / 1e9
             return {"bound": "hbm", "kernel": "the layer's launches (code bytes / layer time)",
                     "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),

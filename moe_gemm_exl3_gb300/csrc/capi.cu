@@ -72,16 +72,34 @@ int32_t *workspace_counters(void *base) {
     return reinterpret_cast<int32_t *>(static_cast<char *>(base) + kHeaderBytes);
 }
 
-// Rows above which the prefill (tensor-core) path is taken.
-int64_t prefill_threshold() {
-    static int64_t t = -1;
-    if (t < 0) {
-        const char *f = std::getenv("EXL3_FORCE_MODE");
-        t = kDecodeMaxRows;
-        if (f && !std::strcmp(f, "decode")) t = INT64_MAX;
-        if (f && !std::strcmp(f, "prefill")) t = 0;
-    }
-    return t;
+// Which GEMM path serves M rows:
+//   decode   M <= kDecodeModeMaxRows: register-resident decode + mma.sync, rows on the MMA's N
+//   fused    M <= kFusedMaxRows: decode into shared memory + tcgen05 MMAs
+//   prefill  larger M: reconstruct W^T once, then the persistent tcgen05 GEMM
+// The boundaries are where the measured times of neighbouring paths cross on
+// the 5120 -> 2 x 17408 projection.  EXL3_FORCE_MODE=decode|fused|prefill
+// overrides the choice (read on every call).
+constexpr int64_t kDecodeModeMaxRows = kDecodeMaxRows;
+enum class GemmMode { kDecode, kFused, kPrefill };
+
+static int forced_mode() {
+    const char *f = std::getenv("EXL3_FORCE_MODE");
+    if (!f) return 0;
+    if (!std::strcmp(f, "decode")) return 1;
+    if (!std::strcmp(f, "fused")) return 2;
+    if (!std::strcmp(f, "prefill")) return 3;
+    return 0;
+}
+
+GemmMode gemm_mode(int64_t M) {
+    const int force = forced_mode();
+    if (force == 1) return GemmMode::kDecode;
+    if (force == 2 && M <= kFusedMaxRows && fused_supported()) return GemmMode::kFused;
+    if (force == 3 && prefill_supported()) return GemmMode::kPrefill;
+    if (M <= kDecodeModeMaxRows) return GemmMode::kDecode;
+    if (M <= kFusedMaxRows && fused_supported()) return GemmMode::kFused;
+    if (prefill_supported()) return GemmMode::kPrefill;
+    return GemmMode::kDecode;
 }
 
 size_t linear_workspace_layout(int64_t max_M, int32_t max_IC, int32_t max_OC, LinearWorkspace *ws,
@@ -89,6 +107,8 @@ size_t linear_workspace_layout(int64_t max_M, int32_t max_IC, int32_t max_OC, Li
     return linear_workspace_layout_n(max_M, max_IC, 1, max_OC / 128, max_OC, ws, base);
 }
 
+// Sized for every path that some M <= max_M can take, so the byte count never
+// decreases as max_M grows.
 size_t linear_workspace_layout_n(int64_t max_M, int32_t IC, int n_shards, int total_groups, int32_t max_OC,
                                  LinearWorkspace *ws, void *base) {
     if (max_M < 0 || IC <= 0 || max_OC <= 0 || n_shards <= 0) return 0;
@@ -98,11 +118,15 @@ size_t linear_workspace_layout_n(int64_t max_M, int32_t IC, int n_shards, int to
     const size_t u_elems = (size_t)n_shards * max_M * IC;
     const size_t u_off = off;
     off = align256(off + u_elems * sizeof(uint16_t));
-    const size_t part_elems = group_slab_floats(total_groups, nb);
+    size_t part_elems = group_slab_floats(total_groups, nb);
+    if (fused_supported() && max_M > 0) {
+        const size_t f = fused_slab_floats(total_groups, max_M);
+        if (f > part_elems) part_elems = f;
+    }
     const size_t part_off = off;
     off = align256(off + part_elems * sizeof(float));
     size_t wt_elems = 0, wt_off = off;
-    if (max_M > prefill_threshold() && prefill_supported()) {
+    if ((max_M > kFusedMaxRows || (max_M > 0 && forced_mode() == 3)) && prefill_supported()) {
         wt_elems = (size_t)max_OC * IC;
         off = align256(off + wt_elems * sizeof(uint16_t));
     }
@@ -206,7 +230,35 @@ struct ShardDesc {
 static exl3_status run_gemm(const char *fn, const uint16_t *u, int64_t M, int32_t IC, const ShardDesc *sh, int n,
                             uint16_t *out, int64_t ldo, const LinearWorkspace &ws, bool pdl, cudaStream_t s) {
     cudaError_t e;
-    if (M > prefill_threshold() && prefill_supported()) {
+    const GemmMode mode = gemm_mode(M);
+    if (mode == GemmMode::kFused) {
+        FusedArgs a = {};
+        a.n_shards = n;
+        a.M = (int32_t)M;
+        a.IC = IC;
+        int g0 = 0;
+        for (int i = 0; i < n; i++) {
+            FusedShard &f = a.sh[i];
+            f.code = sh[i].code;
+            f.rout = sh[i].rout;
+            f.s_out = sh[i].s_out;
+            f.col0 = sh[i].col0;
+            f.K = sh[i].K;
+            f.OC = sh[i].OC;
+            f.g0 = g0;
+            g0 += sh[i].OC / 128;
+        }
+        a.out = out;
+        a.ldo = ldo;
+        a.partials = ws.partials;
+        a.counters = ws.counters;
+        a.err = ws.err;
+        e = launch_fused(a, u, s);
+        if (e != cudaSuccess) return cuda_fail(e, fn);
+        trace("%s M=%lld IC=%d shards=%d mode=fused", fn, (long long)M, IC, n);
+        return EXL3_OK;
+    }
+    if (mode == GemmMode::kPrefill) {
         for (int i = 0; i < n; i++) {
             bool launched = false;
             e = launch_reconstruct(sh[i].code, IC, sh[i].OC, sh[i].K, ws.wt, /*transposed=*/true, s);

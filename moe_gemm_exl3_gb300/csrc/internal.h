@@ -1,6 +1,7 @@
 // internal.h -- host-side launch interfaces between the C ABI layer and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -91,6 +92,36 @@ constexpr int kMaxInlineEntries = 4;
 // column groups (for the partial slab), rows per entry <= 8 * nb.
 cudaError_t launch_group_gemm(const GroupGemmArgs &a, int nb, bool pdl, cudaStream_t s);
 size_t group_slab_floats(int max_groups, int nb);
+
+// Fused decode + tensor-core GEMM for 8 < M <= kFusedMaxRows rows: the trellis
+// is decoded into shared-memory operand tiles that tcgen05 MMAs multiply by the
+// pre-transformed activations u [shard][M][IC] (fp16).
+constexpr int kFusedMaxRows = 128;
+constexpr int kFusedMaxCtas = 256;
+struct FusedShard {
+    const int16_t *code;
+    const uint16_t *rout, *s_out;
+    int64_t col0;        // first output column of this shard
+    int32_t K, OC;
+    int32_t g0;          // first global column-group index
+    int32_t pad_;
+};
+struct FusedArgs {
+    CUtensorMap tm_u;        // u [n_shards * M][IC], box 64 channels x rows-per-tile
+    CUtensorMap tm_code[4];  // per shard: the code as (tile words, tiles, tile rows)
+    FusedShard sh[4];
+    int32_t n_shards, M, IC, pad_;
+    uint16_t *out;       // bf16, row stride ldo
+    int64_t ldo;
+    float *partials;     // split-K slab, fused_slab_floats() floats
+    int32_t *counters;
+    int32_t *err;
+    uint32_t hash_xor;
+    uint32_t pow2[17];
+};
+bool fused_supported();
+size_t fused_slab_floats(int max_groups, int64_t rows);
+cudaError_t launch_fused(FusedArgs &a, const uint16_t *u, cudaStream_t s);
 
 bool prefill_supported();
 cudaError_t launch_prefill(const uint16_t *u, const uint16_t *wt, int64_t M, int IC, int OC,

@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace exl3 {
 
@@ -31,96 +32,7 @@ constexpr int B_BYTES = BN * BK * 2;                 // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 256;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* alignment */ + 256 /* barriers */;
-constexpr uint32_t kWaitLimit = 1u << 22;
-
-// ------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// Bounded wait: false (and the error recorded, abort raised) if the phase never completes.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t *err, volatile int *abort) {
-    for (uint32_t i = 0; i < kWaitLimit; i++) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-    }
-    record_error(err, kErrWaitTimeout);
-    *abort = 1;
-    return false;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr >> 4) & 0x3FFFu);          // start address
-    d |= (uint64_t)(16 >> 4) << 16;                   // leading byte offset (unused for this layout)
-    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset: 8 rows x 128 B
-    d |= (uint64_t)1 << 46;                           // descriptor version
-    d |= (uint64_t)2 << 61;                           // swizzle: 128 B
-    return d;
-}
-
-// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M = 128, N = 256.
-constexpr uint32_t kIdesc = (1u << 4)                 // D format: f32
-                            | (0u << 7) | (0u << 10)  // A, B format: f16
-                            | ((uint32_t)(BN >> 3) << 17)
-                            | ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(da), "l"(db), "r"(kIdesc), "r"(accumulate));
-}
-
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+constexpr uint32_t kIdesc = make_idesc_f16(BM, BN);
 
 // ------------------------------------------------------------ kernel
 // Tile order: groups of kGroupN column tiles, row tiles fastest within a group,
@@ -223,14 +135,14 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_const
                 for (int k = 0; k < BK / 16; k++) {
                     const uint64_t da = smem_desc_sw128(sa + k * 32);
                     const uint64_t db = smem_desc_sw128(sa + A_BYTES + k * 32);
-                    umma_f16(acc, da, db, (kb | k) != 0);
+                    umma_f16(acc, da, db, kIdesc, (kb | k) != 0);
                 }
                 umma_commit(smem_u32(&bars[STAGES + s]));   // frees the stage when these MMAs finish
             }
             if (ok) umma_commit(smem_u32(&acc_full[b]));   // this tile's accumulator is complete
         }
         umma_commit(smem_u32(mma_done));                   // every MMA this thread issued has finished
-        mbar_wait(smem_u32(mma_done), 0, err, s_abort);
+        mbar_drain(smem_u32(mma_done), 0);                 // even after an abort: TMEM is freed below
     } else if (warp >= 2) {
         // ---------------- epilogue: one output row per thread
         const int quarter = warp & 3;                    // TMEM lanes this warp may access
@@ -301,9 +213,7 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_const
         // drain: wait (bounded) for the copies this CTA issued into stages nobody consumed
         const int issued = *s_issued;
         for (int g = issued - STAGES > 0 ? issued - STAGES : 0; g < issued; g++) {
-            const uint32_t bar = smem_u32(&bars[g % STAGES]);
-            for (uint32_t k = 0; k < kWaitLimit && !mbar_try_wait(bar, (g / STAGES) & 1); k++) {
-            }
+            mbar_drain(smem_u32(&bars[g % STAGES]), (g / STAGES) & 1);
         }
     }
     __syncthreads();
@@ -313,41 +223,9 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_const
     }
 }
 
-// ------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// 2-D fp16 tensor [rows][cols] (cols contiguous), box [box_rows][64 cols], 128-byte swizzle.
-bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
-bool prefill_supported() { return encode_fn() != nullptr; }
+bool prefill_supported() { return tma_encode_available(); }
 
 cudaError_t launch_prefill(const uint16_t *u, const uint16_t *wt, int64_t M, int IC, int OC, const uint16_t *rout,
                            const uint16_t *s_out, uint16_t *out, int64_t ldo, int32_t *err, cudaStream_t s,
@@ -356,7 +234,7 @@ cudaError_t launch_prefill(const uint16_t *u, const uint16_t *wt, int64_t M, int
     if (M <= 0 || IC % BK || OC % kHad || M > INT32_MAX) return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(u) | reinterpret_cast<uintptr_t>(wt)) & 15u) return cudaErrorInvalidValue;
     CUtensorMap tm_u, tm_w;
-    if (!make_map(&tm_u, u, M, IC, BM) || !make_map(&tm_w, wt, OC, IC, BN)) return cudaErrorInvalidValue;
+    if (!make_map_f16(&tm_u, u, M, IC, BM) || !make_map_f16(&tm_w, wt, OC, IC, BN)) return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

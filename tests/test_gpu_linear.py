@@ -217,3 +217,65 @@ def test_shards_call_equals_per_shard_calls(M):
         ref = oracle.linear_f64(x, s.code, s.K, s.s_in, s.rin, s.rout, s.s_out)
         assert_rows_close(as_f64(got)[:, col:col + s.OC], ref)
         col += s.OC
+
+
+# ---------------------------------------------------------------- fused tensor-core path (8 < M <= 128)
+
+@pytest.mark.parametrize("M", (9, 16, 17, 31, 64, 65, 100, 128))
+def test_fused_parity_split_and_whole_groups(M, monkeypatch):
+    # 160 column groups of 8 stages over one persistent grid: some groups are
+    # reduced across CTAs through the split-K slab, others owned by one CTA;
+    # M spans all four accumulator widths (16, 32, 64, 128 rows)
+    monkeypatch.setenv("EXL3_FORCE_MODE", "fused")
+    K = 2 + M % 3
+    x, sh = syn.linear_case(300 + M, M, 512, 20480, K)
+    ws = m.workspace(m.exl3_linear_workspace_bytes(M, sh.IC, sh.OC))
+    y = run_linear(x, sh, ws)
+    ref = oracle.linear_f64(x, sh.code, K, sh.s_in, sh.rin, sh.rout, sh.s_out)
+    assert_rows_close(as_f64(y), ref)
+    assert m.exl3_workspace_error(ws) == 0
+
+
+@pytest.mark.parametrize("mode", ("decode", "fused", "prefill"))
+def test_forced_modes_agree_with_oracle(mode, monkeypatch):
+    # every GEMM path serves the same M; each must match the oracle
+    monkeypatch.setenv("EXL3_FORCE_MODE", mode)
+    x, sh = syn.linear_case(77, 24, 1024, 768, 3)
+    y = run_linear(x, sh)
+    ref = oracle.linear_f64(x, sh.code, 3, sh.s_in, sh.rin, sh.rout, sh.s_out)
+    assert_rows_close(as_f64(y), ref)
+
+
+@pytest.mark.parametrize("M", (12, 96))
+def test_gemm_into_fused_from_caller_activations(M, monkeypatch):
+    # caller-supplied pre-transformed activations go straight to the fused GEMM
+    monkeypatch.setenv("EXL3_FORCE_MODE", "fused")
+    x, sh = syn.linear_case(500 + M, M, 1024, 1280, 4)
+    c, s_in, rin, rout, s_out = shard_dev(sh)
+    u = m.exl3_pretransform(dev(x, torch.bfloat16), s_in, rin)
+    out = torch.full((M, 1280 + 128), NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    ws = m.workspace(m.exl3_linear_workspace_bytes(M, 1024, 1280))
+    m.exl3_gemm_into(u, c, 4, rout, s_out, out, 128, ws)
+    torch.cuda.synchronize()
+    assert np.all(bits(out)[:, :128] == NAN_BF16)
+    ref = oracle.linear_f64(x, sh.code, 4, sh.s_in, sh.rin, sh.rout, sh.s_out)
+    assert_rows_close(as_f64(out)[:, 128:], ref)
+
+
+def test_fused_repeated_calls_deterministic():
+    # the split-K counters reset themselves: back-to-back calls give identical bits
+    x, sh = syn.linear_case(91, 40, 512, 20480, 3)
+    ws = m.workspace(m.exl3_linear_workspace_bytes(40, 512, 20480))
+    a = bits(run_linear(x, sh, ws))
+    b = bits(run_linear(x, sh, ws))
+    assert np.array_equal(a, b)
+
+
+def test_fused_single_stage_segments(monkeypatch):
+    # IC = 128: two stages per column group, so CTAs at group boundaries get
+    # one-stage segments that only one of the two MMA issuers accumulates
+    monkeypatch.setenv("EXL3_FORCE_MODE", "fused")
+    x, sh = syn.linear_case(93, 20, 128, 128 * 300, 2)
+    y = run_linear(x, sh)
+    ref = oracle.linear_f64(x, sh.code, 2, sh.s_in, sh.rin, sh.rout, sh.s_out)
+    assert_rows_close(as_f64(y), ref)

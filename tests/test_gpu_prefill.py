@@ -40,7 +40,7 @@ def run(x, sh, out=None, col0=0):
     return out
 
 
-@pytest.mark.parametrize("M,OC,K", [(33, 384, 2), (300, 640, 3), (1000, 256, 4), (129, 1152, 2)])
+@pytest.mark.parametrize("M,OC,K", [(161, 384, 2), (300, 640, 3), (1000, 256, 4), (129, 1152, 2)])
 def test_prefill_ragged(M, OC, K):
     x, sh = syn.linear_case(500 + M, M, 1024, OC, K, outlier_frac=0.01)
     y = run(x, sh)
