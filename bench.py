@@ -160,7 +160,7 @@ def t16(torch, a, dev, dtype):
 # ------------------------------------------------------------------ workloads
 def gemm_path(M):
     """The GEMM path the library takes for M rows (the C-ABI's default choice)."""
-    return "decode" if M <= 32 else ("fused" if M <= 128 else "prefill")
+    return "decode" if M <= 16 else ("fused" if M <= 128 else "prefill")
 
 
 def linear_launches(M, n_shards):

@@ -79,7 +79,7 @@ int32_t *workspace_counters(void *base) {
 // The boundaries are where the measured times of neighbouring paths cross on
 // the 5120 -> 2 x 17408 projection.  EXL3_FORCE_MODE=decode|fused|prefill
 // overrides the choice (read on every call).
-constexpr int64_t kDecodeModeMaxRows = kDecodeMaxRows;
+constexpr int64_t kDecodeModeMaxRows = 16;
 enum class GemmMode { kDecode, kFused, kPrefill };
 
 static int forced_mode() {

@@ -17,14 +17,16 @@
 // adds.  Code words and B tiles arrive through rings of their own, deep enough
 // to cover HBM and TMA latency.
 //
-// Warp roles (512 threads, one CTA per SM):
+// Warp roles (640 threads, one CTA per SM):
 //   warp 0        TMEM allocation; MMA issuer for even stages
 //   warp 1        TMA producer of the B tiles (released in chunks of 2 stages)
 //   warp 2        TMA producer of the code ring (one 3-D box per stage)
 //   warp 3        MMA issuer for odd stages
 //   warps 4..7    epilogue: TMEM -> registers -> split-K slab or shared
 //                 transpose -> per-row Had128 -> rout, s_out -> bf16
-//   warps 8..15   decoders: group 0 (warps 8..11) even stages, group 1 odd
+//   warps 8..19   decoders: three groups of four warps; group p decodes the
+//                 stages g with g % 3 == p (three warps per sub-partition, so
+//                 one group's ring waits overlap the others' arithmetic)
 // Work units (column group x stage) of all shards are split evenly over the
 // persistent grid; the accumulators are double-buffered in TMEM so that the
 // epilogue of one column group overlaps the MMAs of the next.  CTAs that share
@@ -43,13 +45,14 @@ namespace exl3 {
 
 namespace {
 
-constexpr int FT_ASLOTS = 6;                       // A ring depth (three slots per decoder group)
+constexpr int FT_NGROUPS = 3;                      // decoder groups (4 warps each); group p decodes stages g % 3 == p
+constexpr int FT_ASLOTS = 6;                       // A ring depth (two slots per decoder group)
 constexpr int FT_MAX_CSTAGES = 12;                 // code ring depth (fewer at 128 rows)
 constexpr int FT_CSLOT = 4096;                     // code bytes per stage: 4 trellis rows x 8 tiles x 32K, K <= 4
 constexpr int FT_BM = 128;                         // output columns per tile (one Had128 block)
 constexpr int FT_KC = 64;                          // input channels per stage
 constexpr int FT_A_BYTES = FT_BM * FT_KC * 2;      // 16 KB
-constexpr int FT_THREADS = 512;
+constexpr int FT_THREADS = 256 + FT_NGROUPS * 128;
 constexpr int W_MMA0 = 0, W_BLOAD = 1, W_CODE = 2, W_MMA1 = 3, W_EPI = 4, W_DEC = 8;
 constexpr int FT_TSTRIDE = 144;                    // transpose buffer: 4 parts x 36 floats per row
 constexpr int FT_T_BYTES = 32 * FT_TSTRIDE * 4;
@@ -65,20 +68,23 @@ template <int NT>
 struct FtCfg {
     static constexpr int B_BYTES = NT * FT_KC * 2;                   // one stage of activations
     static constexpr int CHUNK_BYTES = 2 * B_BYTES;
-    static constexpr int CSTAGES = NT >= 128 ? 8 : FT_MAX_CSTAGES;   // code ring depth
-    static constexpr int FIXED = FT_ASLOTS * FT_A_BYTES + CSTAGES * FT_CSLOT + FT_T_BYTES + B_COUNT * 8 + 64 + 1024;
+    static constexpr int CSTAGES = NT >= 128 ? 9 : FT_MAX_CSTAGES;   // code ring depth (a multiple of the groups)
+    static constexpr int FIXED =
+        FT_ASLOTS * FT_A_BYTES + CSTAGES * FT_CSLOT + FT_T_BYTES + 4 * FT_BM + B_COUNT * 8 + 64 + 1024;
     static constexpr int FIT = (FT_SMEM_LIMIT - FIXED) / CHUNK_BYTES;
     static constexpr int BCHUNKS = FIT < FT_MAX_BCHUNKS ? FIT : FT_MAX_BCHUNKS;
     static constexpr int B_OFF = FT_ASLOTS * FT_A_BYTES;
     static constexpr int CODE_OFF = B_OFF + BCHUNKS * CHUNK_BYTES;
     static constexpr int T_OFF = CODE_OFF + CSTAGES * FT_CSLOT;
-    static constexpr int BAR_OFF = T_OFF + FT_T_BYTES;
+    static constexpr int SC_OFF = T_OFF + FT_T_BYTES;                 // the segment's rout, s_out (fp16)
+    static constexpr int BAR_OFF = SC_OFF + 2 * FT_BM * 2;
     static constexpr int SMEM = BAR_OFF + B_COUNT * 8 + 64 + 1024;
     static constexpr int BUF = NT < 32 ? 32 : NT;                    // TMEM columns per accumulator
     static constexpr int TMEM_COLS = 4 * BUF;                        // 2 issuers x 2 buffers
     static constexpr uint32_t IDESC = make_idesc_f16(FT_BM, NT);
     static_assert(BCHUNKS >= 2 && SMEM <= FT_SMEM_LIMIT, "shared-memory plan does not fit");
     static_assert(TMEM_COLS <= 512, "tensor memory plan does not fit");
+    static_assert(CSTAGES % FT_NGROUPS == 0 && FT_ASLOTS % FT_NGROUPS == 0, "rings must rotate with the groups");
 };
 
 // Stage g of a CTA is work unit f0 + g: column group gi = unit / ST, stage
@@ -119,21 +125,30 @@ __device__ __forceinline__ void lds_quarter(uint32_t (&w)[2 * K], uint32_t addr)
     }
 }
 
-// One decoder thread's share of a stage: quarter q (tile rows 4q..4q+3, all 16
+// A decoder thread's share of a stage is quarter q (tile rows 4q..4q+3, all 16
 // columns) of tile (kt, oc_tile).  Tile column c is operand row c*8 + oc_tile;
 // its four weights are the 8 bytes at channel 16*kt + 4*q of that row, i.e.
 // 16-byte chunk 2*kt + q/2, half q%2, 128-byte swizzled (chunk ^ row % 8).
 // oc_tile is spread over the lanes so that each half-warp's 8-byte stores hit
 // 16 distinct bank pairs.
+
+// Wait for a stage's code, load this thread's quarter, release the ring slot.
 template <int K>
-__device__ __forceinline__ bool ft_decode_stage(const FusedArgs &a, uint32_t code_slot, uint32_t cempty,
-                                                uint32_t empty, uint32_t empty_parity, uint32_t full,
-                                                uint32_t a_base, int kt, int oc_tile, int q, int lane,
-                                                volatile int *abort) {
-    uint32_t w[2 * K];
+__device__ __forceinline__ bool ft_fetch(const FusedArgs &a, uint32_t (&w)[2 * K], uint32_t cfull, uint32_t cph,
+                                         uint32_t cempty, uint32_t code_slot, int kt, int oc_tile, int q, int lane,
+                                         volatile int *abort) {
+    if (!__all_sync(kFull, mbar_wait(cfull, cph, a.err, abort))) return false;
     lds_quarter<K>(w, code_slot + (uint32_t)(kt * 256 * K + oc_tile * 32 * K + q * 8 * K));
     __syncwarp();
     if (lane == 0) mbar_arrive(cempty);
+    return true;
+}
+
+// Decode a quarter held in registers into its A slot, then publish it to the MMA issuer.
+template <int K>
+__device__ __forceinline__ bool ft_decode_quarter(const FusedArgs &a, const uint32_t (&w)[2 * K], uint32_t empty,
+                                                  uint32_t empty_parity, uint32_t full, uint32_t a_base, int kt,
+                                                  int oc_tile, int q, int lane, volatile int *abort) {
     if (!__all_sync(kFull, mbar_wait(empty, empty_parity, a.err, abort))) return false;
     QuarterStream<K> st;
     st.build(w, quarter_prev_word(w[2 * K - 1], lane));
@@ -157,26 +172,29 @@ __device__ __forceinline__ bool ft_decode_stage(const FusedArgs &a, uint32_t cod
     return true;
 }
 
-// Ring positions of a decoder group: code slot / phase, A slot / "empty" parity.
+// Ring positions of a decoder group: code slot / phase and A slot / the parity
+// its "empty" wait takes, of the group's next stage.
 struct DecState {
     int cs, cph, slot, eph;
 };
 
-// Decode this group's stages g, g + 2, ... below end, all of one shard (one K).
-// g is left at the first stage not decoded.
+// Decode this group's stages g, g + FT_NGROUPS, ... below end, all of one shard
+// (one K).  g is left at the first stage not decoded.
 template <int K, int CSTAGES>
 __device__ __forceinline__ bool ft_decode_run(const FusedArgs &a, uint32_t code_base, uint32_t a_ring, uint32_t bar0,
                                               int &g, int end, DecState &ds, int kt, int oc_tile, int q, int lane,
                                               volatile int *abort) {
-    for (; g < end; g += 2) {
-        if (!__all_sync(kFull, mbar_wait(bar0 + 8u * (B_CFULL + ds.cs), ds.cph, a.err, abort))) return false;
-        if (!ft_decode_stage<K>(a, code_base + ds.cs * FT_CSLOT, bar0 + 8u * (B_CEMPTY + ds.cs),
-                                bar0 + 8u * (B_EMPTY + ds.slot), ds.eph, bar0 + 8u * (B_FULL + ds.slot),
-                                a_ring + ds.slot * FT_A_BYTES, kt, oc_tile, q, lane, abort))
+    for (; g < end; g += FT_NGROUPS) {
+        uint32_t w[2 * K];
+        if (!ft_fetch<K>(a, w, bar0 + 8u * (B_CFULL + ds.cs), ds.cph, bar0 + 8u * (B_CEMPTY + ds.cs),
+                         code_base + ds.cs * FT_CSLOT, kt, oc_tile, q, lane, abort))
             return false;
-        ds.cs += 2;
+        ds.cs += FT_NGROUPS;
         if (ds.cs >= CSTAGES) { ds.cs -= CSTAGES; ds.cph ^= 1; }
-        ds.slot += 2;
+        if (!ft_decode_quarter<K>(a, w, bar0 + 8u * (B_EMPTY + ds.slot), ds.eph, bar0 + 8u * (B_FULL + ds.slot),
+                                  a_ring + ds.slot * FT_A_BYTES, kt, oc_tile, q, lane, abort))
+            return false;
+        ds.slot += FT_NGROUPS;
         if (ds.slot >= FT_ASLOTS) { ds.slot -= FT_ASLOTS; ds.eph ^= 1; }
     }
     return true;
@@ -190,6 +208,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *sbase = smem_raw + (base - raw);
     float *T = reinterpret_cast<float *>(sbase + C::T_OFF);
+    uint16_t *s_scale = reinterpret_cast<uint16_t *>(sbase + C::SC_OFF);   // [0, 128) rout, [128, 256) s_out
     uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + C::BAR_OFF);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + B_COUNT);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
@@ -330,7 +349,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
             }
         }
     } else if (warp >= W_DEC) {
-        // ---------------- decoders: group p decodes the stages of parity p
+        // ---------------- decoders: group p decodes the stages g % FT_NGROUPS == p
         const int p = (warp - W_DEC) >> 2;
         const int kt = (warp - W_DEC) & 3;
         const int oc_tile = ((lane >> 2) & 3) * 2 + (lane >> 4);
@@ -378,6 +397,9 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
             const FusedShard &sh = a.sh[si.shard];
             const int G = si.gi - sh.g0;
             const int j = si.gi - gi0, b = j & 1;
+            // this column group's output scales, fetched while the MMAs finish
+            s_scale[et] = __ldg(sh.rout + G * kHad + et);
+            s_scale[FT_BM + et] = __ldg(sh.s_out + G * kHad + et);
             const bool have = mbar_wait(bar(B_ACCF + b), (j >> 1) & 1, a.err, s_abort);
             tc_fence_after();
             if (!named_bar_and(1, 128, have)) break;
@@ -422,14 +444,26 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
             }
             for (int c0 = 0; c0 < rows; c0 += 32) {
                 float v[32];
-                if (split) {
+                if (split && c_last == c_first + 1) {
+                    // two contributors (the common case): both partials' rows in
+                    // flight at once; a two-term sum does not depend on order
+                    const float *s0 = a.partials + (int64_t)(c_first + si.gi) * frag + (int64_t)c0 * FT_BM + r;
+                    const float *s1 = a.partials + (int64_t)(c_last + si.gi) * frag + (int64_t)c0 * FT_BM + r;
 #pragma unroll
-                    for (int i = 0; i < 32; i++) {
-                        float s = 0.f;
-                        if (c0 + i < rows)
-                            for (int cc = c_first; cc <= c_last; cc++)
-                                s += __ldcg(a.partials + (int64_t)(cc + si.gi) * frag + (int64_t)(c0 + i) * FT_BM + r);
-                        v[i] = s;
+                    for (int i = 0; i < 32; i++) v[i] = c0 + i < rows ? __ldcg(s0 + i * FT_BM) : 0.f;
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        if (c0 + i < rows) v[i] += __ldcg(s1 + i * FT_BM);
+                } else if (split) {
+                    // CTA order outermost: each CTA's 32 rows load in parallel; the
+                    // sum runs in ascending CTA order (deterministic)
+#pragma unroll
+                    for (int i = 0; i < 32; i++) v[i] = 0.f;
+                    for (int cc = c_first; cc <= c_last; cc++) {
+                        const float *src = a.partials + (int64_t)(cc + si.gi) * frag + (int64_t)c0 * FT_BM + r;
+#pragma unroll
+                        for (int i = 0; i < 32; i++)
+                            if (c0 + i < rows) v[i] += __ldcg(src + i * FT_BM);
                     }
                 } else {
                     load_acc(c0, v);
@@ -472,8 +506,9 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                     uint16_t *dst = a.out + (int64_t)nrow * a.ldo + sh.col0 + colb;
 #pragma unroll
                     for (int jj = 0; jj < 8; jj++) {
-                        const uint2 rv = __ldg(reinterpret_cast<const uint2 *>(sh.rout + colb + 16 * jj));
-                        const uint2 sv = __ldg(reinterpret_cast<const uint2 *>(sh.s_out + colb + 16 * jj));
+                        const int cl = 4 * part + 16 * jj;     // column within the block
+                        const uint2 rv = *reinterpret_cast<const uint2 *>(s_scale + cl);
+                        const uint2 sv = *reinterpret_cast<const uint2 *>(s_scale + FT_BM + cl);
                         const uint32_t rw[2] = {rv.x, rv.y}, sw[2] = {sv.x, sv.y};
                         uint32_t o2[2];
 #pragma unroll

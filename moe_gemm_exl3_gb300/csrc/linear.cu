@@ -348,11 +348,24 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
             do_epilogue = *s_last;
             if (do_epilogue) {
                 __threadfence();
-                for (int i = threadIdx.x; i < FRAG; i += blockDim.x) {
-                    float sum = 0.f;
-                    for (int cc = c_first; cc <= c_last; cc++)
-                        sum += __ldcg(a.partials + (int64_t)(cc + gi) * FRAG + i);
-                    red[i] = sum;
+                // CTA order outermost so each CTA's elements load in parallel; the
+                // sum runs in ascending CTA order (deterministic)
+                constexpr int PER = (FRAG + kDecodeWarps * 32 - 1) / (kDecodeWarps * 32);
+                float sum[PER];
+#pragma unroll
+                for (int k = 0; k < PER; k++) sum[k] = 0.f;
+                for (int cc = c_first; cc <= c_last; cc++) {
+                    const float *src = a.partials + (int64_t)(cc + gi) * FRAG;
+#pragma unroll
+                    for (int k = 0; k < PER; k++) {
+                        const int i = threadIdx.x + k * kDecodeWarps * 32;
+                        if (i < FRAG) sum[k] += __ldcg(src + i);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < PER; k++) {
+                    const int i = threadIdx.x + k * kDecodeWarps * 32;
+                    if (i < FRAG) red[i] = sum[k];
                 }
                 if (threadIdx.x == 0) a.counters[gi] = 0;
                 __syncthreads();
