@@ -221,8 +221,11 @@ class GateUp:
         return {"bound": "hbm", "kernel": kernel + " (gate K=2 + up K=3 in one call)",
                 "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
-                "traffic": (profile_traffic("decode_gemm_gate_up_m8.json", ["linear.cu", "common.cuh"])
-                            if gemm_path(self.M) == "decode" else None),
+                "traffic": {"decode": lambda: profile_traffic(f"decode_gemm_gate_up_m{self.M}.json",
+                                                              ["linear.cu", "common.cuh"]),
+                            "fused": lambda: profile_traffic(f"fused_gemm_gate_up_m{self.M}.json",
+                                                             ["fused_tc.cu", "tc_ptx.cuh", "common.cuh"]),
+                            "prefill": lambda: None}[gemm_path(self.M)](),
                 "per_launch_us": round(ms * 1e3, 2), "algorithmic_bytes_per_launch": alg,
                 "code_GBps": round(sum(self.code_bytes(K) for K in self.KS) / (ms * 1e-3) / 1e9, 1)}
 
@@ -292,7 +295,7 @@ class Prefill:
         return {"bound": "tensor", "kernel": "prefill_gemm_kernel (tcgen05 128x256 tiles)",
                 "achieved": round(a, 1), "peak": tf, "unit": "TFLOP/s", "frac": round(a / tf, 4),
                 "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops; fp16 has the same dense rate)",
-                "traffic": profile_traffic("prefill_gemm_m8192.json", ["prefill.cu"]),
+                "traffic": profile_traffic(f"prefill_gemm_m{self.M}.json", ["prefill.cu", "tc_ptx.cuh"]),
                 "per_launch_us": round(ms * 1e3, 1), "reconstruct_us": round(ms_rec * 1e3, 1),
                 "algorithmic_flops_per_launch": fl}
 

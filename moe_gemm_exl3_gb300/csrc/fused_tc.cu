@@ -443,33 +443,49 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                 if (et == 0) a.counters[si.gi] = 0;
             }
             for (int c0 = 0; c0 < rows; c0 += 32) {
-                float v[32];
-                if (split && c_last == c_first + 1) {
-                    // two contributors (the common case): both partials' rows in
-                    // flight at once; a two-term sum does not depend on order
-                    const float *s0 = a.partials + (int64_t)(c_first + si.gi) * frag + (int64_t)c0 * FT_BM + r;
-                    const float *s1 = a.partials + (int64_t)(c_last + si.gi) * frag + (int64_t)c0 * FT_BM + r;
+                if (split) {
+                    // sum the contributors' slabs for rows c0 .. c0 + 31 (32 x 128
+                    // floats): thread et takes float4 f = et + 128 k, coalesced; two
+                    // contributors' loads in flight at a time, added in ascending
+                    // CTA order (the same order whichever CTA finishes last)
+                    const float4 *pbase = reinterpret_cast<const float4 *>(a.partials + (int64_t)c0 * FT_BM);
 #pragma unroll
-                    for (int i = 0; i < 32; i++) v[i] = c0 + i < rows ? __ldcg(s0 + i * FT_BM) : 0.f;
+                    for (int kb = 0; kb < 8; kb += 4) {
+                        float4 acc[4];
 #pragma unroll
-                    for (int i = 0; i < 32; i++)
-                        if (c0 + i < rows) v[i] += __ldcg(s1 + i * FT_BM);
-                } else if (split) {
-                    // CTA order outermost: each CTA's 32 rows load in parallel; the
-                    // sum runs in ascending CTA order (deterministic)
+                        for (int k = 0; k < 4; k++) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int cc = c_first; cc <= c_last; cc += 2) {
+                            const bool two = cc + 1 <= c_last;
+                            const float4 *p0 = pbase + (int64_t)(cc + si.gi) * (frag / 4);
+                            const float4 *p1 = p0 + frag / 4;
+                            float4 t0[4], t1[4];
 #pragma unroll
-                    for (int i = 0; i < 32; i++) v[i] = 0.f;
-                    for (int cc = c_first; cc <= c_last; cc++) {
-                        const float *src = a.partials + (int64_t)(cc + si.gi) * frag + (int64_t)c0 * FT_BM + r;
+                            for (int k = 0; k < 4; k++) {
+                                const int f = et + 128 * (kb + k);
+                                const bool live = c0 + (f >> 5) < rows;
+                                t0[k] = live ? __ldcg(p0 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+                                t1[k] = live && two ? __ldcg(p1 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
 #pragma unroll
-                        for (int i = 0; i < 32; i++)
-                            if (c0 + i < rows) v[i] += __ldcg(src + i * FT_BM);
+                            for (int k = 0; k < 4; k++) {
+                                acc[k].x += t0[k].x; acc[k].y += t0[k].y; acc[k].z += t0[k].z; acc[k].w += t0[k].w;
+                                if (two) {
+                                    acc[k].x += t1[k].x; acc[k].y += t1[k].y; acc[k].z += t1[k].z; acc[k].w += t1[k].w;
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; k++) {
+                            const int f = et + 128 * (kb + k), row = f >> 5, cq = f & 31;   // columns 4 cq .. 4 cq + 3
+                            *reinterpret_cast<float4 *>(T + row * FT_TSTRIDE + (cq >> 3) * 36 + 4 * (cq & 7)) = acc[k];
+                        }
                     }
                 } else {
+                    float v[32];
                     load_acc(c0, v);
-                }
 #pragma unroll
-                for (int i = 0; i < 32; i++) T[i * FT_TSTRIDE + (r >> 5) * 36 + (r & 31)] = v[i];
+                    for (int i = 0; i < 32; i++) T[i * FT_TSTRIDE + (r >> 5) * 36 + (r & 31)] = v[i];
+                }
                 named_bar(1, 128);
                 // row c0 + ti, values of operand rows 32*part .. 32*part + 31
                 float x[32];
