@@ -82,7 +82,7 @@ int32_t *workspace_counters(void *base) {
 constexpr int64_t kDecodeModeMaxRows = 16;
 enum class GemmMode { kDecode, kFused, kPrefill };
 
-static int forced_mode() {
+int forced_mode() {
     const char *f = std::getenv("EXL3_FORCE_MODE");
     if (!f) return 0;
     if (!std::strcmp(f, "decode")) return 1;

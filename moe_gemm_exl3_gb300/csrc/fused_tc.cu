@@ -58,6 +58,7 @@ constexpr int FT_TSTRIDE = 144;                    // transpose buffer: 4 parts 
 constexpr int FT_T_BYTES = 32 * FT_TSTRIDE * 4;
 constexpr int FT_MAX_BCHUNKS = 12;                 // B ring: chunks of 2 stages
 constexpr int FT_SMEM_LIMIT = 232448;              // opt-in shared memory per CTA
+constexpr int kFtMaxEntries = 32;                  // rows mode: entries one CTA may touch (cached in shared memory)
 // barriers
 constexpr int B_FULL = 0, B_EMPTY = B_FULL + FT_ASLOTS, B_BFULL = B_EMPTY + FT_ASLOTS,
               B_BEMPTY = B_BFULL + FT_MAX_BCHUNKS, B_CFULL = B_BEMPTY + FT_MAX_BCHUNKS,
@@ -69,15 +70,16 @@ struct FtCfg {
     static constexpr int B_BYTES = NT * FT_KC * 2;                   // one stage of activations
     static constexpr int CHUNK_BYTES = 2 * B_BYTES;
     static constexpr int CSTAGES = NT >= 128 ? 9 : FT_MAX_CSTAGES;   // code ring depth (a multiple of the groups)
-    static constexpr int FIXED =
-        FT_ASLOTS * FT_A_BYTES + CSTAGES * FT_CSLOT + FT_T_BYTES + 4 * FT_BM + B_COUNT * 8 + 64 + 1024;
+    static constexpr int FIXED = FT_ASLOTS * FT_A_BYTES + CSTAGES * FT_CSLOT + FT_T_BYTES + 4 * FT_BM +
+                                 kFtMaxEntries * (int)sizeof(GroupEntry) + B_COUNT * 8 + 64 + 1024;
     static constexpr int FIT = (FT_SMEM_LIMIT - FIXED) / CHUNK_BYTES;
     static constexpr int BCHUNKS = FIT < FT_MAX_BCHUNKS ? FIT : FT_MAX_BCHUNKS;
     static constexpr int B_OFF = FT_ASLOTS * FT_A_BYTES;
     static constexpr int CODE_OFF = B_OFF + BCHUNKS * CHUNK_BYTES;
     static constexpr int T_OFF = CODE_OFF + CSTAGES * FT_CSLOT;
     static constexpr int SC_OFF = T_OFF + FT_T_BYTES;                 // the segment's rout, s_out (fp16)
-    static constexpr int BAR_OFF = SC_OFF + 2 * FT_BM * 2;
+    static constexpr int ENT_OFF = SC_OFF + 2 * FT_BM * 2;            // rows mode: cached entries
+    static constexpr int BAR_OFF = ENT_OFF + kFtMaxEntries * (int)sizeof(GroupEntry);
     static constexpr int SMEM = BAR_OFF + B_COUNT * 8 + 64 + 1024;
     static constexpr int BUF = NT < 32 ? 32 : NT;                    // TMEM columns per accumulator
     static constexpr int TMEM_COLS = 4 * BUF;                        // 2 issuers x 2 buffers
@@ -89,26 +91,18 @@ struct FtCfg {
 
 // Stage g of a CTA is work unit f0 + g: column group gi = unit / ST, stage
 // st = unit % ST.  A segment is the run of stages of one column group; its
-// accumulator is buffer (gi - first group of the CTA) & 1.  Every role walks its
-// stages with a cursor (no division per stage) that also tracks the shard.
-struct Cursor {
-    int gi, st, shard, shard_end;   // shard_end: first column group of the next shard
-
-    __device__ __forceinline__ void init(const FusedArgs &a, int gi_, int st_) {
-        gi = gi_;
-        st = st_;
-        shard = 0;
-        while (shard + 1 < a.n_shards && a.sh[shard + 1].g0 <= gi) shard++;
-        shard_end = shard + 1 < a.n_shards ? a.sh[shard + 1].g0 : 0x7FFFFFFF;
-    }
-    __device__ __forceinline__ void step(const FusedArgs &a, int ST) {
-        if (++st < ST) return;
-        st = 0;
-        if (++gi < shard_end) return;
-        shard++;
-        shard_end = shard + 1 < a.n_shards ? a.sh[shard + 1].g0 : 0x7FFFFFFF;
-    }
+// accumulator is buffer (gi - first group of the CTA) & 1.  What a role needs
+// about a segment's column group:
+struct SegDesc {
+    const char *code;                // the code tensor (bytes)
+    const uint16_t *post, *post2;    // dense: rout, s_out; rows mode: the post-scale, nullptr
+    int K, TO, G;                    // bits per weight, tiles per trellis row, column group in the tensor
+    int u_row;                       // first activation row
+    int rows;                        // rows of the segment
+    int64_t out0;                    // dense: first output column; rows mode: first output row
+    int tm;                          // dense: code tensor map index; rows mode: -1 (bulk copies)
 };
+
 
 template <int K>
 __device__ __forceinline__ void lds_quarter(uint32_t (&w)[2 * K], uint32_t addr) {
@@ -200,7 +194,7 @@ __device__ __forceinline__ bool ft_decode_run(const FusedArgs &a, uint32_t code_
     return true;
 }
 
-template <int NT>
+template <int NT, bool ROWS>
 __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_constant__ FusedArgs a) {
     using C = FtCfg<NT>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -209,6 +203,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
     unsigned char *sbase = smem_raw + (base - raw);
     float *T = reinterpret_cast<float *>(sbase + C::T_OFF);
     uint16_t *s_scale = reinterpret_cast<uint16_t *>(sbase + C::SC_OFF);   // [0, 128) rout, [128, 256) s_out
+    GroupEntry *s_ent = reinterpret_cast<GroupEntry *>(sbase + C::ENT_OFF);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + C::BAR_OFF);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + B_COUNT);
     volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
@@ -255,14 +250,76 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     int n_groups = 0;
-    for (int i = 0; i < a.n_shards; i++) n_groups += a.sh[i].OC / kHad;
+    if constexpr (ROWS) {
+        n_groups = *a.n_entries_dev * a.groups_per_entry;
+    } else {
+        for (int i = 0; i < a.n_shards; i++) n_groups += a.sh[i].OC / kHad;
+    }
     const int64_t total = (int64_t)n_groups * ST;
     const int nCTA = (int64_t)gridDim.x < total ? (int)gridDim.x : (int)total;
     const int c = blockIdx.x;
     const int64_t f0 = c < nCTA ? (int64_t)c * total / nCTA : 0;
-    const int n = c < nCTA ? (int)((int64_t)(c + 1) * total / nCTA - f0) : 0;   // stages of this CTA
+    int n = c < nCTA ? (int)((int64_t)(c + 1) * total / nCTA - f0) : 0;   // stages of this CTA
     const int gi0 = (int)(f0 / ST), st0 = (int)(f0 - (int64_t)gi0 * ST);
     int issued = 0;   // copies issued by a producer thread (drained on abort)
+
+    // rows mode: the entries this CTA's column groups belong to, cached in shared memory
+    int e_first = 0;
+    if constexpr (ROWS) {
+        e_first = gi0 / a.groups_per_entry;
+        int e_cnt = n > 0 ? (gi0 + (st0 + n - 1) / ST) / a.groups_per_entry - e_first + 1 : 0;
+        if (e_cnt > kFtMaxEntries) {
+            // the host sizes the grid so that this cannot happen; do no work rather than overrun
+            if (threadIdx.x == 0) record_error(a.err, kErrRouteOverflow);
+            n = 0;
+            e_cnt = 0;
+        }
+        static_assert(sizeof(GroupEntry) % 8 == 0, "entries are copied in 8-byte words");
+        for (int i = threadIdx.x; i < e_cnt * (int)(sizeof(GroupEntry) / 8); i += blockDim.x)
+            reinterpret_cast<long long *>(s_ent)[i] = __ldg(reinterpret_cast<const long long *>(a.entries + e_first) + i);
+        __syncthreads();
+    }
+    // Everything a role needs about column group gi (one segment).
+    auto seg_desc = [&](int gi) -> SegDesc {
+        SegDesc d;
+        if constexpr (ROWS) {
+            const int e = gi / a.groups_per_entry;
+            const GroupEntry &ge = s_ent[e - e_first];
+            d.code = reinterpret_cast<const char *>(ge.code);
+            d.post = ge.post;
+            d.post2 = nullptr;
+            d.K = ge.K;
+            d.TO = ge.OC / kTile;
+            d.G = gi - e * a.groups_per_entry;
+            d.u_row = ge.u_row0;
+            d.rows = ge.nrows;
+            d.out0 = ge.out_off;
+            d.tm = -1;
+        } else {
+            int sidx = 0;
+            while (sidx + 1 < a.n_shards && a.sh[sidx + 1].g0 <= gi) sidx++;
+            const FusedShard &sh = a.sh[sidx];
+            d.code = reinterpret_cast<const char *>(sh.code);
+            d.post = sh.rout;
+            d.post2 = sh.s_out;
+            d.K = sh.K;
+            d.TO = sh.OC / kTile;
+            d.G = gi - sh.g0;
+            d.u_row = sidx * M;
+            d.rows = M;
+            d.out0 = sh.col0;
+            d.tm = sidx;
+        }
+        return d;
+    };
+    // Segment walk: segment j holds stages [lo, hi) of column group gi0 + j, starting at stage st_lo.
+#define FT_FOR_SEGMENTS(...)                                                                  \
+    for (int lo_ = 0, hi_ = (ST - st0 < n ? ST - st0 : n), j_ = 0; lo_ < n;                  \
+         lo_ = hi_, hi_ = (hi_ + ST < n ? hi_ + ST : n), j_++) {                              \
+        const int lo = lo_, hi = hi_, jseg = j_, gi = gi0 + j_, st_lo = j_ == 0 ? st0 : 0;    \
+        (void)lo; (void)hi; (void)jseg; (void)gi; (void)st_lo;                                \
+        __VA_ARGS__                                                                           \
+    }
 
     if (warp == W_MMA0 || warp == W_MMA1) {
         // ---------------- MMA issuers: stages of parity p into accumulator p
@@ -320,33 +377,53 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
     } else if (warp == W_BLOAD) {
         // ---------------- TMA producer of the B tiles, two stages per chunk
         if (lane == 0) {
-            Cursor cu;
-            cu.init(a, gi0, st0);
-            for (int g = 0; g < n; g++, cu.step(a, ST)) {
-                const int jc = g >> 1, ch = jc % C::BCHUNKS;
-                if ((g & 1) == 0) {
-                    if (!mbar_wait(bar(B_BEMPTY + ch), ((jc / C::BCHUNKS) & 1) ^ 1, a.err, s_abort)) break;
-                    mbar_expect_tx(bar(B_BFULL + ch), (g + 1 < n ? 2 : 1) * C::B_BYTES);
-                    issued++;
+            bool ok = true;
+            FT_FOR_SEGMENTS({
+                if (!ok) break;
+                const SegDesc d = seg_desc(gi);
+                for (int g = lo; g < hi; g++) {
+                    const int jc = g >> 1, ch = jc % C::BCHUNKS;
+                    if ((g & 1) == 0) {
+                        if (!mbar_wait(bar(B_BEMPTY + ch), ((jc / C::BCHUNKS) & 1) ^ 1, a.err, s_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(bar(B_BFULL + ch), (g + 1 < n ? 2 : 1) * C::B_BYTES);
+                        issued++;
+                    }
+                    tma_load_2d(base + C::B_OFF + ch * C::CHUNK_BYTES + (g & 1) * C::B_BYTES, &a.tm_u,
+                                (st_lo + g - lo) * FT_KC, d.u_row, bar(B_BFULL + ch));
                 }
-                tma_load_2d(base + C::B_OFF + ch * C::CHUNK_BYTES + (g & 1) * C::B_BYTES, &a.tm_u, cu.st * FT_KC,
-                            cu.shard * M, bar(B_BFULL + ch));
-            }
+            })
         }
     } else if (warp == W_CODE) {
-        // ---------------- TMA producer of the code ring: one 3-D box (4 tile rows x 8 tiles) per stage
+        // ---------------- producer of the code ring: per stage one 3-D TMA box (4 tile rows
+        // x 8 tiles) when the code tensor has a tensor map, else four bulk copies
         if (lane == 0) {
-            Cursor cu;
-            cu.init(a, gi0, st0);
-            for (int g = 0; g < n; g++, cu.step(a, ST)) {
-                const FusedShard &sh = a.sh[cu.shard];
-                const int cs = g % C::CSTAGES;
-                if (!mbar_wait(bar(B_CEMPTY + cs), ((g / C::CSTAGES) & 1) ^ 1, a.err, s_abort)) break;
-                mbar_expect_tx(bar(B_CFULL + cs), 1024u * (uint32_t)sh.K);
-                tma_load_3d(base + C::CODE_OFF + cs * FT_CSLOT, &a.tm_code[cu.shard], 0, 8 * (cu.gi - sh.g0),
-                            4 * cu.st, bar(B_CFULL + cs));
-                issued++;
-            }
+            bool ok = true;
+            FT_FOR_SEGMENTS({
+                if (!ok) break;
+                const SegDesc d = seg_desc(gi);
+                const uint32_t bytes = 256u * (uint32_t)d.K;        // 8 tiles of one trellis row
+                for (int g = lo; g < hi; g++) {
+                    const int cs = g % C::CSTAGES, st = st_lo + g - lo;
+                    if (!mbar_wait(bar(B_CEMPTY + cs), ((g / C::CSTAGES) & 1) ^ 1, a.err, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(bar(B_CFULL + cs), 4 * bytes);
+                    const uint32_t dst = base + C::CODE_OFF + cs * FT_CSLOT;
+                    if (d.tm >= 0) {
+                        tma_load_3d(dst, &a.tm_code[d.tm], 0, 8 * d.G, 4 * st, bar(B_CFULL + cs));
+                    } else {
+#pragma unroll
+                        for (int kt = 0; kt < 4; kt++)
+                            bulk_load(dst + kt * bytes, d.code + ((int64_t)(4 * st + kt) * d.TO + 8 * d.G) * 32 * d.K,
+                                      bytes, bar(B_CFULL + cs));
+                    }
+                    issued++;
+                }
+            })
         }
     } else if (warp >= W_DEC) {
         // ---------------- decoders: group p decodes the stages g % FT_NGROUPS == p
@@ -359,53 +436,46 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
         ds.cph = 0;
         ds.slot = p;
         ds.eph = 1;
-        // the CTA's stages split into runs of one shard (one K): decode each run
-        // with a loop specialised for its K
+        // decode this group's stages segment by segment with a loop specialised for the segment's K
         int g = p;
-        for (int si = 0; si < a.n_shards && g < n; si++) {
-            const int64_t first = (int64_t)a.sh[si].g0 * ST - f0;
-            const int64_t last = si + 1 < a.n_shards ? (int64_t)a.sh[si + 1].g0 * ST - f0 : (int64_t)n;
-            const int end = last < n ? (int)last : n;
-            if (end <= g || first >= end) continue;
+        FT_FOR_SEGMENTS({
+            if (g >= hi) continue;
+            const int K = seg_desc(gi).K;
             bool ok;
-            if (a.sh[si].K == 2)
-                ok = ft_decode_run<2, C::CSTAGES>(a, base + C::CODE_OFF, base, bar0, g, end, ds, kt, oc_tile, q, lane,
+            if (K == 2)
+                ok = ft_decode_run<2, C::CSTAGES>(a, base + C::CODE_OFF, base, bar0, g, hi, ds, kt, oc_tile, q, lane,
                                                   s_abort);
-            else if (a.sh[si].K == 3)
-                ok = ft_decode_run<3, C::CSTAGES>(a, base + C::CODE_OFF, base, bar0, g, end, ds, kt, oc_tile, q, lane,
+            else if (K == 3)
+                ok = ft_decode_run<3, C::CSTAGES>(a, base + C::CODE_OFF, base, bar0, g, hi, ds, kt, oc_tile, q, lane,
                                                   s_abort);
             else
-                ok = ft_decode_run<4, C::CSTAGES>(a, base + C::CODE_OFF, base, bar0, g, end, ds, kt, oc_tile, q, lane,
+                ok = ft_decode_run<4, C::CSTAGES>(a, base + C::CODE_OFF, base, bar0, g, hi, ds, kt, oc_tile, q, lane,
                                                   s_abort);
             if (!ok) break;
-        }
+        })
     } else {
         // ---------------- epilogue, warps 4..7 (128 threads, named barrier 1)
         const int r = (warp & 3) * 32 + lane;         // TMEM lane = operand row of this thread
         const int et = (warp - W_EPI) * 32 + lane;    // 0..127
         const int ti = et >> 2, part = et & 3;        // transpose phase: row in chunk, quarter of the block
-        const int rows = M < NT ? M : NT;
-        const int64_t frag = (int64_t)M * FT_BM;
-        Cursor si;
-        si.init(a, gi0, st0);
-        for (int g = 0; g < n; si.gi++, si.st = 0) {
-            if (si.gi >= si.shard_end) si.init(a, si.gi, 0);
-            const int seg_len = (ST - si.st) < (n - g) ? (ST - si.st) : (n - g);
-            // which issuers accumulated into this segment: parity g always, the other one if it is longer than 1
-            const bool has[2] = {(g & 1) == 0 || seg_len > 1, (g & 1) == 1 || seg_len > 1};
-            g += seg_len;
-            const FusedShard &sh = a.sh[si.shard];
-            const int G = si.gi - sh.g0;
-            const int j = si.gi - gi0, b = j & 1;
+        const int64_t frag = (int64_t)M * FT_BM;   // split-K slab slot: M (the row bound) x 128 columns
+        FT_FOR_SEGMENTS({
+            const int seg_len = hi - lo;
+            // which issuers accumulated into this segment: parity lo always, the other one if it is longer than 1
+            const bool has[2] = {(lo & 1) == 0 || seg_len > 1, (lo & 1) == 1 || seg_len > 1};
+            const SegDesc d = seg_desc(gi);
+            const int G = d.G;
+            const int rows = d.rows < NT ? d.rows : NT;
+            const int b = jseg & 1;
             // this column group's output scales, fetched while the MMAs finish
-            s_scale[et] = __ldg(sh.rout + G * kHad + et);
-            s_scale[FT_BM + et] = __ldg(sh.s_out + G * kHad + et);
-            const bool have = mbar_wait(bar(B_ACCF + b), (j >> 1) & 1, a.err, s_abort);
+            s_scale[et] = __ldg(d.post + G * kHad + et);
+            if constexpr (!ROWS) s_scale[FT_BM + et] = __ldg(d.post2 + G * kHad + et);
+            const bool have = mbar_wait(bar(B_ACCF + b), (jseg >> 1) & 1, a.err, s_abort);
             tc_fence_after();
             if (!named_bar_and(1, 128, have)) break;
             const uint32_t tb = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(2 * b * C::BUF);
             // CTAs sharing this column group
-            const int64_t x0 = (int64_t)si.gi * ST, x1 = x0 + ST - 1;
+            const int64_t x0 = (int64_t)gi * ST, x1 = x0 + ST - 1;
             const int c_first = (int)(((x0 + 1) * nCTA - 1) / total);
             const int c_last = (int)(((x1 + 1) * nCTA - 1) / total);
             const bool split = c_first != c_last;
@@ -423,7 +493,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                 }
             };
             if (split) {
-                float *slot = a.partials + (int64_t)(c + si.gi) * frag;
+                float *slot = a.partials + (int64_t)(c + gi) * frag;
                 for (int c0 = 0; c0 < rows; c0 += 32) {
                     float v[32];
                     load_acc(c0, v);
@@ -436,11 +506,11 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                 if (lane == 0) mbar_arrive(bar(B_ACCE + b));
                 __threadfence();
                 named_bar(1, 128);
-                if (et == 0) *s_last = (atomicAdd(a.counters + si.gi, 1) == c_last - c_first);
+                if (et == 0) *s_last = (atomicAdd(a.counters + gi, 1) == c_last - c_first);
                 named_bar(1, 128);
                 if (!*s_last) continue;
                 __threadfence();
-                if (et == 0) a.counters[si.gi] = 0;
+                if (et == 0) a.counters[gi] = 0;
             }
             for (int c0 = 0; c0 < rows; c0 += 32) {
                 if (split) {
@@ -456,7 +526,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                         for (int k = 0; k < 4; k++) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
                         for (int cc = c_first; cc <= c_last; cc += 2) {
                             const bool two = cc + 1 <= c_last;
-                            const float4 *p0 = pbase + (int64_t)(cc + si.gi) * (frag / 4);
+                            const float4 *p0 = pbase + (int64_t)(cc + gi) * (frag / 4);
                             const float4 *p1 = p0 + frag / 4;
                             float4 t0[4], t1[4];
 #pragma unroll
@@ -519,23 +589,38 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                 if (nrow < rows) {
                     // operand row 32*part + k holds column 16*(k % 8) + 4*part + k / 8
                     const int colb = G * kHad + 4 * part;
-                    uint16_t *dst = a.out + (int64_t)nrow * a.ldo + sh.col0 + colb;
+                    if constexpr (ROWS) {
+                        // fp32 rows: y = Had128(v) * post
+                        float *dst = a.out_rows + (int64_t)(d.out0 + nrow) * a.OC_rows + colb;
 #pragma unroll
-                    for (int jj = 0; jj < 8; jj++) {
-                        const int cl = 4 * part + 16 * jj;     // column within the block
-                        const uint2 rv = *reinterpret_cast<const uint2 *>(s_scale + cl);
-                        const uint2 sv = *reinterpret_cast<const uint2 *>(s_scale + FT_BM + cl);
-                        const uint32_t rw[2] = {rv.x, rv.y}, sw[2] = {sv.x, sv.y};
-                        uint32_t o2[2];
-#pragma unroll
-                        for (int h = 0; h < 2; h++) {
-                            float y0 = (x[jj + 16 * h] * kHadNorm) * f16_bits_to_f32((uint16_t)(rw[h] & 0xFFFFu));
-                            float y1 = (x[jj + 16 * h + 8] * kHadNorm) * f16_bits_to_f32((uint16_t)(rw[h] >> 16));
-                            y0 *= f16_bits_to_f32((uint16_t)(sw[h] & 0xFFFFu));
-                            y1 *= f16_bits_to_f32((uint16_t)(sw[h] >> 16));
-                            o2[h] = (uint32_t)f32_to_bf16_bits(y0) | ((uint32_t)f32_to_bf16_bits(y1) << 16);
+                        for (int jj = 0; jj < 8; jj++) {
+                            const uint2 rv = *reinterpret_cast<const uint2 *>(s_scale + 4 * part + 16 * jj);
+                            float4 o;
+                            o.x = (x[jj] * kHadNorm) * f16_bits_to_f32((uint16_t)(rv.x & 0xFFFFu));
+                            o.y = (x[jj + 8] * kHadNorm) * f16_bits_to_f32((uint16_t)(rv.x >> 16));
+                            o.z = (x[jj + 16] * kHadNorm) * f16_bits_to_f32((uint16_t)(rv.y & 0xFFFFu));
+                            o.w = (x[jj + 24] * kHadNorm) * f16_bits_to_f32((uint16_t)(rv.y >> 16));
+                            *reinterpret_cast<float4 *>(dst + 16 * jj) = o;
                         }
-                        *reinterpret_cast<uint2 *>(dst + 16 * jj) = make_uint2(o2[0], o2[1]);
+                    } else {
+                        uint16_t *dst = a.out + (int64_t)nrow * a.ldo + d.out0 + colb;
+#pragma unroll
+                        for (int jj = 0; jj < 8; jj++) {
+                            const int cl = 4 * part + 16 * jj;     // column within the block
+                            const uint2 rv = *reinterpret_cast<const uint2 *>(s_scale + cl);
+                            const uint2 sv = *reinterpret_cast<const uint2 *>(s_scale + FT_BM + cl);
+                            const uint32_t rw[2] = {rv.x, rv.y}, sw[2] = {sv.x, sv.y};
+                            uint32_t o2[2];
+#pragma unroll
+                            for (int h = 0; h < 2; h++) {
+                                float y0 = (x[jj + 16 * h] * kHadNorm) * f16_bits_to_f32((uint16_t)(rw[h] & 0xFFFFu));
+                                float y1 = (x[jj + 16 * h + 8] * kHadNorm) * f16_bits_to_f32((uint16_t)(rw[h] >> 16));
+                                y0 *= f16_bits_to_f32((uint16_t)(sw[h] & 0xFFFFu));
+                                y1 *= f16_bits_to_f32((uint16_t)(sw[h] >> 16));
+                                o2[h] = (uint32_t)f32_to_bf16_bits(y0) | ((uint32_t)f32_to_bf16_bits(y1) << 16);
+                            }
+                            *reinterpret_cast<uint2 *>(dst + 16 * jj) = make_uint2(o2[0], o2[1]);
+                        }
                     }
                 }
                 named_bar(1, 128);   // T is rewritten by the next chunk
@@ -545,8 +630,9 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_ACCE + b));
             }
-        }
+        })
     }
+#undef FT_FOR_SEGMENTS
 
     tc_fence_before();
     __syncthreads();
@@ -564,8 +650,8 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
     }
 }
 
-template <int NT>
-cudaError_t launch_fused_t(const FusedArgs &a, cudaStream_t s) {
+template <int NT, bool ROWS>
+cudaError_t launch_fused_t(const FusedArgs &a, int64_t total_units, cudaStream_t s) {
     using C = FtCfg<NT>;
     static std::once_flag once[64];
     static cudaError_t attr_err[64];
@@ -574,15 +660,13 @@ cudaError_t launch_fused_t(const FusedArgs &a, cudaStream_t s) {
     if (dev < 0 || dev >= 64) dev = 0;
     std::call_once(once[dev], [&] {
         attr_err[dev] =
-            cudaFuncSetAttribute(fused_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+            cudaFuncSetAttribute(fused_tc_kernel<NT, ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     });
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
-    int64_t groups = 0;
-    for (int i = 0; i < a.n_shards; i++) groups += a.sh[i].OC / kHad;
-    const int64_t total = groups * (a.IC / FT_KC);
     int64_t grid = device_info().sm_count;       // one CTA per SM (shared memory)
     if (grid > kFusedMaxCtas) grid = kFusedMaxCtas;
-    if (grid > total) grid = total;
+    if (grid > total_units) grid = total_units;
+    if (grid < 1) grid = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(FT_THREADS);
@@ -593,7 +677,7 @@ cudaError_t launch_fused_t(const FusedArgs &a, cudaStream_t s) {
     attrs[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fused_tc_kernel<NT>, a);
+    return cudaLaunchKernelEx(&cfg, fused_tc_kernel<NT, ROWS>, a);
 }
 
 }  // namespace
@@ -612,14 +696,42 @@ cudaError_t launch_fused(FusedArgs &a, const uint16_t *u, cudaStream_t s) {
     if (!make_map_f16(&a.tm_u, u, (int64_t)a.n_shards * a.M, a.IC, nt)) return cudaErrorInvalidValue;
     for (int i = 0; i < a.n_shards; i++)
         if (!make_map_code(&a.tm_code[i], a.sh[i].code, a.IC, a.sh[i].OC, a.sh[i].K)) return cudaErrorInvalidValue;
+    a.entries = nullptr;
+    a.n_entries_dev = nullptr;
     a.hash_xor = kHashXor;
     for (int i = 0; i < 17; i++) a.pow2[i] = 1u << i;
+    int64_t groups = 0;
+    for (int i = 0; i < a.n_shards; i++) groups += a.sh[i].OC / kHad;
+    const int64_t total = groups * (a.IC / FT_KC);
     switch (nt) {
-        case 16: return launch_fused_t<16>(a, s);
-        case 32: return launch_fused_t<32>(a, s);
-        case 64: return launch_fused_t<64>(a, s);
-        default: return launch_fused_t<128>(a, s);
+        case 16: return launch_fused_t<16, false>(a, total, s);
+        case 32: return launch_fused_t<32, false>(a, total, s);
+        case 64: return launch_fused_t<64, false>(a, total, s);
+        default: return launch_fused_t<128, false>(a, total, s);
     }
+}
+
+bool fused_rows_fits(int64_t max_entries, int groups_per_entry, int IC) {
+    // every CTA's column groups must fall in at most kFtMaxEntries entries
+    int64_t grid = device_info().sm_count;
+    if (grid > kFusedMaxCtas) grid = kFusedMaxCtas;
+    const int64_t units = max_entries * groups_per_entry * (int64_t)(IC / FT_KC);
+    const int64_t per_cta = (units + grid - 1) / grid;
+    const int64_t per_entry = (int64_t)groups_per_entry * (IC / FT_KC);
+    return per_cta / per_entry + 2 <= kFtMaxEntries;
+}
+
+cudaError_t launch_fused_rows(FusedArgs &a, const uint16_t *u, int64_t u_rows, int64_t max_entries,
+                              cudaStream_t s) {
+    if (a.IC <= 0 || a.IC % 128 || a.groups_per_entry < 1 || !a.entries || !a.n_entries_dev || !a.out_rows)
+        return cudaErrorInvalidValue;
+    a.M = kFusedRowsNT;
+    a.n_shards = 0;
+    if (!make_map_f16(&a.tm_u, u, u_rows, a.IC, kFusedRowsNT)) return cudaErrorInvalidValue;
+    a.hash_xor = kHashXor;
+    for (int i = 0; i < 17; i++) a.pow2[i] = 1u << i;
+    const int64_t total = max_entries * a.groups_per_entry * (int64_t)(a.IC / FT_KC);
+    return launch_fused_t<kFusedRowsNT, true>(a, total, s);
 }
 
 }  // namespace exl3

@@ -98,6 +98,7 @@ size_t group_slab_floats(int max_groups, int nb);
 // pre-transformed activations u [shard][M][IC] (fp16).
 constexpr int kFusedMaxRows = 128;
 constexpr int kFusedMaxCtas = 256;
+constexpr int kFusedRowsNT = 64;      // rows mode (grouped MoE entries): rows per entry
 struct FusedShard {
     const int16_t *code;
     const uint16_t *rout, *s_out;
@@ -113,6 +114,14 @@ struct FusedArgs {
     int32_t n_shards, M, IC, pad_;
     uint16_t *out;       // bf16, row stride ldo
     int64_t ldo;
+    // rows mode (device-built entry lists, e.g. the grouped MoE): per entry a code
+    // tensor applied to rows [u_row0, u_row0 + nrows) of u, written as fp32 rows
+    // out_rows[(out_off + row) * OC_rows + col] = Had128(v) * post
+    const GroupEntry *entries;
+    const int32_t *n_entries_dev;
+    int32_t groups_per_entry;   // OC_rows / 128
+    int32_t OC_rows;
+    float *out_rows;
     float *partials;     // split-K slab, fused_slab_floats() floats
     int32_t *counters;
     int32_t *err;
@@ -122,6 +131,15 @@ struct FusedArgs {
 bool fused_supported();
 size_t fused_slab_floats(int max_groups, int64_t rows);
 cudaError_t launch_fused(FusedArgs &a, const uint16_t *u, cudaStream_t s);
+// Rows mode over a device-built entry list of at most max_entries entries, each
+// with at most kFusedRowsNT rows; u has u_rows rows.  fused_rows_fits() tells
+// whether a launch of that size fits the kernel's per-CTA entry cache.
+bool fused_rows_fits(int64_t max_entries, int groups_per_entry, int IC);
+cudaError_t launch_fused_rows(FusedArgs &a, const uint16_t *u, int64_t u_rows, int64_t max_entries,
+                              cudaStream_t s);
+
+// EXL3_FORCE_MODE: 0 none, 1 decode, 2 fused, 3 prefill (read on every call).
+int forced_mode();
 
 bool prefill_supported();
 cudaError_t launch_prefill(const uint16_t *u, const uint16_t *wt, int64_t M, int IC, int OC,

@@ -42,13 +42,27 @@ int moe_nb(int T) { return T <= 8 ? 1 : (T <= 16 ? 2 : 4); }
 struct MoeLayout {
     size_t pos, row_pair, row_slot, counts, ent1, ent2, u13, st1, h2, st2, slab, total;
     int R, chunk, max_entries, nb;
+    bool fused;   // FC1 and FC2 on the fused tensor-core GEMM (rows mode) instead of the decode-mode GEMM
 };
+
+// The fused tensor-core GEMM pays off once experts average 16 or more rows
+// (measured on E = 128, H = 2048, I = 768: T = 512 averages 32).
+bool moe_fused(int T, int H, int I, int E, int topk) {
+    const int force = forced_mode();
+    if (force == 1 || !fused_supported()) return false;
+    const int64_t R = (int64_t)T * topk;
+    if (force != 2 && R < 16 * (int64_t)E) return false;
+    const int active = E < R ? E : (int)R;
+    const int64_t max_entries = (R + kFusedRowsNT - 1) / kFusedRowsNT + active;
+    return fused_rows_fits(2 * max_entries, I / kHad, H) && fused_rows_fits(max_entries, H / kHad, I);
+}
 
 MoeLayout moe_layout(int T, int H, int I, int E, int topk) {
     MoeLayout L = {};
     L.R = T * topk;
     L.nb = moe_nb(T);
-    L.chunk = 8 * L.nb;
+    L.fused = moe_fused(T, H, I, E, topk);
+    L.chunk = L.fused ? kFusedRowsNT : 8 * L.nb;
     const int active = E < L.R ? E : L.R;
     L.max_entries = (L.R + L.chunk - 1) / L.chunk + active;
     size_t off = fixed_workspace_bytes();
@@ -64,7 +78,8 @@ MoeLayout moe_layout(int T, int H, int I, int E, int topk) {
     L.h2 = take(sizeof(uint16_t) * (size_t)L.R * I);
     L.st2 = take(sizeof(float) * (size_t)L.R * H);
     const int groups1 = 2 * L.max_entries * (I / kHad), groups2 = L.max_entries * (H / kHad);
-    L.slab = take(sizeof(float) * group_slab_floats(groups1 > groups2 ? groups1 : groups2, L.nb));
+    const int gmax = groups1 > groups2 ? groups1 : groups2;
+    L.slab = take(sizeof(float) * (L.fused ? fused_slab_floats(gmax, kFusedRowsNT) : group_slab_floats(gmax, L.nb)));
     L.total = off;
     return L;
 }
@@ -402,33 +417,60 @@ exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
                                                                          row_slot, counts, u13);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "moe_grouped: rotate");
 
-    GroupGemmArgs g1 = {};
-    g1.u = u13;
-    g1.IC = H;
-    g1.mode = kModeRows;
-    g1.entries = ent1;
-    g1.n_entries_dev = counts + 1;
-    g1.n_groups_per_entry = I / kHad;
-    g1.out_rows = st1;
-    g1.partials = slab;
-    g1.counters = counters;
-    if ((e = launch_group_gemm(g1, L.nb, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC1");
+    if (L.fused) {
+        FusedArgs f1 = {};
+        f1.IC = H;
+        f1.entries = ent1;
+        f1.n_entries_dev = counts + 1;
+        f1.groups_per_entry = I / kHad;
+        f1.OC_rows = I;
+        f1.out_rows = st1;
+        f1.partials = slab;
+        f1.counters = counters;
+        f1.err = err;
+        if ((e = launch_fused_rows(f1, u13, 2 * (int64_t)R, 2 * (int64_t)L.max_entries, s)) != cudaSuccess)
+            return cuda_fail(e, "moe_grouped: FC1");
+        act_kernel<<<warp_grid((int64_t)R * (I / kHad)), 256, 0, s>>>(st1, I, R, b.w2_suh, row_slot, counts, h2);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "moe_grouped: act");
+        FusedArgs f2 = f1;
+        f2.IC = I;
+        f2.entries = ent2;
+        f2.n_entries_dev = counts + 2;
+        f2.groups_per_entry = H / kHad;
+        f2.OC_rows = H;
+        f2.out_rows = st2;
+        if ((e = launch_fused_rows(f2, h2, (int64_t)R, (int64_t)L.max_entries, s)) != cudaSuccess)
+            return cuda_fail(e, "moe_grouped: FC2");
+    } else {
+        GroupGemmArgs g1 = {};
+        g1.u = u13;
+        g1.IC = H;
+        g1.mode = kModeRows;
+        g1.entries = ent1;
+        g1.n_entries_dev = counts + 1;
+        g1.n_groups_per_entry = I / kHad;
+        g1.out_rows = st1;
+        g1.partials = slab;
+        g1.counters = counters;
+        if ((e = launch_group_gemm(g1, L.nb, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC1");
 
-    act_kernel<<<warp_grid((int64_t)R * (I / kHad)), 256, 0, s>>>(st1, I, R, b.w2_suh, row_slot, counts, h2);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "moe_grouped: act");
+        act_kernel<<<warp_grid((int64_t)R * (I / kHad)), 256, 0, s>>>(st1, I, R, b.w2_suh, row_slot, counts, h2);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "moe_grouped: act");
 
-    GroupGemmArgs g2 = g1;
-    g2.u = h2;
-    g2.IC = I;
-    g2.entries = ent2;
-    g2.n_entries_dev = counts + 2;
-    g2.n_groups_per_entry = H / kHad;
-    g2.out_rows = st2;
-    if ((e = launch_group_gemm(g2, L.nb, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC2");
+        GroupGemmArgs g2 = g1;
+        g2.u = h2;
+        g2.IC = I;
+        g2.entries = ent2;
+        g2.n_entries_dev = counts + 2;
+        g2.n_groups_per_entry = H / kHad;
+        g2.out_rows = st2;
+        if ((e = launch_group_gemm(g2, L.nb, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC2");
+    }
 
     combine_kernel<<<warp_grid((int64_t)T * (H / kHad)), 256, 0, s>>>(st2, H, T, topk, w, pos, y);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "moe_grouped: combine");
-    trace("moe_grouped T=%d H=%d I=%d E=%d topk=%d rows<=%d nb=%d", T, H, I, E, topk, R, L.nb);
+    trace("moe_grouped T=%d H=%d I=%d E=%d topk=%d rows<=%d nb=%d gemm=%s", T, H, I, E, topk, R, L.nb,
+          L.fused ? "fused" : "decode");
     return EXL3_OK;
 }
 

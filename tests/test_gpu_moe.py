@@ -126,3 +126,39 @@ def test_moe_zero_tokens_is_a_no_op():
     m.exl3_moe_grouped(torch.empty((0, H), dtype=torch.bfloat16, device="cuda"),
                        torch.empty((0, 2), dtype=torch.int32, device="cuda"),
                        torch.empty((0, 2), dtype=torch.float32, device="cuda"), bank_dev(bank), ws, y=y)
+
+
+# ---------------------------------------------------------------- FC1 / FC2 on the fused tensor-core GEMM
+
+@pytest.mark.parametrize("T", (1, 5, 20, 40))
+def test_moe_small_bank_fused_gemm(T, monkeypatch):
+    # rows-mode fused GEMM over the device-built entry lists, mixed K, one to 40 tokens
+    monkeypatch.setenv("EXL3_FORCE_MODE", "fused")
+    E, H, I, topk = 6, 256, 128, 3
+    bank = syn.moe_bank(11, E=E, H=H, I=I, distinct_down_k=True)
+    x, logits = syn.moe_tokens(12 + T, T, H=H, E=E)
+    ids, w = oracle.topk_softmax(logits, topk)
+    y, ws = run_moe(x, ids, w, bank_dev(bank), E, H, I)
+    assert_rows_close(as_f64(y), oracle.moe_f64(x, ids, w, bank))
+    assert m.exl3_workspace_error(ws) == 0
+
+
+def test_moe_full_geometry_fused_gemm_16_tokens(full_bank, monkeypatch):
+    monkeypatch.setenv("EXL3_FORCE_MODE", "fused")
+    bank, bank_d = full_bank
+    x, logits = syn.moe_tokens(36, 16)
+    ids, w = oracle.topk_softmax(logits, 8)
+    y, ws = run_moe(x, ids, w, bank_d, 128, 2048, 768)
+    assert_rows_close(as_f64(y), oracle.moe_f64(x, ids, w, bank))
+    assert m.exl3_workspace_error(ws) == 0
+
+
+def test_moe_fused_gemm_deterministic(full_bank, monkeypatch):
+    monkeypatch.setenv("EXL3_FORCE_MODE", "fused")
+    bank, bank_d = full_bank
+    x, logits = syn.moe_tokens(42, 300)
+    ids, w = oracle.topk_softmax(logits, 8)
+    y1, ws = run_moe(x, ids, w, bank_d, 128, 2048, 768)
+    y2, _ = run_moe(x, ids, w, bank_d, 128, 2048, 768, ws)
+    assert np.array_equal(bits(y1), bits(y2))
+    assert m.exl3_workspace_error(ws) == 0
