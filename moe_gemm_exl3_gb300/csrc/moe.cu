@@ -143,15 +143,27 @@ struct RouteArgs {
     int32_t *err;
 };
 
+constexpr int kRouteParE = 128;   // slots up to which the stable ranking runs on all warps at once
+
 // One CTA of 1024 threads.  Rows of one slot are ordered by pair index (stable),
 // so the row -> entry assignment, and with it every partial sum, is the same on
-// every run.
+// every run.  With E <= kRouteParE each warp ranks a contiguous chunk of pairs
+// starting from its own per-slot cursor (the counts of the chunks before it);
+// otherwise one warp walks all pairs.
 __global__ void __launch_bounds__(1024) route_kernel(const RouteArgs a) {
     __shared__ int cnt[kMoeMaxE], base[kMoeMaxE], ebase[kMoeMaxE], cursor[kMoeMaxE];
-    const int tid = threadIdx.x;
+    __shared__ int wcur[32][kRouteParE];     // per warp and slot: pairs in the chunk, then its cursor
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, W = blockDim.x >> 5;
+    const bool par = a.E <= kRouteParE;
+    const int C = ((a.R + W - 1) / W + 31) & ~31;              // pairs per warp chunk
+    const int c_lo = w * C, c_hi = (w + 1) * C < a.R ? (w + 1) * C : a.R;
     for (int p = tid; p < a.E; p += blockDim.x) { cnt[p] = 0; cursor[p] = 0; }
+    if (par)
+        for (int i = tid; i < W * kRouteParE; i += blockDim.x) (&wcur[0][0])[i] = 0;
     __syncthreads();
-    for (int i = tid; i < a.R; i += blockDim.x) {
+    // pass 1: slot of every pair, counted per slot (and per warp chunk)
+    const int i_first = par ? c_lo + lane : tid, i_step = par ? 32 : (int)blockDim.x, i_end = par ? c_hi : a.R;
+    for (int i = i_first; i < i_end; i += i_step) {
         const int e = a.ids[i];
         int p = -1;
         if (e >= 0 && e < a.E) p = a.bank.perm[e];
@@ -161,8 +173,12 @@ __global__ void __launch_bounds__(1024) route_kernel(const RouteArgs a) {
         } else {
             p = -1;
         }
-        if (p < 0) record_error(a.err, kErrBadExpertId);
-        else atomicAdd(&cnt[p], 1);
+        if (p < 0) {
+            record_error(a.err, kErrBadExpertId);
+        } else {
+            atomicAdd(&cnt[p], 1);
+            if (par) atomicAdd(&wcur[w][p], 1);
+        }
         a.row_slot[i] = p;   // scratch: slot per pair (overwritten below with slot per row)
     }
     __syncthreads();
@@ -179,9 +195,32 @@ __global__ void __launch_bounds__(1024) route_kernel(const RouteArgs a) {
         a.counts[2] = chunks;
     }
     __syncthreads();
-    // stable positions: warp 0 walks the pairs 32 at a time
-    if (tid < 32) {
-        const unsigned lt = (1u << tid) - 1u;
+    const unsigned lt = (1u << lane) - 1u;
+    if (par) {
+        // each warp's starting cursor per slot: the slot's base plus the earlier chunks' counts
+        for (int p = tid; p < a.E; p += blockDim.x) {
+            int run = base[p];
+            for (int ww = 0; ww < W; ww++) {
+                const int t = wcur[ww][p];
+                wcur[ww][p] = run;
+                run += t;
+            }
+        }
+        __syncthreads();
+        for (int i0 = c_lo; i0 < c_hi; i0 += 32) {
+            const int i = i0 + lane;
+            const int p = i < c_hi ? a.row_slot[i] : -2;
+            const unsigned peers = __match_any_sync(kFull, p);
+            const int rank = __popc(peers & lt);
+            int position = -1;
+            if (p >= 0) position = wcur[w][p] + rank;
+            __syncwarp();
+            if (p >= 0 && (peers & lt) == 0) wcur[w][p] += __popc(peers);
+            __syncwarp();
+            if (i < c_hi) a.pos[i] = position;
+        }
+    } else if (tid < 32) {
+        // stable positions: warp 0 walks the pairs 32 at a time
         for (int i0 = 0; i0 < a.R; i0 += 32) {
             const int i = i0 + tid;
             const int p = i < a.R ? a.row_slot[i] : -2;
@@ -247,33 +286,55 @@ __global__ void __launch_bounds__(256) rotate_kernel(const uint16_t *__restrict_
                                                      const int32_t *__restrict__ row_pair,
                                                      const int32_t *__restrict__ row_slot,
                                                      const int32_t *__restrict__ counts,
-                                                     uint16_t *__restrict__ u) {
+                                                     uint16_t *__restrict__ u, int parts) {
     asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
-    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int blocks = H / kHad;
-    const int rows = counts[0];
-    if (wid >= (int64_t)2 * R * blocks) return;
-    const int j = (int)(wid / ((int64_t)R * blocks));
-    const int64_t rem = wid % ((int64_t)R * blocks);
-    const int r = (int)(rem / blocks);
-    if (r >= rows) return;
-    const int c0 = (int)(rem % blocks) * kHad + 4 * lane;
+    // `parts` warps per row (many when there are few rows), each a contiguous run of 128-blocks
+    const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int r = wid / parts, part = wid - r * parts;
+    if (r >= R || r >= counts[0]) return;
+    const int span = H / parts;                                  // channels per warp, a multiple of 128
+    const int c_begin = part * span, c_end = c_begin + span;
     const int t = row_pair[r] / topk;
     const int p = row_slot[r];
-    const uint2 xv = *reinterpret_cast<const uint2 *>(x + (int64_t)t * H + c0);
-    const uint2 sv = __ldg(reinterpret_cast<const uint2 *>(suh + ((int64_t)p * 2 + j) * H + c0));
-    const uint32_t xs[2] = {xv.x, xv.y}, ss[2] = {sv.x, sv.y};
-    float v[4];
+    const uint16_t *xr = x + (int64_t)t * H;
+    const uint16_t *sj[2] = {suh + (int64_t)p * 2 * H, suh + ((int64_t)p * 2 + 1) * H};
+    uint16_t *uj[2] = {u + (int64_t)r * H, u + ((int64_t)R + r) * H};
+    // two 128-blocks per iteration, every load issued before the transforms; the
+    // token's x block serves both projections
+    for (int c0 = c_begin + 4 * lane; c0 < c_end; c0 += 2 * kHad) {
+        const bool two = c0 + kHad < c_end;
+        uint2 xv[2], sv[2][2];
 #pragma unroll
-    for (int i = 0; i < 4; i++)
-        v[i] = bf16_bits_to_f32((xs[i >> 1] >> (16 * (i & 1))) & 0xFFFFu) *
-               f16_bits_to_f32((uint16_t)(ss[i >> 1] >> (16 * (i & 1))));
-    warp_fwht128(v, lane);
-    uint2 o;
-    o.x = (uint32_t)f32_to_f16_bits(v[0] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[1] * kHadNorm) << 16);
-    o.y = (uint32_t)f32_to_f16_bits(v[2] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[3] * kHadNorm) << 16);
-    *reinterpret_cast<uint2 *>(u + ((int64_t)j * R + r) * H + c0) = o;
+        for (int h = 0; h < 2; h++) {
+            const int c = c0 + h * kHad;
+            if (h == 0 || two) {
+                xv[h] = *reinterpret_cast<const uint2 *>(xr + c);
+                sv[h][0] = __ldg(reinterpret_cast<const uint2 *>(sj[0] + c));
+                sv[h][1] = __ldg(reinterpret_cast<const uint2 *>(sj[1] + c));
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            if (h == 1 && !two) break;
+            const int c = c0 + h * kHad;
+            const uint32_t xs[2] = {xv[h].x, xv[h].y};
+#pragma unroll
+            for (int j = 0; j < 2; j++) {
+                const uint32_t ss[2] = {sv[h][j].x, sv[h][j].y};
+                float v[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    v[i] = bf16_bits_to_f32((xs[i >> 1] >> (16 * (i & 1))) & 0xFFFFu) *
+                           f16_bits_to_f32((uint16_t)(ss[i >> 1] >> (16 * (i & 1))));
+                warp_fwht128(v, lane);
+                uint2 o;
+                o.x = (uint32_t)f32_to_f16_bits(v[0] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[1] * kHadNorm) << 16);
+                o.y = (uint32_t)f32_to_f16_bits(v[2] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[3] * kHadNorm) << 16);
+                *reinterpret_cast<uint2 *>(uj[j] + c) = o;
+            }
+        }
+    }
 }
 
 // ------------------------------------------------------------------ act
@@ -287,12 +348,12 @@ __global__ void __launch_bounds__(256) act_kernel(const float *__restrict__ st1,
                                                   uint16_t *__restrict__ h2) {
     asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
-    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);   // R * I / 128 < 2^31
     const int blocks = I / kHad;
     const int rows = counts[0];
-    const int r = (int)(wid / blocks);
+    const int r = wid / blocks;
     if (r >= rows || r >= R) return;
-    const int c0 = (int)(wid % blocks) * kHad + 4 * lane;
+    const int c0 = (wid - r * blocks) * kHad + 4 * lane;
     const int p = row_slot[r];
     const float4 g = *reinterpret_cast<const float4 *>(st1 + (int64_t)r * I + c0);
     const float4 uu = *reinterpret_cast<const float4 *>(st1 + ((int64_t)R + r) * I + c0);
@@ -320,11 +381,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
                                                       const int32_t *__restrict__ pos,
                                                       uint16_t *__restrict__ y) {
     const int lane = threadIdx.x & 31;
-    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);   // T * H / 128 < 2^31
     const int blocks = H / kHad;
-    const int t = (int)(wid / blocks);
+    const int t = wid / blocks;
     if (t >= T) return;
-    const int c0 = (int)(wid % blocks) * kHad + 4 * lane;
+    const int c0 = (wid - t * blocks) * kHad + 4 * lane;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int k = 0; k < topk; k++) {
         const int r = pos[(int64_t)t * topk + k];
@@ -413,8 +474,11 @@ exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "moe_grouped: route");
 
-    rotate_kernel<<<warp_grid((int64_t)2 * R * (H / kHad)), 256, 0, s>>>(x, H, R, topk, b.w13_suh, row_pair,
-                                                                         row_slot, counts, u13);
+    // warps per row: enough warps to fill the GPU when few rows are routed, whole rows otherwise
+    int parts = 1;
+    while (parts * 2 <= H / kHad && (H / kHad) % (parts * 2) == 0 && (int64_t)R * parts < 4096) parts *= 2;
+    rotate_kernel<<<warp_grid((int64_t)R * parts), 256, 0, s>>>(x, H, R, topk, b.w13_suh, row_pair, row_slot, counts,
+                                                               u13, parts);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "moe_grouped: rotate");
 
     if (L.fused) {
