@@ -85,6 +85,7 @@ struct GroupGemmArgs {
     uint32_t hash_xor;            // the codebook's xor constant, kept in a register
     uint32_t pow2[17];            // pow2[o] = 1 << o (multipliers of the state extraction)
     int32_t max_rows;             // rows per entry the launch was sized for
+    int32_t parts;                // > 0: CTA c takes part c % parts of group c / parts (set by the launcher)
 };
 constexpr int kMaxInlineEntries = 4;
 

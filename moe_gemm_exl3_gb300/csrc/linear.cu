@@ -276,13 +276,26 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
         for (int i = 0; i < n_entries; i++) n_groups += a.inline_e[i].OC / kHad;
     }
     const int64_t total = (int64_t)n_groups * A;
-    // every CTA of the partition must own at least one unit (an empty range would
-    // never arrive at its group's counter): with fewer units than CTAs the extra
-    // CTAs leave
-    const int nCTA = (int64_t)gridDim.x < total ? (int)gridDim.x : (int)total, c = blockIdx.x;
-    if (c >= nCTA) return;
-    int64_t f = (int64_t)c * total / nCTA;
-    const int64_t f_end = (int64_t)(c + 1) * total / nCTA;
+    const int c = blockIdx.x;
+    int nCTA;
+    int64_t f, f_end;
+    if (a.parts > 0) {
+        // item partition: CTA c takes part c % parts of column group c / parts, so a
+        // CTA never switches groups and a group's partials come from exactly `parts` CTAs
+        nCTA = n_groups * a.parts;
+        if (c >= nCTA) return;
+        const int g = c / a.parts, pp = c - g * a.parts;
+        f = (int64_t)g * A + (int64_t)pp * A / a.parts;
+        f_end = (int64_t)g * A + (int64_t)(pp + 1) * A / a.parts;
+    } else {
+        // stream-K: every CTA of the partition must own at least one unit (an empty
+        // range would never arrive at its group's counter): with fewer units than
+        // CTAs the extra CTAs leave
+        nCTA = (int64_t)gridDim.x < total ? (int)gridDim.x : (int)total;
+        if (c >= nCTA) return;
+        f = (int64_t)c * total / nCTA;
+        f_end = (int64_t)(c + 1) * total / nCTA;
+    }
     const uint32_t hx = a.hash_xor;
 
     while (f < f_end) {
@@ -331,9 +344,15 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
         __syncthreads();
 
         // ---- split-K across CTAs
-        const int64_t x0 = (int64_t)gi * A, x1 = (int64_t)(gi + 1) * A - 1;
-        const int c_first = (int)(((x0 + 1) * nCTA - 1) / total);
-        const int c_last = (int)(((x1 + 1) * nCTA - 1) / total);
+        int c_first, c_last;     // the CTAs that own units of group gi
+        if (a.parts > 0) {
+            c_first = gi * a.parts;
+            c_last = c_first + a.parts - 1;
+        } else {
+            const int64_t x0 = (int64_t)gi * A, x1 = (int64_t)(gi + 1) * A - 1;
+            c_first = (int)(((x0 + 1) * nCTA - 1) / total);
+            c_last = (int)(((x1 + 1) * nCTA - 1) / total);
+        }
         bool do_epilogue = true;
         if (c_first != c_last) {
             float *slot = a.partials + (int64_t)(c + gi) * FRAG;
@@ -423,6 +442,19 @@ static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t tot
     for (int i = 0; i < 17; i++) a.pow2[i] = 1u << i;
     int64_t grid = (int64_t)device_info().sm_count * occ;
     if (grid > kDecodeMaxCtas) grid = kDecodeMaxCtas;
+    a.parts = 0;
+    const int64_t A = a.IC / kTile;
+    if (total_hint > 0 && !a.n_entries_dev && a.n_groups_per_entry == 0) {
+        // column groups known on the host: when they fit in one wave, give every CTA
+        // one part of one group (no group switches inside a CTA, equal work per CTA)
+        const int64_t groups = total_hint / A;
+        if (groups > 0 && groups <= grid) {
+            int64_t parts = grid / groups;
+            if (parts > A) parts = A;
+            a.parts = (int32_t)parts;
+            grid = groups * parts;
+        }
+    }
     if (total_hint > 0 && grid > total_hint) grid = total_hint;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
