@@ -182,17 +182,39 @@ __global__ void __launch_bounds__(1024) route_kernel(const RouteArgs a) {
         a.row_slot[i] = p;   // scratch: slot per pair (overwritten below with slot per row)
     }
     __syncthreads();
-    if (tid == 0) {   // E <= 1024 slots: a serial scan is a few microseconds at most
-        int rows = 0, chunks = 0;
-        for (int p = 0; p < a.E; p++) {
-            base[p] = rows;
-            ebase[p] = chunks;
-            rows += cnt[p];
-            chunks += (cnt[p] + a.chunk - 1) / a.chunk;
+    // exclusive scans of rows and row chunks over the slots (E <= 1024 = one value per
+    // thread): warp scans, then a scan of the warp totals
+    {
+        __shared__ int wsum_r[32], wsum_c[32];
+        const int vr = tid < a.E ? cnt[tid] : 0;
+        const int vc = tid < a.E ? (vr + a.chunk - 1) / a.chunk : 0;
+        int ir = vr, ic = vc;   // inclusive within the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int tr = __shfl_up_sync(kFull, ir, o), tc = __shfl_up_sync(kFull, ic, o);
+            if (lane >= o) { ir += tr; ic += tc; }
         }
-        a.counts[0] = rows;
-        a.counts[1] = 2 * chunks;
-        a.counts[2] = chunks;
+        if (lane == 31) { wsum_r[w] = ir; wsum_c[w] = ic; }
+        __syncthreads();
+        if (w == 0) {
+            int xr = lane < W ? wsum_r[lane] : 0, xc = lane < W ? wsum_c[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int tr = __shfl_up_sync(kFull, xr, o), tc = __shfl_up_sync(kFull, xc, o);
+                if (lane >= o) { xr += tr; xc += tc; }
+            }
+            if (lane < W) { wsum_r[lane] = xr; wsum_c[lane] = xc; }   // inclusive warp prefix
+            if (lane == 31) {
+                a.counts[0] = xr;
+                a.counts[1] = 2 * xc;
+                a.counts[2] = xc;
+            }
+        }
+        __syncthreads();
+        if (tid < a.E) {
+            base[tid] = ir - vr + (w > 0 ? wsum_r[w - 1] : 0);
+            ebase[tid] = ic - vc + (w > 0 ? wsum_c[w - 1] : 0);
+        }
     }
     __syncthreads();
     const unsigned lt = (1u << lane) - 1u;
