@@ -452,6 +452,9 @@ exl3_status exl3_embed_int8_gather(const int8_t *q, const uint16_t *scale, int64
                     (long long)V, H, (long long)N);
     if (N == 0) return EXL3_OK;
     if (!q || !scale || !ids || !out) return fail(EXL3_EINVAL, "embed_int8_gather: null pointer");
+    if (N * (int64_t)(H / 16) >= 0x7FFFFF00LL)
+        return fail(EXL3_EINVAL, "embed_int8_gather: N * H / 16 = %lld chunks; one call handles fewer than 2^31",
+                    (long long)(N * (int64_t)(H / 16)));
     if (!aligned16(q) || !aligned16(out))
         return fail(EXL3_EINVAL, "embed_int8_gather: q (%p) and out (%p) must be 16-byte aligned", q, out);
     cudaError_t e = launch_gather(q, scale, V, H, ids, N, out, n_bad, (cudaStream_t)stream);
