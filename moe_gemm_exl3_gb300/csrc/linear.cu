@@ -13,7 +13,8 @@ namespace exl3 {
 // One warp per (row, block); lane l holds channels 4l..4l+3 of the block.
 // --------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) pretransform_kernel(const uint16_t *__restrict__ x,
-                                                           int64_t M, int IC, PretransformShards p,
+                                                           int64_t M, int IC,
+                                                           const __grid_constant__ PretransformShards p,
                                                            uint16_t *__restrict__ u) {
     // let a dependent launch (the GEMM that reads u) get scheduled early; it
     // still waits for this grid to finish before touching u
