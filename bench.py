@@ -106,18 +106,27 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def kernel_time_ms(torch, stream, fn, n):
-    """Mean duration of fn(j) (the launches of one call) from CUDA events on `stream`;
-    the stream is kept busy first so that no launch gap is measured."""
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+def kernel_time_ms(torch, stream, fn, n, reps=4):
+    """Mean duration of fn(j) (the launches of one call), j = 0..n-1, in the launch
+    configuration of the timed steps: the n calls are captured in one CUDA graph,
+    which is replayed `reps` times between two CUDA events on `stream`."""
     with torch.cuda.stream(stream):
-        torch.cuda._sleep(50_000_000)
         for j in range(n):
-            evs[j][0].record(stream)
             fn(j)
-            evs[j][1].record(stream)
     torch.cuda.synchronize()
-    return statistics.mean(a.elapsed_time(b) for a, b in evs[n // 4:])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for j in range(n):
+            fn(j)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * n)
 
 
 def profile_traffic(name, src_files):

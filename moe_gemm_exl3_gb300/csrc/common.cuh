@@ -109,9 +109,10 @@ struct QuarterStream {
     }
 
     // 16-bit trellis state of quarter weight i (compile-time i after unrolling).
-    // The general case shifts the window to the top of the word with a multiply
-    // by 2^o and then down by 16: the multiply runs on the FMA pipe, which
-    // balances the integer ALU pipe that the hash's LOP3 and the shift occupy.
+    // Windows on a byte boundary take one byte permute.  The general case shifts
+    // the window to the top of the word with a multiply by 2^o and then down by
+    // 16: the multiply runs on the FMA pipe, which balances the integer ALU pipe
+    // that the hash's LOP3 and the shift occupy.
     // pow2[o] must hold 1 << o; it is read from a kernel argument so that the
     // compiler cannot turn the multiply back into an ALU shift.
     __device__ __forceinline__ uint32_t state(int i, const uint32_t *pow2) const {
@@ -121,6 +122,7 @@ struct QuarterStream {
         const int oo = o <= 16 ? o : o - 16;
         if (oo == 0) return R >> 16;
         if (oo == 16) return R & 0xFFFFu;
+        if (oo == 8) return __byte_perm(R, 0, 0x4421);   // bytes 1..2: one permute
         return (R * pow2[oo]) >> 16;
     }
 };

@@ -186,7 +186,6 @@ template <int K, int NB>
 __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const GroupEntry &e, const uint16_t *u,
                                                  int IC, int G, int a_lo, int a_hi, int lane, int warp,
                                                  uint32_t hx, const uint32_t *pow2) {
-    constexpr int PF = 2;   // tile rows of code words in flight per warp
     const int g = lane >> 2, q = lane & 3;
     const int TO = e.OC / kTile;
     const uint32_t *tile0 = reinterpret_cast<const uint32_t *>(e.code) + (int64_t)(8 * G + g) * 8 * K + q * 2 * K;
@@ -201,36 +200,18 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
                 v[nb] = __ldg(reinterpret_cast<const uint2 *>(ub + (int64_t)(8 * nb + g) * IC + 16 * ar + 4 * q));
         }
     };
-    int ar = a_lo + warp;
-    uint32_t wq[PF][2 * K];
-#pragma unroll
-    for (int d = 0; d < PF; d++)
-        if (ar + d * kDecodeWarps < a_hi) load_quarter<K>(wq[d], tile0 + (ar + d * kDecodeWarps) * row_words);
-    uint2 un[NB];
-    load_u(un, ar);
-    for (; ar < a_hi; ar += kDecodeWarps) {
-        uint32_t w[2 * K];
-#pragma unroll
-        for (int i = 0; i < 2 * K; i++) w[i] = wq[0][i];
-#pragma unroll
-        for (int d = 0; d + 1 < PF; d++)
-#pragma unroll
-            for (int i = 0; i < 2 * K; i++) wq[d][i] = wq[d + 1][i];
-        if (ar + PF * kDecodeWarps < a_hi) load_quarter<K>(wq[PF - 1], tile0 + (ar + PF * kDecodeWarps) * row_words);
-
-        // this row's activations, each duplicated into a half2; prefetch the next row's
-        uint32_t b[NB][4];
+    // this row's activations, each duplicated into a half2
+    auto dup_u = [&](uint32_t (&b)[NB][4], const uint2 (&v)[NB]) {
 #pragma unroll
         for (int nb = 0; nb < NB; nb++) {
-            b[nb][0] = dup_half_lo(un[nb].x);
-            b[nb][1] = dup_half_hi(un[nb].x);
-            b[nb][2] = dup_half_lo(un[nb].y);
-            b[nb][3] = dup_half_hi(un[nb].y);
+            b[nb][0] = dup_half_lo(v[nb].x);
+            b[nb][1] = dup_half_hi(v[nb].x);
+            b[nb][2] = dup_half_lo(v[nb].y);
+            b[nb][3] = dup_half_hi(v[nb].y);
         }
-        load_u(un, ar + kDecodeWarps);
-
-        QuarterStream<K> st;
-        st.build(w, quarter_prev_word(w[2 * K - 1], lane));
+    };
+    // the 64 weights of this lane's quarter: hash, then MMAs against the activations
+    auto mma_row = [&](const QuarterStream<K> &st, const uint32_t (&b)[NB][4]) {
 #pragma unroll
         for (int rp = 0; rp < 2; rp++) {
 #pragma unroll
@@ -244,6 +225,54 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
                 for (int nb = 0; nb < NB; nb++)
                     mma_16816(acc[j][nb], z0, z1, z2, z3, b[nb][2 * rp], b[nb][2 * rp + 1]);
             }
+        }
+    };
+    int ar = a_lo + warp;
+    uint2 un[NB];
+    if constexpr (NB == 1) {
+        // two tile-row buffers used in turn: a buffer is refilled with the row two
+        // steps ahead as soon as its words are realigned, so no register copies
+        uint32_t wa[2 * K], wb[2 * K];
+        if (ar < a_hi) load_quarter<K>(wa, tile0 + ar * row_words);
+        if (ar + kDecodeWarps < a_hi) load_quarter<K>(wb, tile0 + (ar + kDecodeWarps) * row_words);
+        load_u(un, ar);
+        auto row = [&](uint32_t (&w)[2 * K], int arc) {
+            QuarterStream<K> st;
+            st.build(w, quarter_prev_word(w[2 * K - 1], lane));
+            if (arc + 2 * kDecodeWarps < a_hi) load_quarter<K>(w, tile0 + (arc + 2 * kDecodeWarps) * row_words);
+            uint32_t b[NB][4];
+            dup_u(b, un);
+            load_u(un, arc + kDecodeWarps);
+            mma_row(st, b);
+        };
+        for (; ar < a_hi; ar += 2 * kDecodeWarps) {
+            row(wa, ar);
+            if (ar + kDecodeWarps >= a_hi) break;
+            row(wb, ar + kDecodeWarps);
+        }
+    } else {
+        // one rotating prefetch queue (fewer live registers with more rows)
+        constexpr int PF = 2;   // tile rows of code words in flight per warp
+        uint32_t wq[PF][2 * K];
+#pragma unroll
+        for (int d = 0; d < PF; d++)
+            if (ar + d * kDecodeWarps < a_hi) load_quarter<K>(wq[d], tile0 + (ar + d * kDecodeWarps) * row_words);
+        load_u(un, ar);
+        for (; ar < a_hi; ar += kDecodeWarps) {
+            uint32_t w[2 * K];
+#pragma unroll
+            for (int i = 0; i < 2 * K; i++) w[i] = wq[0][i];
+#pragma unroll
+            for (int d = 0; d + 1 < PF; d++)
+#pragma unroll
+                for (int i = 0; i < 2 * K; i++) wq[d][i] = wq[d + 1][i];
+            if (ar + PF * kDecodeWarps < a_hi) load_quarter<K>(wq[PF - 1], tile0 + (ar + PF * kDecodeWarps) * row_words);
+            uint32_t b[NB][4];
+            dup_u(b, un);
+            load_u(un, ar + kDecodeWarps);
+            QuarterStream<K> st;
+            st.build(w, quarter_prev_word(w[2 * K - 1], lane));
+            mma_row(st, b);
         }
     }
 }
