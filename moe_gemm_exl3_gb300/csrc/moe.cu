@@ -37,7 +37,11 @@ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Rows per grouped-GEMM entry: an expert gets at most T rows (a token routes to
 // an expert at most once), so small batches need only small row blocks.
-int moe_nb(int T) { return T <= 8 ? 1 : (T <= 16 ? 2 : 4); }
+// Row blocks (of 8) per decode-mode entry, from the mean rows per expert: one
+// block costs ~22 % less per code byte than two, and an expert with more rows
+// than a block just gets more entries, so wider blocks only pay once most
+// experts fill them.
+int moe_nb(int R, int E) { return R <= 4 * E ? 1 : (R <= 8 * E ? 2 : 4); }
 
 struct MoeLayout {
     size_t pos, row_pair, row_slot, counts, ent1, ent2, u13, st1, h2, st2, slab, total;
@@ -60,7 +64,7 @@ bool moe_fused(int T, int H, int I, int E, int topk) {
 MoeLayout moe_layout(int T, int H, int I, int E, int topk) {
     MoeLayout L = {};
     L.R = T * topk;
-    L.nb = moe_nb(T);
+    L.nb = moe_nb(L.R, E);
     L.fused = moe_fused(T, H, I, E, topk);
     L.chunk = L.fused ? kFusedRowsNT : 8 * L.nb;
     const int active = E < L.R ? E : L.R;

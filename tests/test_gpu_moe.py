@@ -63,6 +63,20 @@ def test_moe_small_bank_mixed_k(T):
     assert m.exl3_workspace_error(ws) == 0
 
 
+@pytest.mark.parametrize("T", (16, 40))
+def test_moe_skewed_routing_splits_entries(T):
+    # every token picks the same experts: each gets T rows, more than one row block
+    E, H, I, topk = 16, 256, 128, 4
+    bank = syn.moe_bank(21, E=E, H=H, I=I, distinct_down_k=True)
+    x, logits = syn.moe_tokens(30 + T, T, H=H, E=E)
+    logits[:, [2, 7, 11, 13]] += 50.0
+    ids, w = oracle.topk_softmax(logits, topk)
+    assert len(np.unique(ids)) == topk
+    y, ws = run_moe(x, ids, w, bank_dev(bank), E, H, I)
+    assert_rows_close(as_f64(y), oracle.moe_f64(x, ids, w, bank))
+    assert m.exl3_workspace_error(ws) == 0
+
+
 @pytest.fixture(scope="module")
 def full_bank():
     bank = syn.moe_bank(3)           # E = 128, H = 2048, I = 768, K per expert in {2, 3, 4}
