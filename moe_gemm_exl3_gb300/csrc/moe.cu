@@ -148,38 +148,74 @@ struct RouteArgs {
 };
 
 constexpr int kRouteParE = 128;   // slots up to which the stable ranking runs on all warps at once
+constexpr int kRouteRegPairs = 8; // pairs per lane that the ranking keeps in registers (fast path)
 
 // One CTA of 1024 threads.  Rows of one slot are ordered by pair index (stable),
 // so the row -> entry assignment, and with it every partial sum, is the same on
 // every run.  With E <= kRouteParE each warp ranks a contiguous chunk of pairs
 // starting from its own per-slot cursor (the counts of the chunks before it);
-// otherwise one warp walks all pairs.
+// otherwise one warp walks all pairs.  When a warp's chunk is at most
+// 32 * kRouteRegPairs pairs (fast path), its lanes keep the pairs' slots in
+// registers from the count to the ranking, read the expert tables from shared
+// memory, and write each row's pair and slot as soon as the row is known.
 __global__ void __launch_bounds__(1024) route_kernel(const RouteArgs a) {
     __shared__ int cnt[kMoeMaxE], base[kMoeMaxE], ebase[kMoeMaxE], cursor[kMoeMaxE];
     __shared__ int wcur[32][kRouteParE];     // per warp and slot: pairs in the chunk, then its cursor
+    __shared__ int s_perm[kRouteParE], s_kgu[kRouteParE], s_kd[kRouteParE];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, W = blockDim.x >> 5;
     const bool par = a.E <= kRouteParE;
     const int C = ((a.R + W - 1) / W + 31) & ~31;              // pairs per warp chunk
     const int c_lo = w * C, c_hi = (w + 1) * C < a.R ? (w + 1) * C : a.R;
+    const bool fast = par && C <= 32 * kRouteRegPairs;
     for (int p = tid; p < a.E; p += blockDim.x) { cnt[p] = 0; cursor[p] = 0; }
-    if (par)
+    if (par) {
         for (int i = tid; i < W * kRouteParE; i += blockDim.x) (&wcur[0][0])[i] = 0;
+        for (int e = tid; e < a.E; e += blockDim.x) {
+            s_perm[e] = a.bank.perm[e];
+            s_kgu[e] = a.bank.k_gu[e];
+            s_kd[e] = a.bank.k_d[e];
+        }
+    }
     __syncthreads();
-    // pass 1: slot of every pair, counted per slot (and per warp chunk)
-    const int i_first = par ? c_lo + lane : tid, i_step = par ? 32 : (int)blockDim.x, i_end = par ? c_hi : a.R;
-    for (int i = i_first; i < i_end; i += i_step) {
-        const int e = a.ids[i];
+    // slot of expert id e, or -1 (invalid id, slot or bitrate: recorded, routed nowhere)
+    auto slot_of = [&](int e) {
         int p = -1;
-        if (e >= 0 && e < a.E) p = a.bank.perm[e];
+        if (e >= 0 && e < a.E) p = par ? s_perm[e] : a.bank.perm[e];
         if (p >= 0 && p < a.E) {
-            const int kg = a.bank.k_gu[p], kd = a.bank.k_d[p];
+            const int kg = par ? s_kgu[p] : a.bank.k_gu[p], kd = par ? s_kd[p] : a.bank.k_d[p];
             if (kg < 2 || kg > 4 || kd < 2 || kd > 4) p = -1;
         } else {
             p = -1;
         }
-        if (p < 0) {
-            record_error(a.err, kErrBadExpertId);
-        } else {
+        if (p < 0) record_error(a.err, kErrBadExpertId);
+        return p;
+    };
+    int pr[kRouteRegPairs];   // fast path: slot of pair c_lo + 32 k + lane (-2: no pair)
+    if (fast) {
+#pragma unroll
+        for (int k = 0; k < kRouteRegPairs; k++) {
+            const int i = c_lo + 32 * k + lane;
+            pr[k] = i < c_hi ? a.ids[i] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < kRouteRegPairs; k++) {
+            const int i = c_lo + 32 * k + lane;
+            if (i < c_hi) {
+                pr[k] = slot_of(pr[k]);
+                if (pr[k] >= 0) {
+                    atomicAdd(&cnt[pr[k]], 1);
+                    atomicAdd(&wcur[w][pr[k]], 1);
+                }
+            } else {
+                pr[k] = -2;
+            }
+        }
+    }
+    // pass 1: slot of every pair, counted per slot (and per warp chunk)
+    const int i_first = par ? c_lo + lane : tid, i_step = par ? 32 : (int)blockDim.x, i_end = par ? c_hi : a.R;
+    for (int i = i_first; i < i_end && !fast; i += i_step) {
+        const int p = slot_of(a.ids[i]);
+        if (p >= 0) {
             atomicAdd(&cnt[p], 1);
             if (par) atomicAdd(&wcur[w][p], 1);
         }
@@ -233,7 +269,27 @@ __global__ void __launch_bounds__(1024) route_kernel(const RouteArgs a) {
             }
         }
         __syncthreads();
-        for (int i0 = c_lo; i0 < c_hi; i0 += 32) {
+        if (fast) {
+#pragma unroll
+            for (int k = 0; k < kRouteRegPairs; k++) {
+                const int i = c_lo + 32 * k + lane;
+                if (c_lo + 32 * k >= c_hi) break;
+                const int p = pr[k];
+                const unsigned peers = __match_any_sync(kFull, p);
+                const int rank = __popc(peers & lt);
+                int position = -1;
+                if (p >= 0) position = wcur[w][p] + rank;
+                __syncwarp();
+                if (p >= 0 && (peers & lt) == 0) wcur[w][p] += __popc(peers);
+                __syncwarp();
+                if (i < c_hi) a.pos[i] = position;
+                if (position >= 0) {
+                    a.row_pair[position] = i;
+                    a.row_slot[position] = p;
+                }
+            }
+        }
+        for (int i0 = c_lo; i0 < c_hi && !fast; i0 += 32) {
             const int i = i0 + lane;
             const int p = i < c_hi ? a.row_slot[i] : -2;
             const unsigned peers = __match_any_sync(kFull, p);
@@ -260,17 +316,19 @@ __global__ void __launch_bounds__(1024) route_kernel(const RouteArgs a) {
             if (i < a.R) a.pos[i] = position;
         }
     }
-    __syncthreads();
-    for (int i = tid; i < a.R; i += blockDim.x) {
-        const int r = a.pos[i];
-        if (r >= 0) a.row_pair[r] = i;
-    }
-    __syncthreads();
-    // slot per row (after every pair read its slot above)
-    for (int i = tid; i < a.R; i += blockDim.x) {
-        const int r = a.pos[i];
-        const int e = a.ids[i];
-        if (r >= 0) a.row_slot[r] = a.bank.perm[e];
+    if (!fast) {
+        __syncthreads();
+        for (int i = tid; i < a.R; i += blockDim.x) {
+            const int r = a.pos[i];
+            if (r >= 0) a.row_pair[r] = i;
+        }
+        __syncthreads();
+        // slot per row (after every pair read its slot above)
+        for (int i = tid; i < a.R; i += blockDim.x) {
+            const int r = a.pos[i];
+            const int e = a.ids[i];
+            if (r >= 0) a.row_slot[r] = a.bank.perm[e];
+        }
     }
     // grouped-GEMM entries: one per (slot, block of `chunk` rows); FC1 has a w1 and a w3 entry
     for (int p = tid; p < a.E; p += blockDim.x) {
@@ -502,7 +560,7 @@ exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
 
     // warps per row: enough warps to fill the GPU when few rows are routed, whole rows otherwise
     int parts = 1;
-    while (parts * 2 <= H / kHad && (H / kHad) % (parts * 2) == 0 && (int64_t)R * parts < 4096) parts *= 2;
+    while (parts * 2 <= H / kHad && (H / kHad) % (parts * 2) == 0 && (int64_t)R * parts < 32768) parts *= 2;
     rotate_kernel<<<warp_grid((int64_t)R * parts), 256, 0, s>>>(x, H, R, topk, b.w13_suh, row_pair, row_slot, counts,
                                                                u13, parts);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "moe_grouped: rotate");

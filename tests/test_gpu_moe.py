@@ -108,6 +108,26 @@ def test_moe_full_geometry_512_tokens_sampled(full_bank):
     assert_rows_close(got[sample], ref)
 
 
+@pytest.mark.parametrize("E,T,topk", ((160, 40, 4), (16, 1200, 8)))
+def test_moe_routing_paths_sampled(E, T, topk):
+    # E above the per-warp ranking table (one warp ranks every pair) and more
+    # pairs than the register-resident ranking holds (ranking through memory)
+    H, I = 256, 128
+    bank = syn.moe_bank(50 + E, E=E, H=H, I=I, distinct_down_k=True)
+    x, logits = syn.moe_tokens(51 + T, T, H=H, E=E)
+    ids, w = oracle.topk_softmax(logits, topk)
+    y, ws = run_moe(x, ids, w, bank_dev(bank), E, H, I)
+    assert m.exl3_workspace_error(ws) == 0
+    got = as_f64(y)
+    assert np.all(np.isfinite(got))
+    sample = np.unique(np.array([0, 1, T // 3, T // 2, T - 2, T - 1]))
+    ref = oracle.moe_f64(np.ascontiguousarray(x[sample]), np.ascontiguousarray(ids[sample]),
+                         np.ascontiguousarray(w[sample]), bank)
+    assert_rows_close(got[sample], ref)
+    y2, _ = run_moe(x, ids, w, bank_dev(bank), E, H, I, ws)
+    assert np.array_equal(bits(y), bits(y2))
+
+
 def test_moe_deterministic(full_bank):
     bank, bank_d = full_bank
     x, logits = syn.moe_tokens(41, 37)
