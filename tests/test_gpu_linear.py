@@ -32,6 +32,12 @@ def shard_dev(sh):
     return (dev(sh.code, torch.int16), *(dev(v, torch.float16) for v in (sh.s_in, sh.rin, sh.rout, sh.s_out)))
 
 
+def shard_set(sh, col0):
+    """(code, K, s_in, rin, rout, s_out, col0) on the device: one shard of a merged call."""
+    c, *sc = shard_dev(sh)
+    return (c, sh.K, *sc, col0)
+
+
 def test_codebook_table_exhaustive():
     got = bits(m.exl3_codebook_table())
     assert np.array_equal(got, oracle.codebook_table())
@@ -125,6 +131,59 @@ def test_gate_up_full_size_sampled_blocks(M):
         for blk in (0, 77, OC // 128 - 1):
             ref = oracle.linear_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=blk, nblk=1)
             assert_rows_close(got[:, i * OC + blk * 128:i * OC + (blk + 1) * 128], ref)
+
+
+@pytest.mark.parametrize("M", (1, 8, 16, 32, 64, 128))
+def test_gate_up_one_call_full_size_sampled_blocks(M):
+    # the benchmarked launch: both shards in one exl3_linear_into_shards call (decode
+    # mode to M = 16, the fused tensor-core kernel above); blocks on both sides of
+    # the shard boundary and at the ends
+    x, shards = syn.gate_up(1, M=M)
+    OC = 17408
+    out = torch.full((M, 2 * OC), NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    sets = [shard_set(sh, i * OC) for i, sh in enumerate(shards)]
+    ws = m.workspace(m.exl3_linear_shards_workspace_bytes(M, 5120, sets))
+    m.exl3_linear_into_shards(dev(x, torch.bfloat16), sets, out, ws)
+    torch.cuda.synchronize()
+    got = as_f64(out)
+    assert np.all(np.isfinite(got)), "a column of the output was left unwritten"
+    for i, sh in enumerate(shards):
+        for blk in (0, 1, 77, OC // 128 - 1):
+            ref = oracle.linear_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=blk, nblk=1)
+            assert_rows_close(got[:, i * OC + blk * 128:i * OC + (blk + 1) * 128], ref)
+    assert m.exl3_workspace_error(ws) == 0
+
+
+@pytest.mark.parametrize("M", (8, 8192))
+def test_decoder_layer_full_size_sampled(M):
+    # the five projections of the benchmarked decoder layer, launched as the bench
+    # launches them (qkv, o, down alone; gate and up in one call on gate's input)
+    projs = {n: (x, sh) for n, x, sh in syn.decoder_layer(4, M=M)}
+    sets = [shard_set(projs[n][1], c) for n, c in (("gate", 0), ("up", 17408))]
+    ws = m.workspace(max(m.exl3_linear_workspace_bytes(M, 17408, 17408),
+                         m.exl3_linear_shards_workspace_bytes(M, 5120, sets)))
+    rows = np.arange(M) if M <= 128 else np.array([0, 1, 127, 128, 4095, 8190, 8191])
+    checks = []
+    for name in ("qkv", "o", "down"):
+        x, sh = projs[name]
+        out = torch.full((M, sh.OC), NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+        c, *sc = shard_dev(sh)
+        m.exl3_linear_into(dev(x, torch.bfloat16), c, sh.K, *sc, out, 0, ws)
+        torch.cuda.synchronize()
+        checks.append((x, sh, as_f64(out), 0))
+    xg = projs["gate"][0]
+    out = torch.full((M, 2 * 17408), NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    m.exl3_linear_into_shards(dev(xg, torch.bfloat16), sets, out, ws)
+    torch.cuda.synchronize()
+    got_gu = as_f64(out)
+    checks += [(xg, projs["gate"][1], got_gu, 0), (xg, projs["up"][1], got_gu, 17408)]
+    for x, sh, got, col0 in checks:
+        assert np.all(np.isfinite(got[:, col0:col0 + sh.OC]))
+        xs = np.ascontiguousarray(x[rows])
+        for blk in (0, sh.OC // 256, sh.OC // 128 - 1):
+            ref = oracle.linear_f64(xs, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=blk, nblk=1)
+            assert_rows_close(got[rows, col0 + blk * 128:col0 + (blk + 1) * 128], ref)
+    assert m.exl3_workspace_error(ws) == 0
 
 
 def test_column_slice_isolation_and_merged_layer():
