@@ -10,47 +10,69 @@ namespace exl3 {
 // --------------------------------------------------------------------------
 // Activation pre-transform: u = Had128((x * s_in) * rin) per 128-channel
 // block (radiance_escha.py, module docstring "THE FORWARD", first factor).
-// One warp per (row, block); lane l holds channels 4l..4l+3 of the block.
+// One warp per (shard, row, run of bpw <= kPtRun consecutive blocks); lane l
+// holds channels 4l..4l+3 of a block.  A warp issues the loads of its whole run
+// before transforming it, so large calls keep enough bytes in flight; small
+// calls use runs of one block (more warps, shorter latency).
 // --------------------------------------------------------------------------
+constexpr int kPtRun = 4;
+
 __global__ void __launch_bounds__(256) pretransform_kernel(const uint16_t *__restrict__ x,
                                                            int64_t M, int IC,
                                                            const __grid_constant__ PretransformShards p,
-                                                           uint16_t *__restrict__ u) {
+                                                           uint16_t *__restrict__ u, int bpw) {
     // let a dependent launch (the GEMM that reads u) get scheduled early; it
     // still waits for this grid to finish before touching u
     asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int blocks = IC / kHad;
-    if (wid >= (int64_t)p.n * M * blocks) return;
-    const int sh = (int)(wid / (M * blocks));
-    const int64_t rem = wid % (M * blocks);
-    const int64_t m = rem / blocks;
-    const int c0 = (int)(rem % blocks) * kHad + 4 * lane;
-    const uint2 xv = *reinterpret_cast<const uint2 *>(x + m * IC + c0);
-    const uint2 sv = __ldg(reinterpret_cast<const uint2 *>(p.s_in[sh] + c0));
-    const uint2 rv = __ldg(reinterpret_cast<const uint2 *>(p.rin[sh] + c0));
-    const uint32_t xs[2] = {xv.x, xv.y}, ss[2] = {sv.x, sv.y}, rs[2] = {rv.x, rv.y};
-    float v[4];
+    const int runs = (blocks + bpw - 1) / bpw;
+    if (wid >= (int64_t)p.n * M * runs) return;
+    const int sh = (int)(wid / (M * runs));
+    const int64_t rem = wid % (M * runs);
+    const int64_t m = rem / runs;
+    const int b0 = (int)(rem % runs) * bpw;
+    uint2 xv[kPtRun], sv[kPtRun], rv[kPtRun];
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const uint32_t xb = (xs[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
-        const float sc = f16_bits_to_f32((uint16_t)(ss[i >> 1] >> (16 * (i & 1))));
-        const float r = f16_bits_to_f32((uint16_t)(rs[i >> 1] >> (16 * (i & 1))));
-        v[i] = (bf16_bits_to_f32(xb) * sc) * r;
+    for (int k = 0; k < kPtRun; k++) {
+        if (k < bpw && b0 + k < blocks) {
+            const int c0 = (b0 + k) * kHad + 4 * lane;
+            xv[k] = *reinterpret_cast<const uint2 *>(x + m * IC + c0);
+            sv[k] = __ldg(reinterpret_cast<const uint2 *>(p.s_in[sh] + c0));
+            rv[k] = __ldg(reinterpret_cast<const uint2 *>(p.rin[sh] + c0));
+        }
     }
-    warp_fwht128(v, lane);
-    uint2 o;
-    o.x = (uint32_t)f32_to_f16_bits(v[0] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[1] * kHadNorm) << 16);
-    o.y = (uint32_t)f32_to_f16_bits(v[2] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[3] * kHadNorm) << 16);
-    *reinterpret_cast<uint2 *>(u + ((int64_t)sh * M + m) * IC + c0) = o;
+#pragma unroll
+    for (int k = 0; k < kPtRun; k++) {
+        if (!(k < bpw && b0 + k < blocks)) break;   // warp-uniform
+        const int c0 = (b0 + k) * kHad + 4 * lane;
+        const uint32_t xs[2] = {xv[k].x, xv[k].y}, ss[2] = {sv[k].x, sv[k].y}, rs[2] = {rv[k].x, rv[k].y};
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint32_t xb = (xs[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+            const float sc = f16_bits_to_f32((uint16_t)(ss[i >> 1] >> (16 * (i & 1))));
+            const float r = f16_bits_to_f32((uint16_t)(rs[i >> 1] >> (16 * (i & 1))));
+            v[i] = (bf16_bits_to_f32(xb) * sc) * r;
+        }
+        warp_fwht128(v, lane);
+        uint2 o;
+        o.x = (uint32_t)f32_to_f16_bits(v[0] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[1] * kHadNorm) << 16);
+        o.y = (uint32_t)f32_to_f16_bits(v[2] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[3] * kHadNorm) << 16);
+        *reinterpret_cast<uint2 *>(u + ((int64_t)sh * M + m) * IC + c0) = o;
+    }
 }
 
 cudaError_t launch_pretransform_shards(const uint16_t *x, int64_t M, int IC, const PretransformShards &p,
                                        uint16_t *u, cudaStream_t s) {
-    const int64_t warps = (int64_t)p.n * M * (IC / kHad);
+    const int64_t blocks = (int64_t)p.n * M * (IC / kHad);
+    // runs of kPtRun blocks once the blocks alone fill several waves of warps
+    const int bpw = blocks >= (int64_t)device_info().sm_count * 64 * 8 ? kPtRun : 1;
+    const int64_t runs = (IC / kHad + bpw - 1) / bpw;
+    const int64_t warps = (int64_t)p.n * M * runs;
     const int64_t grid = (warps + 7) / 8;
-    pretransform_kernel<<<(unsigned)grid, 256, 0, s>>>(x, M, IC, p, u);
+    pretransform_kernel<<<(unsigned)grid, 256, 0, s>>>(x, M, IC, p, u, bpw);
     return cudaGetLastError();
 }
 

@@ -85,6 +85,18 @@ def test_pretransform_matches_oracle():
     assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -10 + 1e-6)
 
 
+@pytest.mark.parametrize("M,IC", ((16000, 640), (2500, 5120)))
+def test_pretransform_long_runs_matches_oracle(M, IC):
+    # enough blocks for the four-block runs per warp, including a row whose last
+    # run is short (IC / 128 = 5 blocks); rows sampled for the oracle
+    x, sh = syn.linear_case(61, M, IC, 128, 2, outlier_frac=0.01)
+    u = m.exl3_pretransform(dev(x, torch.bfloat16), dev(sh.s_in, torch.float16), dev(sh.rin, torch.float16))
+    rows = np.array([0, 1, M // 2, M - 2, M - 1])
+    ref = oracle.pretransform_f64(np.ascontiguousarray(x[rows]), sh.s_in, sh.rin)
+    got = as_f64(u)[rows]
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -10 + 1e-6)
+
+
 def run_linear(x, sh, ws=None):
     M = x.shape[0]
     if ws is None:
