@@ -57,6 +57,45 @@ const DeviceInfo &device_info() {
     return info[dev];
 }
 
+// Per (kernel, device): the dynamic shared-memory opt-in and the resident CTAs
+// per SM.  Both are properties of the current device, so they are cached per
+// device, under a lock (calls may come from several host threads).
+struct KernelSetup {
+    const void *kernel;
+    int dev;
+    size_t smem;
+    cudaError_t err;
+    int occ;
+};
+
+static KernelSetup kernel_setup(const void *kernel, int threads, size_t smem) {
+    static std::mutex mu;
+    static KernelSetup done[256];
+    static int n_done = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_done; i++)
+        if (done[i].kernel == kernel && done[i].dev == dev && done[i].smem == smem) return done[i];
+    KernelSetup k = {kernel, dev, smem, cudaSuccess, 1};
+    if (smem > 48 * 1024)
+        k.err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (k.err == cudaSuccess && threads > 0) {
+        k.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k.occ, kernel, threads, smem);
+        if (k.occ < 1) k.occ = 1;
+    }
+    if (n_done < 256) done[n_done++] = k;
+    return k;
+}
+
+cudaError_t kernel_smem_optin(const void *kernel, size_t smem) { return kernel_setup(kernel, 0, smem).err; }
+
+cudaError_t kernel_occupancy(const void *kernel, int threads, size_t smem, int *occ) {
+    const KernelSetup k = kernel_setup(kernel, threads, smem);
+    *occ = k.occ;
+    return k.err;
+}
+
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 size_t linear_workspace_layout_n(int64_t max_M, int32_t IC, int n_shards, int total_groups, int32_t max_OC,
                                  LinearWorkspace *ws, void *base);

@@ -35,8 +35,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -653,16 +651,8 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
 template <int NT, bool ROWS>
 cudaError_t launch_fused_t(const FusedArgs &a, int64_t total_units, cudaStream_t s) {
     using C = FtCfg<NT>;
-    static std::once_flag once[64];
-    static cudaError_t attr_err[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    std::call_once(once[dev], [&] {
-        attr_err[dev] =
-            cudaFuncSetAttribute(fused_tc_kernel<NT, ROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    });
-    if (attr_err[dev] != cudaSuccess) return attr_err[dev];
+    const cudaError_t ea = kernel_smem_optin((const void *)fused_tc_kernel<NT, ROWS>, C::SMEM);
+    if (ea != cudaSuccess) return ea;
     int64_t grid = device_info().sm_count;       // one CTA per SM (shared memory)
     if (grid > kFusedMaxCtas) grid = kFusedMaxCtas;
     if (grid > total_units) grid = total_units;

@@ -21,6 +21,11 @@ struct DeviceInfo {
     int max_smem_optin = 0;
 };
 const DeviceInfo &device_info();
+// Opt `kernel` in to `smem` bytes of dynamic shared memory on the current device
+// (once per kernel and device), and its resident CTAs per SM with `threads`
+// threads per CTA.
+cudaError_t kernel_smem_optin(const void *kernel, size_t smem);
+cudaError_t kernel_occupancy(const void *kernel, int threads, size_t smem, int *occ);
 
 // Workspace carving shared by the linear entry points.
 struct LinearWorkspace {

@@ -479,16 +479,10 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
 
 template <int NB, int KSET>
 static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t total_hint, cudaStream_t s) {
-    static int occ = -1;
     constexpr size_t smem = group_smem_bytes<NB>();
-    if (occ < 0) {
-        cudaError_t e = cudaFuncSetAttribute(group_gemm_kernel<NB, KSET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, group_gemm_kernel<NB, KSET>, 256, smem);
-        if (e != cudaSuccess) return e;
-        if (occ < 1) occ = 1;
-    }
+    int occ = 1;
+    cudaError_t e = kernel_occupancy((const void *)group_gemm_kernel<NB, KSET>, 256, smem, &occ);
+    if (e != cudaSuccess) return e;
     GroupGemmArgs a = a0;
     a.hash_xor = kHashXor;
     for (int i = 0; i < 17; i++) a.pow2[i] = 1u << i;

@@ -235,13 +235,8 @@ cudaError_t launch_prefill(const uint16_t *u, const uint16_t *wt, int64_t M, int
     if ((reinterpret_cast<uintptr_t>(u) | reinterpret_cast<uintptr_t>(wt)) & 15u) return cudaErrorInvalidValue;
     CUtensorMap tm_u, tm_w;
     if (!make_map_f16(&tm_u, u, M, IC, BM) || !make_map_f16(&tm_w, wt, OC, IC, BN)) return cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    cudaError_t ea = kernel_smem_optin((const void *)prefill_gemm_kernel, SMEM_BYTES);
+    if (ea != cudaSuccess) return ea;
     const int64_t tiles = ((M + BM - 1) / BM) * (int64_t)((OC + BN - 1) / BN);
     int64_t grid = device_info().sm_count;   // persistent: one CTA per SM
     if (grid > tiles) grid = tiles;
