@@ -45,3 +45,19 @@ def test_host_side_queries_without_gpu():
     assert st == m.EXL3_EUNSUPPORTED
     st = L.exl3_embed_int8_gather(None, None, 10, 24, None, 3, None, None, None)
     assert st == m.EXL3_EINVAL
+
+
+def test_workspace_sizes_never_shrink_as_the_call_grows():
+    # a workspace sized for the largest call serves every smaller one
+    b.build()
+    L = m.lib()
+    prev = 0
+    for M in range(0, 300):
+        v = L.exl3_linear_workspace_bytes(M, 5120, 17408)
+        assert v >= prev, (M, prev, v)
+        prev = v
+    prev = 0
+    for T in range(0, 1100, 3):
+        v = L.exl3_moe_workspace_bytes(T, 2048, 768, 128, 8)
+        assert v >= prev, (T, prev, v)
+        prev = v
