@@ -115,8 +115,11 @@ exl3_status exl3_workspace_error(const void *ws, size_t ws_bytes, int32_t *flag_
  *   ws     workspace of at least exl3_linear_workspace_bytes(M, IC, OC) bytes
  * Requires ldo >= OC, 0 <= col0, col0 + OC <= ldo, and 16-byte aligned x,
  * code, and out + col0 rows (ldo and col0 multiples of 8).
- * The decode/prefill choice by M is made inside this call (radiance_escha.py,
- * escha_linear_into: the M <= 64 switch lives in the op).
+ * The GEMM path is chosen by M inside this call (radiance_escha.py,
+ * escha_linear_into: the small-M / large-M switch lives in the op): a
+ * register-resident trellis decode for M <= 16, the trellis decoded into
+ * tensor-core operand tiles for M <= 128, reconstruct + tensor-core GEMM above.
+ * EXL3_FORCE_MODE=decode|fused|prefill in the environment overrides the choice.
  */
 exl3_status exl3_linear_into(const uint16_t *x, int64_t M, int32_t IC,
                              const int16_t *code, int32_t OC, int32_t K,
