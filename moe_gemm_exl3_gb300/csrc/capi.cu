@@ -102,7 +102,7 @@ size_t linear_workspace_layout_n(int64_t max_M, int32_t IC, int n_shards, int to
 
 // Fixed part of every workspace: error word, then the arrival counters.
 constexpr size_t kHeaderBytes = 256;
-constexpr size_t kCounterCount = 65536;
+constexpr size_t kCounterCount = kWorkspaceCounters;
 constexpr size_t kFixedBytes = kHeaderBytes + kCounterCount * sizeof(int32_t);
 
 size_t fixed_workspace_bytes() { return kFixedBytes; }

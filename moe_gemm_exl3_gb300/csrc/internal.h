@@ -15,6 +15,8 @@ constexpr int kDecodeMaxRows = 8 * kDecodeMaxNB;
 // Upper bound on decode-GEMM CTAs (persistent grid); sizes the partial slab.
 constexpr int kDecodeMaxCtas = 1024;
 constexpr int kDecodeWarps = 8;
+// Arrival counters in every workspace: one per output column group of a launch.
+constexpr size_t kWorkspaceCounters = 65536;
 
 struct DeviceInfo {
     int sm_count = 0;

@@ -61,6 +61,17 @@ bool moe_fused(int T, int H, int I, int E, int topk) {
     return fused_rows_fits(2 * max_entries, I / kHad, H) && fused_rows_fits(max_entries, H / kHad, I);
 }
 
+// Tokens one pass of the layer serves.  Every grouped-GEMM column group of a
+// launch owns one workspace arrival counter; a launch has at most
+// G * (ceil(R / 8) + E) groups (G column groups per entry, R = T * topk routed
+// rows, row blocks of at least 8), so passes of this many tokens never run out
+// of counters.  Longer calls run as several passes.  0: not even one token fits.
+int64_t moe_pass_tokens(int H, int I, int E, int topk) {
+    const int64_t G = 2 * (I / kHad) > H / kHad ? 2 * (I / kHad) : H / kHad;
+    const int64_t entries = (int64_t)kWorkspaceCounters / G - 1 - E;
+    return entries > 0 ? entries * 8 / topk : 0;
+}
+
 MoeLayout moe_layout(int T, int H, int I, int E, int topk) {
     MoeLayout L = {};
     L.R = T * topk;
@@ -510,7 +521,14 @@ size_t exl3_moe_workspace_bytes(int32_t T, int32_t H, int32_t I, int32_t E, int3
     if (T < 0 || H <= 0 || I <= 0 || H % 128 || I % 128 || E < 1 || E > kMoeMaxE || topk < 1 ||
         topk > kMoeMaxTopk)
         return 0;
-    return moe_layout(T, H, I, E, topk).total;
+    const int64_t P = moe_pass_tokens(H, I, E, topk);
+    if (P < 1) return 0;
+    if (T <= P) return moe_layout(T, H, I, E, topk).total;
+    // several passes of P tokens and a shorter last one
+    const size_t full = moe_layout((int)P, H, I, E, topk).total;
+    const int rest = (int)(T % P);
+    const size_t last = rest ? moe_layout(rest, H, I, E, topk).total : 0;
+    return full > last ? full : last;
 }
 
 exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I, int32_t E, int32_t topk,
@@ -523,7 +541,22 @@ exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
         return fail(EXL3_EINVAL, "%s: E = %d (1..%d), topk = %d (1..%d)", fn, E, kMoeMaxE, topk, kMoeMaxTopk);
     if ((int64_t)T * topk > (1 << 24)) return fail(EXL3_EINVAL, "%s: T * topk = %lld routes is too many", fn,
                                                    (long long)T * topk);
+    const int64_t P = moe_pass_tokens(H, I, E, topk);
+    if (P < 1)
+        return fail(EXL3_EINVAL, "%s: H = %d, I = %d, E = %d: more column groups than the workspace's %zu counters",
+                    fn, H, I, E, kWorkspaceCounters);
     if (T == 0) return EXL3_OK;
+    if (T > P) {
+        // passes of P tokens: each is the whole layer on its own rows of x, ids, w and y
+        if (!x || !ids || !w || !y) return fail(EXL3_EINVAL, "%s: null pointer", fn);
+        for (int64_t t0 = 0; t0 < T; t0 += P) {
+            const int32_t n = (int32_t)(T - t0 < P ? T - t0 : P);
+            const exl3_status st = exl3_moe_grouped(x + t0 * H, n, H, I, E, topk, ids + t0 * topk, w + t0 * topk, bank,
+                                                    y + t0 * H, wsp, ws_bytes, stream);
+            if (st != EXL3_OK) return st;
+        }
+        return EXL3_OK;
+    }
     if (!x || !ids || !w || !y || !bank) return fail(EXL3_EINVAL, "%s: null pointer", fn);
     const exl3_moe_bank &b = *bank;
     if (!b.w13 || !b.w2 || !b.off_w1 || !b.off_w3 || !b.off_w2 || !b.perm || !b.k_gu || !b.k_d || !b.w13_suh ||

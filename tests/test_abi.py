@@ -61,3 +61,17 @@ def test_workspace_sizes_never_shrink_as_the_call_grows():
         v = L.exl3_moe_workspace_bytes(T, 2048, 768, 128, 8)
         assert v >= prev, (T, prev, v)
         prev = v
+
+
+def test_long_moe_calls_run_in_passes_of_bounded_workspace():
+    # past the tokens one pass serves (its column groups must fit the workspace's
+    # arrival counters) the call runs in passes: the workspace stops growing
+    b.build()
+    L = m.lib()
+    sizes = [L.exl3_moe_workspace_bytes(T, 2048, 768, 128, 8) for T in (3000, 3967, 3968, 8000, 100000, 2097152)]
+    assert sizes[0] <= sizes[1]
+    assert max(sizes[2:]) <= sizes[1] * 1.01 and min(sizes[2:]) > 0
+    # a geometry whose column groups exceed the counters even for one token is refused on the host
+    assert L.exl3_moe_workspace_bytes(1, 128 * 40000, 128, 8, 2) == 0
+    st = L.exl3_moe_grouped(None, 1, 128 * 40000, 128, 8, 2, None, None, None, None, None, 0, None)
+    assert st == m.EXL3_EINVAL and b"counters" in L.exl3_last_error()

@@ -128,6 +128,23 @@ def test_moe_routing_paths_sampled(E, T, topk):
     assert np.array_equal(bits(y), bits(y2))
 
 
+def test_moe_long_call_runs_in_passes(full_bank):
+    # more tokens than one pass serves (the column groups of a pass must fit the
+    # workspace's arrival counters): the layer runs in passes over the token rows
+    bank, bank_d = full_bank
+    T = 4100
+    x, logits = syn.moe_tokens(42, T)
+    ids, w = oracle.topk_softmax(logits, 8)
+    y, ws = run_moe(x, ids, w, bank_d, 128, 2048, 768)
+    assert m.exl3_workspace_error(ws) == 0
+    got = as_f64(y)
+    assert np.all(np.isfinite(got))
+    sample = np.array([0, 1, 3966, 3967, 4099])
+    ref = oracle.moe_f64(np.ascontiguousarray(x[sample]), np.ascontiguousarray(ids[sample]),
+                         np.ascontiguousarray(w[sample]), bank)
+    assert_rows_close(got[sample], ref)
+
+
 def test_moe_deterministic(full_bank):
     bank, bank_d = full_bank
     x, logits = syn.moe_tokens(41, 37)
