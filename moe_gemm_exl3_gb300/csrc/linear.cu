@@ -24,6 +24,9 @@ __global__ void __launch_bounds__(256) pretransform_kernel(const uint16_t *__res
     // let a dependent launch (the GEMM that reads u) get scheduled early; it
     // still waits for this grid to finish before touching u
     asm volatile("griddepcontrol.launch_dependents;");
+    // this launch may itself start before the preceding kernel has finished (a
+    // programmatic dependent launch): wait for it before reading x or writing u
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int blocks = IC / kHad;
@@ -72,8 +75,16 @@ cudaError_t launch_pretransform_shards(const uint16_t *x, int64_t M, int IC, con
     const int64_t runs = (IC / kHad + bpw - 1) / bpw;
     const int64_t warps = (int64_t)p.n * M * runs;
     const int64_t grid = (warps + 7) / 8;
-    pretransform_kernel<<<(unsigned)grid, 256, 0, s>>>(x, M, IC, p, u, bpw);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pretransform_kernel, x, M, IC, p, u, bpw);
 }
 
 cudaError_t launch_pretransform(const uint16_t *x, int64_t M, int IC, const uint16_t *s_in,
@@ -252,25 +263,40 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
     int ar = a_lo + warp;
     uint2 un[NB];
     if constexpr (NB == 1) {
-        // two tile-row buffers used in turn: a buffer is refilled with the row two
-        // steps ahead as soon as its words are realigned, so no register copies
+        // two tile-row buffers used in turn, each refilled with the row two steps
+        // ahead as soon as its words are realigned (no register copies); the code
+        // and activation pointers advance by increments only
+        if (ar >= a_hi) return;
+        const int n = (a_hi - ar + kDecodeWarps - 1) / kDecodeWarps;
+        const int64_t stride = row_words * kDecodeWarps;
+        const uint32_t *p = tile0 + ar * row_words;
+        const bool urow = g < e.nrows;
+        const uint16_t *up = ub + (int64_t)g * IC + 16 * ar + 4 * q;
+        constexpr int kUS = 16 * kDecodeWarps;   // activation step (channels) per warp step
         uint32_t wa[2 * K], wb[2 * K];
-        if (ar < a_hi) load_quarter<K>(wa, tile0 + ar * row_words);
-        if (ar + kDecodeWarps < a_hi) load_quarter<K>(wb, tile0 + (ar + kDecodeWarps) * row_words);
-        load_u(un, ar);
-        auto row = [&](uint32_t (&w)[2 * K], int arc) {
+        uint2 ua = make_uint2(0u, 0u), ubv = make_uint2(0u, 0u);
+        load_quarter<K>(wa, p);
+        if (urow) ua = __ldg(reinterpret_cast<const uint2 *>(up));
+        if (n > 1) {
+            load_quarter<K>(wb, p + stride);
+            if (urow) ubv = __ldg(reinterpret_cast<const uint2 *>(up + kUS));
+        }
+        auto row = [&](uint32_t (&w)[2 * K], uint2 &uv, bool refill, const uint32_t *pn, const uint16_t *upn) {
             QuarterStream<K> st;
             st.build(w, quarter_prev_word(w[2 * K - 1], lane));
-            if (arc + 2 * kDecodeWarps < a_hi) load_quarter<K>(w, tile0 + (arc + 2 * kDecodeWarps) * row_words);
-            uint32_t b[NB][4];
-            dup_u(b, un);
-            load_u(un, arc + kDecodeWarps);
+            uint32_t b[NB][4] = {{dup_half_lo(uv.x), dup_half_hi(uv.x), dup_half_lo(uv.y), dup_half_hi(uv.y)}};
+            if (refill) {
+                load_quarter<K>(w, pn);
+                if (urow) uv = __ldg(reinterpret_cast<const uint2 *>(upn));
+            }
             mma_row(st, b);
         };
-        for (; ar < a_hi; ar += 2 * kDecodeWarps) {
-            row(wa, ar);
-            if (ar + kDecodeWarps >= a_hi) break;
-            row(wb, ar + kDecodeWarps);
+        for (int i = 0; i < n; i += 2) {
+            row(wa, ua, i + 2 < n, p + 2 * stride, up + 2 * kUS);
+            if (i + 1 >= n) break;
+            row(wb, ubv, i + 3 < n, p + 3 * stride, up + 3 * kUS);
+            p += 2 * stride;
+            up += 2 * kUS;
         }
     } else {
         // one rotating prefetch queue (fewer live registers with more rows)
@@ -318,6 +344,9 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
 
     // everything below reads what the preceding kernel in the stream wrote
     grid_dependency_wait();
+    // the next kernel in the stream may be scheduled now: it must itself wait for
+    // this grid to complete before touching memory (every kernel here does)
+    asm volatile("griddepcontrol.launch_dependents;");
 
     int n_groups;
     const int n_entries = a.n_entries_dev ? *a.n_entries_dev : a.n_inline;
