@@ -194,14 +194,19 @@ class GateUp:
     def code_bytes(self, K):
         return self.IC * self.OC * K // 8
 
+    _codes = {}   # device code copies, shared by every M of one run
+
     def setup(self, torch, m, syn, dev):
         M, IC, OC = self.M, self.IC, self.OC
         self.x, shards = syn.gate_up(1, M=M)
         per_step = sum(self.code_bytes(K) for K in self.KS)
         self.R = R = max(4, int(np.ceil(4 * L2_BYTES / per_step)))
-        codes = [[t16(torch, s.code, dev, torch.int16) for s in shards]]
-        for _ in range(R - 1):
-            codes.append([c.clone() for c in codes[0]])
+        codes = GateUp._codes.get(R)
+        if codes is None:
+            codes = [[t16(torch, s.code, dev, torch.int16) for s in shards]]
+            for _ in range(R - 1):
+                codes.append([c.clone() for c in codes[0]])
+            GateUp._codes[R] = codes
         scal = [[t16(torch, v, dev, torch.float16) for v in (s.s_in, s.rin, s.rout, s.s_out)] for s in shards]
         self.sets = [[(codes[r][i], s.K, *scal[i], i * OC) for i, s in enumerate(shards)] for r in range(R)]
         self.xd = t16(torch, self.x, dev, torch.bfloat16)
@@ -341,7 +346,6 @@ class Moe:
         return {"workload": f"moe E=128 H=2048 I=768 top-8, T={self.T}, K per expert in {{2,3,4}}", "T": self.T}
 
     def setup(self, torch, m, syn, dev):
-        import oracle
         self.bank_np = syn.moe_bank(3)
         dt = dict(w13=torch.int16, w2=torch.int16, off_w1=torch.int64, off_w3=torch.int64, off_w2=torch.int64,
                   perm=torch.int32, k_gu=torch.int32, k_d=torch.int32, w13_suh=torch.float16,
@@ -365,7 +369,9 @@ class Moe:
         per_slot = 3 * self.H * self.I * kk // 8
         self.touched = []
         for r in range(R):
-            ids, _ = oracle.topk_softmax(self.ls[r].cpu().numpy(), self.TOPK)
+            # experts a batch touches (bookkeeping for the byte count: the largest
+            # logits, ties to the lower expert id)
+            ids = np.argsort(-self.ls[r].cpu().numpy(), axis=1, kind="stable")[:, :self.TOPK]
             slots = np.unique(self.bank_np["perm"][ids.ravel()])
             self.touched.append(int(per_slot[slots].sum()))
         bank_mb = (self.bank["w13"].numel() + self.bank["w2"].numel()) * 2 / 1e6
@@ -549,6 +555,87 @@ WORKLOADS = {"gate_up": GateUp, "prefill": Prefill, "moe": Moe, "gather": Gather
 
 
 # ------------------------------------------------------------------ our arm
+def capture(torch, stream, fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def timed_steps(torch, stream, wl, K, W, dist, min_seconds, min_trials=5):
+    """Time exactly K steps per trial (CUDA events on `stream`, a barrier and a
+    device synchronize on both sides), after at least W warm-up steps; trials repeat
+    until they add up to min_seconds.  Returns the trial durations in ms."""
+    R = wl.R
+    with torch.cuda.stream(stream):
+        for r in range(R):
+            wl.step(r)                       # eager warm-up of every path
+    torch.cuda.synchronize()
+    g_full = capture(torch, stream, lambda: [wl.step(r) for r in range(R)])
+    rem = K % R
+    g_rem = capture(torch, stream, lambda: [wl.step(r) for r in range(rem)]) if rem else None
+    torch.cuda.synchronize()
+
+    def k_steps():
+        for _ in range(K // R):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+
+    with torch.cuda.stream(stream):
+        for _ in range(-(-W // R)):
+            g_full.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    trials, total = [], 0.0
+    while len(trials) < min_trials or total < min_seconds:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            k_steps()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        t = e0.elapsed_time(e1)
+        trials.append(t)
+        total += t / 1e3
+        if len(trials) >= 200000:
+            break
+    return trials
+
+
+def secondary_workloads():
+    """The other configurations timed beside the headline (one GPU): each line
+    carries its own throughput and the roofline of its dominant kernel."""
+    ns = argparse.Namespace
+    return [("gate_up", ns(m=1)), ("gate_up", ns(m=64)), ("prefill", ns(m=8192, k=2)),
+            ("moe", ns(t=1)), ("moe", ns(t=16)), ("moe", ns(t=512)), ("gather", ns()),
+            ("layer", ns(m=8)), ("layer", ns(m=8192))]
+
+
+def run_secondary(torch, m, syn, dev, stream, local, K, W, min_seconds):
+    out = []
+    for name, a in secondary_workloads():
+        wl = WORKLOADS[name](a)
+        wl.setup(torch, m, syn, dev)
+        k = K if getattr(wl, "M", 0) <= 128 and name != "prefill" else max(wl.R, min(K, 20))
+        with Clocks(local) as clk:
+            trials = timed_steps(torch, stream, wl, k, W, None, min_seconds)
+        ms = statistics.median(trials)
+        value = job_throughput(1, wl.units_per_step, k, ms)
+        out.append({"workload": wl.config()["workload"], "metric": wl.metric, "value": round(value, 3),
+                    "unit": wl.unit, "steps": k, "trials": len(trials), "ms_per_step": round(ms / k, 5),
+                    "roofline": wl.roofline(torch, stream), "clocks": clk.summary()})
+        del wl
+        GateUp._codes.clear() if name == "gate_up" and a.m == 64 else None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import moe_gemm_exl3_gb300 as m
@@ -566,46 +653,18 @@ def run_ours(args):
     wl = WORKLOADS[args.workload](args)
     wl.setup(torch, m, syn, dev)
     R = wl.R
-
     stream = torch.cuda.Stream(dev)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for r in range(R):
-            wl.step(r)                       # eager warm-up of every path
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for r in range(R):
-                wl.step(r)
-    torch.cuda.synchronize()
-
-    steps = max(R, (args.steps // R) * R)
-    reps = steps // R
-    warm = max(1, -(-args.warmup // R))
-    with torch.cuda.stream(stream):
-        for _ in range(warm):
-            g.replay()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    K, W = args.steps, args.warmup
     with Clocks(local) as clk:
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    ms = max_over_ranks(torch, dist, e0.elapsed_time(e1), dev)
-    value = job_throughput(world, wl.units_per_step, steps, ms)
+        trials = timed_steps(torch, stream, wl, K, W, dist, args.min_seconds)
+    ms = max_over_ranks(torch, dist, statistics.median(trials), dev)
+    value = job_throughput(world, wl.units_per_step, K, ms)
 
     roof = wl.roofline(torch, stream)
 
     # ---- end to end through the public API with host buffers (pinned), eager launches
     xh, xdev, oh, out = wl.e2e_io(torch, dev)
-    e2e_steps = max(R, min(steps, 20 * R))
+    e2e_steps = max(R, min(K, 20 * R))
     with torch.cuda.stream(stream):
         for r in range(R):
             xdev.copy_(xh, non_blocking=True)
@@ -623,27 +682,36 @@ def run_ours(args):
     e2e_ms = max_over_ranks(torch, dist, a0.elapsed_time(a1) / e2e_steps, dev)
     e2e_val = job_throughput(world, wl.units_per_step, 1, e2e_ms)
 
+    line = {
+        "metric": wl.metric, "value": round(value, 3), "unit": wl.unit, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded; uniform int16 code words, N(0,1) activations)",
+        "config": dict(wl.config(), l2=wl.l2,
+                       timing=(f"median of {len(trials)} timed trials of exactly {K} steps each "
+                               f"({sum(trials) / 1e3:.2f} s timed); each trial replays CUDA graphs of the "
+                               f"steps between CUDA events, barrier + synchronize on both sides"),
+                       parallelism="replicas" if world > 1 else "single GPU"),
+        "gpu_launches": wl.launches_per_step * K,
+        "roofline": roof,
+        "e2e": {"value": round(e2e_val, 3), "unit": wl.unit,
+                "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
+                "d2h_bytes_per_step": int(oh.numel() * oh.element_size()),
+                "note": "public API with pinned host input copied in and the result read back every step, "
+                        "eager launches"},
+        "clocks": clk.summary(),
+    }
+    del xh, xdev, oh, out
+    if world == 1 and not args.no_secondary and args.workload == "gate_up" and args.m == 8:
+        del wl
+        torch.cuda.empty_cache()
+        line["secondary"] = run_secondary(torch, m, syn, dev, stream, local, K, W, args.secondary_seconds)
     if rank == 0:
-        line = {
-            "metric": wl.metric, "value": round(value, 3), "unit": wl.unit, "n_gpus": world,
-            "steps": steps, "warmup": warm * R, "ms_per_step": round(ms / steps, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
-            "data": "synthetic (seeded; uniform int16 code words, N(0,1) activations)",
-            "config": dict(wl.config(), l2=wl.l2, timing=f"CUDA graph of {R} steps, replayed; CUDA events",
-                           parallelism="replicas" if world > 1 else "single GPU"),
-            "gpu_launches": wl.launches_per_step * steps,
-            "roofline": roof,
-            "e2e": {"value": round(e2e_val, 3), "unit": wl.unit,
-                    "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
-                    "d2h_bytes_per_step": int(oh.numel() * oh.element_size()),
-                    "note": "public API with pinned host input copied in and the result read back every step, "
-                            "eager launches"},
-            "clocks": clk.summary(),
-        }
         if not args.no_cpu_baseline and world == 1:
-            v, sample = wl.cpu_sample(args.cpu_budget)
-            line["cpu_baseline"] = {"value": round(v, 4), "unit": wl.unit, "cores": omp_threads(), "kind": "oracle",
-                                    "sample": sample}
+            wl0 = WORKLOADS[args.workload](args)
+            v, sample = wl0.cpu_sample(args.cpu_budget)
+            line["cpu_baseline"] = {"value": round(v, 4), "unit": wl0.unit, "cores": omp_threads(),
+                                    "kind": "oracle", "sample": sample}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -709,16 +777,18 @@ def main():
     ap.add_argument("--t", type=int, default=16, help="tokens (moe)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the other configurations")
+    ap.add_argument("--min-seconds", type=float, default=1.5, help="timed seconds of the headline trials")
+    ap.add_argument("--secondary-seconds", type=float, default=0.3, help="timed seconds per secondary line")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds of oracle work (reference arm)")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = {"gate_up": 50000, "prefill": 300, "moe": 4000, "gather": 5000, "layer": 4000}[args.workload]
-        if args.workload == "layer" and args.m > 32:
-            args.steps = 100
+        args.steps = 200 if args.workload != "prefill" and not (args.workload == "layer" and args.m > 128) else 20
     if args.warmup is None:
-        args.warmup = 200 if args.workload == "gate_up" else 20
-    args.warmup = max(3, args.warmup)
+        args.warmup = 20
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
     else:
