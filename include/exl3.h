@@ -103,6 +103,23 @@ exl3_status exl3_workspace_error(const void *ws, size_t ws_bytes, int32_t *flag_
 /* ------------------------------------------------------------------ linear */
 
 /*
+ * Test and measurement hook: pin the GEMM path every linear call takes,
+ * process-wide, instead of choosing it by the number of rows.  Workspace
+ * queries made while a path is pinned size for that path, so query after
+ * pinning.  EXL3_PATH_BY_ROWS (the default) restores the normal choice.  The
+ * decode path serves any M (in passes of 32 rows); the fused path applies to
+ * M <= 128 and otherwise falls back to the choice by rows.  Returns
+ * EXL3_EINVAL for any other value.  Not for concurrent use with running calls.
+ */
+enum {
+    EXL3_PATH_BY_ROWS = 0,
+    EXL3_PATH_DECODE = 1,
+    EXL3_PATH_FUSED = 2,
+    EXL3_PATH_PREFILL = 3
+};
+exl3_status exl3_set_gemm_path(int32_t path);
+
+/*
  * One EXL3 projection into a column slice of a caller-owned output
  * (radiance_escha.py, escha_linear_into):
  *   x      bf16 [M][IC], row-major, contiguous
@@ -118,8 +135,8 @@ exl3_status exl3_workspace_error(const void *ws, size_t ws_bytes, int32_t *flag_
  * The GEMM path is chosen by M inside this call (radiance_escha.py,
  * escha_linear_into: the small-M / large-M switch lives in the op): a
  * register-resident trellis decode for M <= 16, the trellis decoded into
- * tensor-core operand tiles for M <= 128, reconstruct + tensor-core GEMM above.
- * EXL3_FORCE_MODE=decode|fused|prefill in the environment overrides the choice.
+ * tensor-core operand tiles for M <= 128, reconstruct + tensor-core GEMM above
+ * (exl3_set_gemm_path pins one path for tests and measurements).
  */
 exl3_status exl3_linear_into(const uint16_t *x, int64_t M, int32_t IC,
                              const int16_t *code, int32_t OC, int32_t K,
@@ -158,11 +175,12 @@ exl3_status exl3_gemm_into(const uint16_t *u, int64_t M, int32_t IC,
  * M <= 8, IC <= 32768, OC <= 65536; larger requests return EXL3_EINVAL and
  * launch nothing.  The call allocates and frees nothing.
  *
- * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
- * Every call on a device shares the one array and clears its counters on
- * entry, so calls that overlap on the GPU (different streams, or other
- * threads) race and give wrong results: serialize them.
+ * Every call looks up the array's device address on the current device; the
+ * first call on a device may load the library's device code there, so make
+ * that first call before any stream capture.  Every call on a device shares
+ * the one array and clears its counters on entry, so calls that overlap on
+ * the GPU (different streams, or other threads) race and give wrong results:
+ * serialize them.
  */
 exl3_status exl3_linear_into_noalloc(const uint16_t *x, int64_t M, int32_t IC,
                                      const int16_t *code, int32_t OC, int32_t K,

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "EXL3_OK", 1: "EXL3_EINVAL", 2: "EXL3_EWORKSPACE", 3: "EXL3_E
 
 # Every symbol include/exl3.h declares.
 EXPORTS = ("exl3_last_error", "exl3_version", "exl3_linear_workspace_bytes", "exl3_workspace_init",
-           "exl3_workspace_error", "exl3_linear_into", "exl3_linear", "exl3_gemm_into", "exl3_linear_into_noalloc",
+           "exl3_workspace_error", "exl3_set_gemm_path", "exl3_linear_into", "exl3_linear", "exl3_gemm_into", "exl3_linear_into_noalloc",
            "exl3_linear_shards_workspace_bytes", "exl3_linear_into_shards", "exl3_gemm_into_shards", "exl3_pretransform",
            "exl3_reconstruct", "exl3_codebook_table", "exl3_moe_topk_softmax",
            "exl3_moe_workspace_bytes", "exl3_moe_grouped", "exl3_embed_int8_gather")
@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
                 "exl3_linear_workspace_bytes": ([i64, i32, i32], sz),
                 "exl3_workspace_init": ([vp, sz, vp], ctypes.c_int),
                 "exl3_workspace_error": ([vp, sz, ctypes.POINTER(ctypes.c_int32), vp], ctypes.c_int),
+                "exl3_set_gemm_path": ([i32], ctypes.c_int),
                 "exl3_linear_into": ([vp, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, i64, i64, vp, sz,
                                       vp], ctypes.c_int),
                 "exl3_linear": ([vp, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp],
@@ -122,6 +123,15 @@ def _check(st: int, fn: str):
 
 def exl3_version() -> str:
     return lib().exl3_version().decode()
+
+
+GEMM_PATHS = {"rows": 0, "decode": 1, "fused": 2, "prefill": 3}
+
+
+def exl3_set_gemm_path(path) -> None:
+    """Pin the GEMM path of every linear call ("rows" restores the choice by M);
+    a test and measurement hook.  Size workspaces after pinning."""
+    _check(lib().exl3_set_gemm_path(GEMM_PATHS.get(path, path)), "exl3_set_gemm_path")
 
 
 # ---------------------------------------------------------------- workspace

@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/exl3.h"
@@ -17,12 +18,19 @@ namespace exl3 {
 
 static thread_local char g_err[512] = "";
 
+// EXL3_TRACE in the environment (read once) prints every call's path and every
+// error message to stderr.
+static bool trace_on() {
+    static const bool on = std::getenv("EXL3_TRACE") != nullptr;
+    return on;
+}
+
 exl3_status fail(exl3_status st, const char *fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
     vsnprintf(g_err, sizeof(g_err), fmt, ap);
     va_end(ap);
-    if (std::getenv("EXL3_TRACE")) std::fprintf(stderr, "[exl3] error: %s\n", g_err);
+    if (trace_on()) std::fprintf(stderr, "[exl3] error: %s\n", g_err);
     return st;
 }
 
@@ -31,7 +39,7 @@ exl3_status cuda_fail(cudaError_t e, const char *where) {
 }
 
 void trace(const char *fmt, ...) {
-    if (!std::getenv("EXL3_TRACE")) return;
+    if (!trace_on()) return;
     va_list ap;
     va_start(ap, fmt);
     std::fprintf(stderr, "[exl3] ");
@@ -116,19 +124,15 @@ int32_t *workspace_counters(void *base) {
 //   fused    M <= kFusedMaxRows: decode into shared memory + tcgen05 MMAs
 //   prefill  larger M: reconstruct W^T once, then the persistent tcgen05 GEMM
 // The boundaries are where the measured times of neighbouring paths cross on
-// the 5120 -> 2 x 17408 projection.  EXL3_FORCE_MODE=decode|fused|prefill
-// overrides the choice (read on every call).
+// the 5120 -> 2 x 17408 projection.  exl3_set_gemm_path() pins one path for
+// tests and A/B measurements; workspace queries made while it is pinned size
+// for that path too.
 constexpr int64_t kDecodeModeMaxRows = 16;
 enum class GemmMode { kDecode, kFused, kPrefill };
 
-int forced_mode() {
-    const char *f = std::getenv("EXL3_FORCE_MODE");
-    if (!f) return 0;
-    if (!std::strcmp(f, "decode")) return 1;
-    if (!std::strcmp(f, "fused")) return 2;
-    if (!std::strcmp(f, "prefill")) return 3;
-    return 0;
-}
+static std::atomic<int> g_gemm_path{0};
+
+int forced_mode() { return g_gemm_path.load(std::memory_order_relaxed); }
 
 GemmMode gemm_mode(int64_t M) {
     const int force = forced_mode();
@@ -194,7 +198,14 @@ extern "C" {
 
 const char *exl3_last_error(void) { return g_err; }
 
-const char *exl3_version(void) { return "exl3-gb300 0.1.0 (sm_103a)"; }
+const char *exl3_version(void) { return "exl3-gb300 0.2.0 (sm_103a)"; }
+
+exl3_status exl3_set_gemm_path(int32_t path) {
+    if (path < EXL3_PATH_BY_ROWS || path > EXL3_PATH_PREFILL)
+        return fail(EXL3_EINVAL, "set_gemm_path: path = %d (0 by rows, 1 decode, 2 fused, 3 prefill)", path);
+    g_gemm_path.store(path, std::memory_order_relaxed);
+    return EXL3_OK;
+}
 
 size_t exl3_linear_workspace_bytes(int64_t max_M, int32_t max_IC, int32_t max_OC) {
     if (max_M < 0 || max_IC <= 0 || max_OC <= 0 || max_IC % 128 || max_OC % 128 ||

@@ -146,7 +146,7 @@ bool fused_rows_fits(int64_t max_entries, int groups_per_entry, int IC);
 cudaError_t launch_fused_rows(FusedArgs &a, const uint16_t *u, int64_t u_rows, int64_t max_entries,
                               cudaStream_t s);
 
-// EXL3_FORCE_MODE: 0 none, 1 decode, 2 fused, 3 prefill (read on every call).
+// The GEMM path pinned by exl3_set_gemm_path: 0 none (by rows), 1 decode, 2 fused, 3 prefill.
 int forced_mode();
 
 bool prefill_supported();

@@ -5,12 +5,11 @@
 // The scratch array is a file-scope __device__ variable: it exists on every
 // GPU that loads this library, from module load until process exit, and every
 // call on that GPU shares it.  Host code cannot use the array's name as a
-// device address (on the host it names a host-side shadow), so the first call
-// on each device looks the real address up with cudaGetSymbolAddress while
-// that device is current, and every launch is given that address.
+// device address (on the host it names a host-side shadow), so every call
+// looks the real address up with cudaGetSymbolAddress while the caller's
+// device is current, and every launch is given that address.  The look-up is
+// not cached: after a device reset the module is loaded again at a new address.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "../../include/exl3.h"
 #include "internal.h"
@@ -39,23 +38,12 @@ constexpr size_t kNaBytes = kNaHeader + kNaCounters + kNaU + kNaSlab;   // 6.8 M
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaBytes];
 
-std::mutex g_mu;
-void *g_addr[64] = {};   // device address of g_noalloc_scratch, per device ordinal
-
-// Looks up the scratch array's device address for the current device (once).
+// The scratch array's device address on the current device.
 exl3_status scratch_address(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "linear_into_noalloc: cudaGetDevice");
-    if (dev < 0 || dev >= 64) return fail(EXL3_EUNSUPPORTED, "linear_into_noalloc: device ordinal %d >= 64", dev);
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "linear_into_noalloc: cudaGetSymbolAddress");
-        g_addr[dev] = p;
-    }
-    *out = g_addr[dev];
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "linear_into_noalloc: cudaGetSymbolAddress");
+    *out = p;
     return EXL3_OK;
 }
 

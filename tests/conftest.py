@@ -17,3 +17,12 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle.lib()
+
+
+@pytest.fixture
+def pin_gemm_path():
+    """Pin the library's GEMM path for one test (a test hook of the C ABI); the
+    choice by rows is restored afterwards."""
+    import moe_gemm_exl3_gb300 as m
+    yield m.exl3_set_gemm_path
+    m.exl3_set_gemm_path("rows")

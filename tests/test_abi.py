@@ -56,11 +56,12 @@ def test_workspace_sizes_never_shrink_as_the_call_grows():
         v = L.exl3_linear_workspace_bytes(M, 5120, 17408)
         assert v >= prev, (M, prev, v)
         prev = v
-    prev = 0
-    for T in range(0, 1100, 3):
-        v = L.exl3_moe_workspace_bytes(T, 2048, 768, 128, 8)
-        assert v >= prev, (T, prev, v)
-        prev = v
+    for H, I, E, topk in ((2048, 768, 128, 8), (1024, 512, 8, 2), (512, 256, 64, 4)):
+        prev = 0
+        for T in list(range(0, 1100, 3)) + [4000, 9000, 20000, 70000]:
+            v = L.exl3_moe_workspace_bytes(T, H, I, E, topk)
+            assert v >= prev, (H, I, E, topk, T, prev, v)
+            prev = v
 
 
 def test_long_moe_calls_run_in_passes_of_bounded_workspace():

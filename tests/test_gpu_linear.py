@@ -115,6 +115,12 @@ def test_linear_parity_small(K, M):
     assert_rows_close(as_f64(y), ref)
 
 
+def sample_rows(M):
+    """Every row for decode-sized calls; for larger M, rows at both ends and the middle
+    (the split-K partition and the reduction depend on the column group, not the row)."""
+    return np.arange(M) if M <= 16 else np.unique(np.array([0, 1, M // 2, M - 2, M - 1]))
+
+
 def test_single_linear_workload():
     x, sh = syn.single_linear(0)
     y = run_linear(x, sh)
@@ -123,9 +129,9 @@ def test_single_linear_workload():
 
 
 @pytest.mark.parametrize("M", (1, 8, 64))
-def test_gate_up_full_size_sampled_blocks(M):
-    # the decode-shaped merged gate (K=2) / up (K=3) layer into one out[M, 34816];
-    # the oracle computes three 128-column blocks of each shard
+def test_gate_up_full_size_per_shard_calls(M):
+    # the decode-shaped merged gate (K=2) / up (K=3) layer into one out[M, 34816],
+    # one exl3_linear_into call per shard; every column against the oracle
     x, shards = syn.gate_up(1, M=M)
     OC = 17408
     out = torch.full((M, 2 * OC), 0, dtype=torch.int16, device="cuda")
@@ -139,17 +145,18 @@ def test_gate_up_full_size_sampled_blocks(M):
     torch.cuda.synchronize()
     got = as_f64(out)
     assert np.all(np.isfinite(got)), "a column of the output was left unwritten"
+    rows = sample_rows(M)
+    xs = np.ascontiguousarray(x[rows])
     for i, sh in enumerate(shards):
-        for blk in (0, 77, OC // 128 - 1):
-            ref = oracle.linear_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=blk, nblk=1)
-            assert_rows_close(got[:, i * OC + blk * 128:i * OC + (blk + 1) * 128], ref)
+        ref = oracle.linear_f64(xs, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out)
+        assert_rows_close(got[rows, i * OC:(i + 1) * OC], ref)
 
 
 @pytest.mark.parametrize("M", (1, 8, 16, 32, 64, 128))
-def test_gate_up_one_call_full_size_sampled_blocks(M):
+def test_gate_up_one_call_full_size_every_column(M):
     # the benchmarked launch: both shards in one exl3_linear_into_shards call (decode
-    # mode to M = 16, the fused tensor-core kernel above); blocks on both sides of
-    # the shard boundary and at the ends
+    # mode to M = 16, the fused tensor-core kernel above); every 128-column block of
+    # both shards is compared with the oracle, on every row up to M = 16
     x, shards = syn.gate_up(1, M=M)
     OC = 17408
     out = torch.full((M, 2 * OC), NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
@@ -159,17 +166,20 @@ def test_gate_up_one_call_full_size_sampled_blocks(M):
     torch.cuda.synchronize()
     got = as_f64(out)
     assert np.all(np.isfinite(got)), "a column of the output was left unwritten"
+    rows = sample_rows(M)
+    xs = np.ascontiguousarray(x[rows])
     for i, sh in enumerate(shards):
-        for blk in (0, 1, 77, OC // 128 - 1):
-            ref = oracle.linear_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=blk, nblk=1)
-            assert_rows_close(got[:, i * OC + blk * 128:i * OC + (blk + 1) * 128], ref)
+        ref = oracle.linear_f64(xs, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out)
+        assert_rows_close(got[rows, i * OC:(i + 1) * OC], ref)
     assert m.exl3_workspace_error(ws) == 0
 
 
 @pytest.mark.parametrize("M", (8, 8192))
-def test_decoder_layer_full_size_sampled(M):
+def test_decoder_layer_full_size_every_column(M):
     # the five projections of the benchmarked decoder layer, launched as the bench
-    # launches them (qkv, o, down alone; gate and up in one call on gate's input)
+    # launches them (qkv, o, down alone; gate and up in one call on gate's input);
+    # every output column of every projection, on all rows at M = 8 and on rows at
+    # both ends and the middle at M = 8192
     projs = {n: (x, sh) for n, x, sh in syn.decoder_layer(4, M=M)}
     sets = [shard_set(projs[n][1], c) for n, c in (("gate", 0), ("up", 17408))]
     ws = m.workspace(max(m.exl3_linear_workspace_bytes(M, 17408, 17408),
@@ -192,9 +202,8 @@ def test_decoder_layer_full_size_sampled(M):
     for x, sh, got, col0 in checks:
         assert np.all(np.isfinite(got[:, col0:col0 + sh.OC]))
         xs = np.ascontiguousarray(x[rows])
-        for blk in (0, sh.OC // 256, sh.OC // 128 - 1):
-            ref = oracle.linear_f64(xs, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=blk, nblk=1)
-            assert_rows_close(got[rows, col0 + blk * 128:col0 + (blk + 1) * 128], ref)
+        ref = oracle.linear_f64(xs, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out)
+        assert_rows_close(got[rows, col0:col0 + sh.OC], ref)
     assert m.exl3_workspace_error(ws) == 0
 
 
@@ -293,11 +302,11 @@ def test_shards_call_equals_per_shard_calls(M):
 # ---------------------------------------------------------------- fused tensor-core path (8 < M <= 128)
 
 @pytest.mark.parametrize("M", (9, 16, 17, 31, 64, 65, 100, 128))
-def test_fused_parity_split_and_whole_groups(M, monkeypatch):
+def test_fused_parity_split_and_whole_groups(M, pin_gemm_path):
     # 160 column groups of 8 stages over one persistent grid: some groups are
     # reduced across CTAs through the split-K slab, others owned by one CTA;
     # M spans all four accumulator widths (16, 32, 64, 128 rows)
-    monkeypatch.setenv("EXL3_FORCE_MODE", "fused")
+    pin_gemm_path("fused")
     K = 2 + M % 3
     x, sh = syn.linear_case(300 + M, M, 512, 20480, K)
     ws = m.workspace(m.exl3_linear_workspace_bytes(M, sh.IC, sh.OC))
@@ -308,9 +317,9 @@ def test_fused_parity_split_and_whole_groups(M, monkeypatch):
 
 
 @pytest.mark.parametrize("mode", ("decode", "fused", "prefill"))
-def test_forced_modes_agree_with_oracle(mode, monkeypatch):
+def test_forced_modes_agree_with_oracle(mode, pin_gemm_path):
     # every GEMM path serves the same M; each must match the oracle
-    monkeypatch.setenv("EXL3_FORCE_MODE", mode)
+    pin_gemm_path(mode)
     x, sh = syn.linear_case(77, 24, 1024, 768, 3)
     y = run_linear(x, sh)
     ref = oracle.linear_f64(x, sh.code, 3, sh.s_in, sh.rin, sh.rout, sh.s_out)
@@ -318,9 +327,9 @@ def test_forced_modes_agree_with_oracle(mode, monkeypatch):
 
 
 @pytest.mark.parametrize("M", (12, 96))
-def test_gemm_into_fused_from_caller_activations(M, monkeypatch):
+def test_gemm_into_fused_from_caller_activations(M, pin_gemm_path):
     # caller-supplied pre-transformed activations go straight to the fused GEMM
-    monkeypatch.setenv("EXL3_FORCE_MODE", "fused")
+    pin_gemm_path("fused")
     x, sh = syn.linear_case(500 + M, M, 1024, 1280, 4)
     c, s_in, rin, rout, s_out = shard_dev(sh)
     u = m.exl3_pretransform(dev(x, torch.bfloat16), s_in, rin)
@@ -342,10 +351,10 @@ def test_fused_repeated_calls_deterministic():
     assert np.array_equal(a, b)
 
 
-def test_fused_single_stage_segments(monkeypatch):
+def test_fused_single_stage_segments(pin_gemm_path):
     # IC = 128: two stages per column group, so CTAs at group boundaries get
     # one-stage segments that only one of the two MMA issuers accumulates
-    monkeypatch.setenv("EXL3_FORCE_MODE", "fused")
+    pin_gemm_path("fused")
     x, sh = syn.linear_case(93, 20, 128, 128 * 300, 2)
     y = run_linear(x, sh)
     ref = oracle.linear_f64(x, sh.code, 2, sh.s_in, sh.rin, sh.rout, sh.s_out)

@@ -143,6 +143,13 @@ def test_moe_long_call_runs_in_passes(full_bank):
     ref = oracle.moe_f64(np.ascontiguousarray(x[sample]), np.ascontiguousarray(ids[sample]),
                          np.ascontiguousarray(w[sample]), bank)
     assert_rows_close(got[sample], ref)
+    # every row is written by exactly one pass: the same tokens as two calls of 3967
+    # and 133 tokens on the same workspace give the identical output
+    y1, _ = run_moe(np.ascontiguousarray(x[:3967]), np.ascontiguousarray(ids[:3967]),
+                    np.ascontiguousarray(w[:3967]), bank_d, 128, 2048, 768, ws)
+    y2, _ = run_moe(np.ascontiguousarray(x[3967:]), np.ascontiguousarray(ids[3967:]),
+                    np.ascontiguousarray(w[3967:]), bank_d, 128, 2048, 768, ws)
+    assert np.array_equal(bits(y), np.concatenate([bits(y1), bits(y2)]))
 
 
 def test_moe_deterministic(full_bank):
@@ -182,9 +189,9 @@ def test_moe_zero_tokens_is_a_no_op():
 # ---------------------------------------------------------------- FC1 / FC2 on the fused tensor-core GEMM
 
 @pytest.mark.parametrize("T", (1, 5, 20, 40))
-def test_moe_small_bank_fused_gemm(T, monkeypatch):
+def test_moe_small_bank_fused_gemm(T, pin_gemm_path):
     # rows-mode fused GEMM over the device-built entry lists, mixed K, one to 40 tokens
-    monkeypatch.setenv("EXL3_FORCE_MODE", "fused")
+    pin_gemm_path("fused")
     E, H, I, topk = 6, 256, 128, 3
     bank = syn.moe_bank(11, E=E, H=H, I=I, distinct_down_k=True)
     x, logits = syn.moe_tokens(12 + T, T, H=H, E=E)
@@ -194,8 +201,8 @@ def test_moe_small_bank_fused_gemm(T, monkeypatch):
     assert m.exl3_workspace_error(ws) == 0
 
 
-def test_moe_full_geometry_fused_gemm_16_tokens(full_bank, monkeypatch):
-    monkeypatch.setenv("EXL3_FORCE_MODE", "fused")
+def test_moe_full_geometry_fused_gemm_16_tokens(full_bank, pin_gemm_path):
+    pin_gemm_path("fused")
     bank, bank_d = full_bank
     x, logits = syn.moe_tokens(36, 16)
     ids, w = oracle.topk_softmax(logits, 8)
@@ -204,8 +211,8 @@ def test_moe_full_geometry_fused_gemm_16_tokens(full_bank, monkeypatch):
     assert m.exl3_workspace_error(ws) == 0
 
 
-def test_moe_fused_gemm_deterministic(full_bank, monkeypatch):
-    monkeypatch.setenv("EXL3_FORCE_MODE", "fused")
+def test_moe_fused_gemm_deterministic(full_bank, pin_gemm_path):
+    pin_gemm_path("fused")
     bank, bank_d = full_bank
     x, logits = syn.moe_tokens(42, 300)
     ids, w = oracle.topk_softmax(logits, 8)

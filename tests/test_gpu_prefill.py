@@ -59,13 +59,13 @@ def test_prefill_column_slice_isolation():
 
 
 @pytest.mark.parametrize("K", (2, 3, 4))
-def test_prefill_full_shape_sampled(K):
+def test_prefill_full_shape_every_column_sampled_rows(K):
+    # the benchmarked prefill shape: every output column, on rows in the first and last
+    # 128-row tiles, around a tile boundary and in the middle
     x, sh = syn.prefill(2, M=8192, K=K)
     y = run(x, sh)
     got = as_f64(y)
     assert np.all(np.isfinite(got))
     rows = np.array([0, 1, 127, 128, 4095, 5000, 8190, 8191])
-    for blk in (0, 70, 135):
-        ref = oracle.linear_f64(np.ascontiguousarray(x[rows]), sh.code, K, sh.s_in, sh.rin, sh.rout, sh.s_out,
-                                blk0=blk, nblk=1)
-        assert_rows_close(got[rows, blk * 128:(blk + 1) * 128], ref)
+    ref = oracle.linear_f64(np.ascontiguousarray(x[rows]), sh.code, K, sh.s_in, sh.rin, sh.rout, sh.s_out)
+    assert_rows_close(got[rows], ref)

@@ -74,3 +74,37 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == m.EXL3_EINVAL
     assert b"M <= 8" in m.lib().exl3_last_error()
+
+
+def test_noalloc_allocates_nothing():
+    # after a warm-up call, a further call changes neither the device's free memory
+    # nor what torch's caching allocator holds
+    M, IC, OC, K = 8, 1024, 1024, 2
+    x, sh = syn.linear_case(960, M, IC, OC, K)
+    xd = dev(x, torch.bfloat16)
+    code = dev(sh.code, torch.int16)
+    sc = [dev(v, torch.float16) for v in (sh.s_in, sh.rin, sh.rout, sh.s_out)]
+    out = torch.empty((M, OC), dtype=torch.bfloat16, device="cuda")
+    _call_noalloc(xd, code, K, sc, out, 0)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    reserved0 = torch.cuda.memory_reserved()
+    _call_noalloc(xd, code, K, sc, out, 0)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert torch.cuda.memory_reserved() == reserved0
+
+
+@pytest.mark.parametrize("M,IC,OC,K", [(8, 32640, 8192, 2), (3, 4992, 8192, 3)])
+def test_noalloc_matches_oracle_near_its_limits(M, IC, OC, K):
+    # a wide input (IC near the 32768 limit, not a power of two) and many column
+    # groups, so the split-K partition runs on the fixed slab; compared with the oracle
+    import oracle
+    x, sh = syn.linear_case(970 + K, M, IC, OC, K)
+    out = torch.full((M, OC), NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    _call_noalloc(dev(x, torch.bfloat16), dev(sh.code, torch.int16), K,
+                  [dev(v, torch.float16) for v in (sh.s_in, sh.rin, sh.rout, sh.s_out)], out, 0)
+    torch.cuda.synchronize()
+    ref = oracle.linear_f64(x, sh.code, K, sh.s_in, sh.rin, sh.rout, sh.s_out)
+    assert_rows_close(as_f64(out), ref)
