@@ -80,14 +80,27 @@ static KernelSetup kernel_setup(const void *kernel, int threads, size_t smem) {
     static std::mutex mu;
     static KernelSetup done[256];
     static int n_done = 0;
+    // per (kernel, device): the largest dynamic shared memory opted in so far; the
+    // opt-in only ever grows, so a launch sized earlier keeps fitting
+    static struct { const void *kernel; int dev; size_t smem; } optin[128];
+    static int n_optin = 0;
     int dev = 0;
     cudaGetDevice(&dev);
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < n_done; i++)
         if (done[i].kernel == kernel && done[i].dev == dev && done[i].smem == smem) return done[i];
     KernelSetup k = {kernel, dev, smem, cudaSuccess, 1};
-    if (smem > 48 * 1024)
-        k.err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (smem > 48 * 1024) {
+        int o = 0;
+        while (o < n_optin && !(optin[o].kernel == kernel && optin[o].dev == dev)) o++;
+        if (o == n_optin || optin[o].smem < smem) {
+            k.err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (k.err == cudaSuccess) {
+                if (o == n_optin && n_optin < 128) n_optin++;
+                if (o < 128) optin[o] = {kernel, dev, smem};
+            }
+        }
+    }
     if (k.err == cudaSuccess && threads > 0) {
         k.err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k.occ, kernel, threads, smem);
         if (k.occ < 1) k.occ = 1;

@@ -93,11 +93,27 @@ struct GroupGemmArgs {
     uint32_t pow2[17];            // pow2[o] = 1 << o (multipliers of the state extraction)
     int32_t max_rows;             // rows per entry the launch was sized for
     int32_t parts;                // > 0: CTA c takes part c % parts of group c / parts (set by the launcher)
+    // Rows mode with gathered activations (grouped MoE, one 8-row block per
+    // entry): u holds two halves of R rows each, stored per (token, route) pair;
+    // entry row g (routed row r = e.u_row0 - j R + g of half j) reads row
+    // row_pair[r] of its half.
+    int32_t gather;
+    int32_t R, topk;
+    const int32_t *row_pair;
+    // Combine epilogue (FC2): after writing routed row r, the last of token t's
+    // valid routes to arrive at column group G sums y[t] = sum_k comb_w[t][k] *
+    // out_rows[comb_pos[t][k]] in k order into comb_y (bf16 [T][OC]).
+    int32_t comb;
+    const float *comb_w;
+    const int32_t *comb_pos;
+    uint16_t *comb_y;
+    int32_t *comb_counters;       // [T][OC / 128], zero between calls
 };
 constexpr int kMaxInlineEntries = 4;
 
 // Launch the grouped decode-mode GEMM; `max_groups` bounds the total number of
-// column groups (for the partial slab), rows per entry <= 8 * nb.
+// column groups (for the partial slab), rows per entry <= 8 * nb.  A launch with
+// gathered activations (a.gather) needs nb == 1.
 cudaError_t launch_group_gemm(const GroupGemmArgs &a, int nb, bool pdl, cudaStream_t s);
 size_t group_slab_floats(int max_groups, int nb);
 

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "decode.cuh"
 #include "internal.h"
 
 namespace exl3 {
@@ -194,145 +195,15 @@ cudaError_t launch_codebook_table(uint16_t *table, cudaStream_t s) {
 // + block counter).
 // --------------------------------------------------------------------------
 
-// Fragment-order index of (row n, group-local column oc).
-template <int NB>
-__device__ __forceinline__ int frag_index(int n, int oc) {
-    const int g = oc >> 4, j = (oc & 15) >> 1, rrow = oc & 1;
-    const int nb = n >> 3, q = (n & 7) >> 1, c = n & 1;
-    return ((j * NB + nb) * 4 + (2 * rrow + c)) * 32 + (4 * g + q);
-}
-
-// CTAs per SM the register budget is sized for.  NB = 1 runs two CTAs (16 warps)
-// of up to 128 registers: measured faster than three CTAs at 80 registers (the
-// extra registers buy prefetch depth and instruction-level parallelism).
-template <int NB>
-struct DecodeOcc { static constexpr int value = NB <= 2 ? 2 : 1; };
-
-template <int NB>
-constexpr size_t group_smem_bytes() {
-    return sizeof(float) * kDecodeWarps * 8 * NB * 4 * 32 + sizeof(GroupEntry) + 16;
-}
-
-// Accumulate tile rows [a_lo, a_hi) of one column group into acc (one warp,
-// rows a_lo + warp, a_lo + warp + 8, ...).
-template <int K, int NB>
-__device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const GroupEntry &e, const uint16_t *u,
-                                                 int IC, int G, int a_lo, int a_hi, int lane, int warp,
-                                                 uint32_t hx, const uint32_t *pow2) {
-    const int g = lane >> 2, q = lane & 3;
-    const int TO = e.OC / kTile;
-    const uint32_t *tile0 = reinterpret_cast<const uint32_t *>(e.code) + (int64_t)(8 * G + g) * 8 * K + q * 2 * K;
-    const int64_t row_words = (int64_t)TO * 8 * K;   // uint32 words per tile row
-    const uint16_t *ub = u + (int64_t)e.u_row0 * IC;
-    // activations of row 8nb+g, channels 16a + 4q .. +3 (zeros past the entry's rows)
-    auto load_u = [&](uint2 (&v)[NB], int ar) {
-#pragma unroll
-        for (int nb = 0; nb < NB; nb++) {
-            v[nb] = make_uint2(0u, 0u);
-            if (8 * nb + g < e.nrows && ar < a_hi)
-                v[nb] = __ldg(reinterpret_cast<const uint2 *>(ub + (int64_t)(8 * nb + g) * IC + 16 * ar + 4 * q));
-        }
-    };
-    // this row's activations, each duplicated into a half2
-    auto dup_u = [&](uint32_t (&b)[NB][4], const uint2 (&v)[NB]) {
-#pragma unroll
-        for (int nb = 0; nb < NB; nb++) {
-            b[nb][0] = dup_half_lo(v[nb].x);
-            b[nb][1] = dup_half_hi(v[nb].x);
-            b[nb][2] = dup_half_lo(v[nb].y);
-            b[nb][3] = dup_half_hi(v[nb].y);
-        }
-    };
-    // the 64 weights of this lane's quarter: hash, then MMAs against the activations
-    auto mma_row = [&](const QuarterStream<K> &st, const uint32_t (&b)[NB][4]) {
-#pragma unroll
-        for (int rp = 0; rp < 2; rp++) {
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const int i0 = 32 * rp + 2 * j;
-                const uint32_t z0 = trellis_hash_x(st.state(i0, pow2), hx);
-                const uint32_t z1 = trellis_hash_x(st.state(i0 + 1, pow2), hx);
-                const uint32_t z2 = trellis_hash_x(st.state(i0 + 16, pow2), hx);
-                const uint32_t z3 = trellis_hash_x(st.state(i0 + 17, pow2), hx);
-#pragma unroll
-                for (int nb = 0; nb < NB; nb++)
-                    mma_16816(acc[j][nb], z0, z1, z2, z3, b[nb][2 * rp], b[nb][2 * rp + 1]);
-            }
-        }
-    };
-    int ar = a_lo + warp;
-    uint2 un[NB];
-    if constexpr (NB == 1) {
-        // two tile-row buffers used in turn, each refilled with the row two steps
-        // ahead as soon as its words are realigned (no register copies); the code
-        // and activation pointers advance by increments only
-        if (ar >= a_hi) return;
-        const int n = (a_hi - ar + kDecodeWarps - 1) / kDecodeWarps;
-        const int64_t stride = row_words * kDecodeWarps;
-        const uint32_t *p = tile0 + ar * row_words;
-        const bool urow = g < e.nrows;
-        const uint16_t *up = ub + (int64_t)g * IC + 16 * ar + 4 * q;
-        constexpr int kUS = 16 * kDecodeWarps;   // activation step (channels) per warp step
-        uint32_t wa[2 * K], wb[2 * K];
-        uint2 ua = make_uint2(0u, 0u), ubv = make_uint2(0u, 0u);
-        load_quarter<K>(wa, p);
-        if (urow) ua = __ldg(reinterpret_cast<const uint2 *>(up));
-        if (n > 1) {
-            load_quarter<K>(wb, p + stride);
-            if (urow) ubv = __ldg(reinterpret_cast<const uint2 *>(up + kUS));
-        }
-        auto row = [&](uint32_t (&w)[2 * K], uint2 &uv, bool refill, const uint32_t *pn, const uint16_t *upn) {
-            QuarterStream<K> st;
-            st.build(w, quarter_prev_word(w[2 * K - 1], lane));
-            uint32_t b[NB][4] = {{dup_half_lo(uv.x), dup_half_hi(uv.x), dup_half_lo(uv.y), dup_half_hi(uv.y)}};
-            if (refill) {
-                load_quarter<K>(w, pn);
-                if (urow) uv = __ldg(reinterpret_cast<const uint2 *>(upn));
-            }
-            mma_row(st, b);
-        };
-        for (int i = 0; i < n; i += 2) {
-            row(wa, ua, i + 2 < n, p + 2 * stride, up + 2 * kUS);
-            if (i + 1 >= n) break;
-            row(wb, ubv, i + 3 < n, p + 3 * stride, up + 3 * kUS);
-            p += 2 * stride;
-            up += 2 * kUS;
-        }
-    } else {
-        // one rotating prefetch queue (fewer live registers with more rows)
-        constexpr int PF = 2;   // tile rows of code words in flight per warp
-        uint32_t wq[PF][2 * K];
-#pragma unroll
-        for (int d = 0; d < PF; d++)
-            if (ar + d * kDecodeWarps < a_hi) load_quarter<K>(wq[d], tile0 + (ar + d * kDecodeWarps) * row_words);
-        load_u(un, ar);
-        for (; ar < a_hi; ar += kDecodeWarps) {
-            uint32_t w[2 * K];
-#pragma unroll
-            for (int i = 0; i < 2 * K; i++) w[i] = wq[0][i];
-#pragma unroll
-            for (int d = 0; d + 1 < PF; d++)
-#pragma unroll
-                for (int i = 0; i < 2 * K; i++) wq[d][i] = wq[d + 1][i];
-            if (ar + PF * kDecodeWarps < a_hi) load_quarter<K>(wq[PF - 1], tile0 + (ar + PF * kDecodeWarps) * row_words);
-            uint32_t b[NB][4];
-            dup_u(b, un);
-            load_u(un, ar + kDecodeWarps);
-            QuarterStream<K> st;
-            st.build(w, quarter_prev_word(w[2 * K - 1], lane));
-            mma_row(st, b);
-        }
-    }
-}
-
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // KSET: bit k set = the launch may contain entries of bitrate k (2, 3, 4); only
 // those decode paths are compiled into the kernel, which keeps registers low.
-template <int NB, int KSET>
+template <int NB, int KSET, bool GATHER = false>
 __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(const GroupGemmArgs a) {
+    static_assert(!GATHER || NB == 1, "gathered activation rows serve one 8-row block per entry");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     constexpr int FRAG = 8 * NB * 4 * 32;
     float *red = reinterpret_cast<float *>(smem_raw);                   // [warps][FRAG]
@@ -404,9 +275,18 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
             for (int nb = 0; nb < NB; nb++)
 #pragma unroll
                 for (int r = 0; r < 4; r++) acc[j][nb][r] = 0.f;
-        if ((KSET & 4) && e.K == 2) group_accumulate<2, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2);
-        if ((KSET & 8) && e.K == 3) group_accumulate<3, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2);
-        if ((KSET & 16) && e.K == 4) group_accumulate<4, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2);
+        if constexpr (GATHER) {
+            if ((KSET & 4) && e.K == 2)
+                group_accumulate<2, NB, kUGather>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+            if ((KSET & 8) && e.K == 3)
+                group_accumulate<3, NB, kUGather>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+            if ((KSET & 16) && e.K == 4)
+                group_accumulate<4, NB, kUGather>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+        } else {
+            if ((KSET & 4) && e.K == 2) group_accumulate<2, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2);
+            if ((KSET & 8) && e.K == 3) group_accumulate<3, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2);
+            if ((KSET & 16) && e.K == 4) group_accumulate<4, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2);
+        }
 
         // ---- CTA reduction in fixed warp order (fragment order, one barrier)
 #pragma unroll
@@ -498,6 +378,39 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
                 } else {
                     *reinterpret_cast<float4 *>(a.out_rows + (e.out_off + n) * (int64_t)e.OC + oc0) =
                         make_float4(y[0], y[1], y[2], y[3]);
+                    if (a.comb) {
+                        // routed row r = token t's route: the last of t's valid routes to
+                        // arrive at this column group sums them in route order into y[t]
+                        __threadfence();
+                        __syncwarp();
+                        const int t = a.row_pair[e.out_off + n] / a.topk;
+                        const int GH = e.OC / kHad;
+                        int last = 0;
+                        if (lane == 0) {
+                            int nv = 0;
+                            for (int k = 0; k < a.topk; k++) nv += a.comb_pos[(int64_t)t * a.topk + k] >= 0;
+                            last = atomicAdd(a.comb_counters + (int64_t)t * GH + G, 1) == nv - 1;
+                        }
+                        last = __shfl_sync(kFull, last, 0);
+                        if (last) {
+                            __threadfence();
+                            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                            for (int k = 0; k < a.topk; k++) {
+                                const int rk = a.comb_pos[(int64_t)t * a.topk + k];
+                                if (rk < 0) continue;
+                                const float wk = a.comb_w[(int64_t)t * a.topk + k];
+                                const float4 d = __ldcg(reinterpret_cast<const float4 *>(a.out_rows + (int64_t)rk * e.OC + oc0));
+                                sum[0] += wk * d.x;
+                                sum[1] += wk * d.y;
+                                sum[2] += wk * d.z;
+                                sum[3] += wk * d.w;
+                            }
+                            const uint32_t o0 = (uint32_t)f32_to_bf16_bits(sum[0]) | ((uint32_t)f32_to_bf16_bits(sum[1]) << 16);
+                            const uint32_t o1 = (uint32_t)f32_to_bf16_bits(sum[2]) | ((uint32_t)f32_to_bf16_bits(sum[3]) << 16);
+                            *reinterpret_cast<uint2 *>(a.comb_y + (int64_t)t * e.OC + oc0) = make_uint2(o0, o1);
+                            if (lane == 0) a.comb_counters[(int64_t)t * GH + G] = 0;
+                        }
+                    }
                 }
             }
         }
@@ -506,11 +419,11 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
     }
 }
 
-template <int NB, int KSET>
+template <int NB, int KSET, bool GATHER = false>
 static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t total_hint, cudaStream_t s) {
     constexpr size_t smem = group_smem_bytes<NB>();
     int occ = 1;
-    cudaError_t e = kernel_occupancy((const void *)group_gemm_kernel<NB, KSET>, 256, smem, &occ);
+    cudaError_t e = kernel_occupancy((const void *)group_gemm_kernel<NB, KSET, GATHER>, 256, smem, &occ);
     if (e != cudaSuccess) return e;
     GroupGemmArgs a = a0;
     a.hash_xor = kHashXor;
@@ -541,7 +454,7 @@ static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t tot
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, group_gemm_kernel<NB, KSET>, a);
+    return cudaLaunchKernelEx(&cfg, group_gemm_kernel<NB, KSET, GATHER>, a);
 }
 
 template <int NB>
@@ -571,6 +484,11 @@ cudaError_t launch_group_gemm(const GroupGemmArgs &a, int nb, bool pdl, cudaStre
             kset |= 1 << a.inline_e[i].K;
         }
         total = groups * (a.IC / kTile);
+    }
+    if (a.gather) {
+        // grouped MoE with activation rows stored per pair: one 8-row block per entry, any K
+        if (nb != 1) return cudaErrorInvalidValue;
+        return launch_group_t<1, 28, true>(a, pdl, total, s);
     }
     if (nb == 3) nb = 4;
     switch (nb) {

@@ -4,13 +4,17 @@
 // Launch chain, all on the caller's stream, no host synchronization:
 //   route     ids -> expert-sorted rows (stable counting sort), per-row slot,
 //             per-pair row position, and the grouped-GEMM entry lists
-//   rotate    u1[r] = Had(x_t * w13_suh[p][0]), u3[r] = Had(x_t * w13_suh[p][1])
+//   rotate    u1 = Had(x_t * w13_suh[p][0]), u3 = Had(x_t * w13_suh[p][1]) per
+//             routed row, or (one 8-row block per entry) per (token, route) pair
+//             in the same launch as the routing
 //   FC1       grouped trellis GEMM over (slot, row block) x {w1, w3}, epilogue
 //             Had(v) * w13_svh -> fp32 rows
 //   act       h = silu(g) * u, then FC2's input transform Had(h * w2_suh[p])
 //   FC2       grouped trellis GEMM over (slot, row block), epilogue
-//             Had(v) * w2_svh -> fp32 rows
-//   combine   y_t = sum over k (in order) of w[t][k] * d[pos(t,k)] -> bf16
+//             Had(v) * w2_svh -> fp32 rows; with one 8-row block per entry the
+//             epilogue also combines (below)
+//   combine   y_t = sum over k (in order) of w[t][k] * d[pos(t,k)] -> bf16: the
+//             last of a token's routes to finish a column group sums them
 #include <cuda_runtime.h>
 
 #include "../../include/exl3.h"
@@ -32,6 +36,10 @@ namespace {
 
 constexpr int kMoeMaxE = 1024;
 constexpr int kMoeMaxTopk = 32;
+// The three-kernel chain's combine counters (one per token and column group of
+// y) sit in the upper half of the workspace counters; the grouped GEMMs' split-K
+// counters use the lower half.
+constexpr int64_t kCombCounterBase = 32768;
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -105,6 +113,8 @@ MoeLayout moe_layout(int T, int H, int I, int E, int topk) {
 // id); then softmax over the selected logits.
 __global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restrict__ logits, int T, int E, int topk,
                                                            int32_t *__restrict__ ids, float *__restrict__ w) {
+    // the routing kernel that follows may be scheduled now; it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -156,6 +166,7 @@ struct RouteArgs {
     int32_t *pos, *row_pair, *row_slot, *counts;
     GroupEntry *ent1, *ent2;
     int32_t *err;
+    uint16_t *y_zero;   // non-null: write zero rows y[t] for tokens with no valid route
 };
 
 constexpr int kRouteParE = 128;   // slots up to which the stable ranking runs on all warps at once
@@ -169,7 +180,7 @@ constexpr int kRouteRegPairs = 8; // pairs per lane that the ranking keeps in re
 // 32 * kRouteRegPairs pairs (fast path), its lanes keep the pairs' slots in
 // registers from the count to the ranking, read the expert tables from shared
 // memory, and write each row's pair and slot as soon as the row is known.
-__global__ void __launch_bounds__(1024) route_kernel(const RouteArgs a) {
+__device__ __forceinline__ void route_body(const RouteArgs &a) {
     __shared__ int cnt[kMoeMaxE], base[kMoeMaxE], ebase[kMoeMaxE], cursor[kMoeMaxE];
     __shared__ int wcur[32][kRouteParE];     // per warp and slot: pairs in the chunk, then its cursor
     __shared__ int s_perm[kRouteParE], s_kgu[kRouteParE], s_kd[kRouteParE];
@@ -372,6 +383,79 @@ __global__ void __launch_bounds__(1024) route_kernel(const RouteArgs a) {
             a.ent2[idx] = ge;
         }
     }
+    if (a.y_zero) {
+        // tokens whose routes are all invalid get y = 0 (no combine reaches them)
+        __syncthreads();
+        const int T = a.R / a.topk;
+        for (int t = tid; t < T; t += blockDim.x) {
+            bool any = false;
+            for (int k = 0; k < a.topk; k++) any |= a.pos[(int64_t)t * a.topk + k] >= 0;
+            if (!any)
+                for (int c = 0; c < a.H; c += 8)
+                    *reinterpret_cast<uint4 *>(a.y_zero + (int64_t)t * a.H + c) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(1024) route_kernel(const RouteArgs a) { route_body(a); }
+
+// Input rotation per (token, route) pair, before the rows are known:
+// u[j][i] = Had(x_t * w13_suh[p][j]) for pair i = t * topk + k routed to slot p
+// (pairs whose expert id, slot or bitrate is invalid are skipped; the routing
+// records them).
+struct PairRotateArgs {
+    const uint16_t *x;
+    const int32_t *ids;
+    int R, topk, E, H;
+    exl3_moe_bank bank;
+    uint16_t *u;   // fp16 [2][R][H]
+};
+
+__device__ __forceinline__ void rotate_pairs(const PairRotateArgs &a, int wid, int nwarps, int lane) {
+    const int blocks = a.H / kHad;
+    for (int task = wid; task < a.R * blocks; task += nwarps) {
+        const int i = task / blocks, c = (task - i * blocks) * kHad + 4 * lane;
+        const int e = a.ids[i];
+        if (e < 0 || e >= a.E) continue;
+        const int p = a.bank.perm[e];
+        if (p < 0 || p >= a.E) continue;
+        const int kg = a.bank.k_gu[p], kd = a.bank.k_d[p];
+        if (kg < 2 || kg > 4 || kd < 2 || kd > 4) continue;
+        const int t = i / a.topk;
+        const uint2 xv = *reinterpret_cast<const uint2 *>(a.x + (int64_t)t * a.H + c);
+        uint2 sv[2];
+#pragma unroll
+        for (int j = 0; j < 2; j++) sv[j] = __ldg(reinterpret_cast<const uint2 *>(a.bank.w13_suh + ((int64_t)p * 2 + j) * a.H + c));
+        const uint32_t xs[2] = {xv.x, xv.y};
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const uint32_t ss[2] = {sv[j].x, sv[j].y};
+            float v[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+                v[k] = bf16_bits_to_f32((xs[k >> 1] >> (16 * (k & 1))) & 0xFFFFu) *
+                       f16_bits_to_f32((uint16_t)(ss[k >> 1] >> (16 * (k & 1))));
+            warp_fwht128(v, lane);
+            uint2 o;
+            o.x = (uint32_t)f32_to_f16_bits(v[0] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[1] * kHadNorm) << 16);
+            o.y = (uint32_t)f32_to_f16_bits(v[2] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[3] * kHadNorm) << 16);
+            *reinterpret_cast<uint2 *>(a.u + ((int64_t)j * a.R + i) * a.H + c) = o;
+        }
+    }
+}
+
+// The first kernel of the three-GEMM-launch chain: CTA 0 routes, the others
+// rotate the pairs' inputs meanwhile (both read only the ids).
+__global__ void __launch_bounds__(1024) route_rotate_kernel(const RouteArgs a, const PairRotateArgs r) {
+    // launched as a dependent of the router: wait for its ids; let FC1 be scheduled
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (blockIdx.x == 0) {
+        route_body(a);
+        return;
+    }
+    rotate_pairs(r, (blockIdx.x - 1) * (blockDim.x >> 5) + (threadIdx.x >> 5), (gridDim.x - 1) * (blockDim.x >> 5),
+                 threadIdx.x & 31);
 }
 
 // ------------------------------------------------------------------ rotate
@@ -442,6 +526,8 @@ __global__ void __launch_bounds__(256) act_kernel(const float *__restrict__ st1,
                                                   const int32_t *__restrict__ counts,
                                                   uint16_t *__restrict__ h2) {
     asm volatile("griddepcontrol.launch_dependents;");
+    // may be launched as a dependent of FC1: wait for its rows
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);   // R * I / 128 < 2^31
     const int blocks = I / kHad;
@@ -586,10 +672,83 @@ exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
     cudaStream_t s = (cudaStream_t)stream;
     const int R = L.R;
 
-    RouteArgs ra = {ids, R, topk, E, H, I, L.chunk, b, pos, row_pair, row_slot, counts, ent1, ent2, err};
+    // One 8-row block per entry: four launches (route with the per-pair input
+    // rotation alongside, FC1 on the pairs' rows, the activation, FC2 with the
+    // weighted combine in its epilogue), chained as programmatic dependents.
+    // Otherwise the separate passes below.
+    const int GH = H / kHad;
+    const bool chain = !L.fused && L.nb == 1 &&
+                       (int64_t)L.max_entries * (2 * (I / kHad) > GH ? 2 * (I / kHad) : GH) <= kCombCounterBase &&
+                       (int64_t)T * GH <= (int64_t)kWorkspaceCounters - kCombCounterBase;
+    RouteArgs ra = {ids, R, topk, E, H, I, L.chunk, b, pos, row_pair, row_slot, counts, ent1, ent2, err,
+                    chain ? y : nullptr};
+    cudaError_t e;
+    cudaLaunchAttribute pdl_attr[1];
+    pdl_attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl_attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (chain) {
+        PairRotateArgs pr = {x, ids, R, topk, E, H, b, u13};
+        const int64_t tasks = (int64_t)R * (H / kHad);
+        const int64_t rot_ctas = (tasks + 31) / 32 < 4 * (int64_t)device_info().sm_count ? (tasks + 31) / 32
+                                                                                          : 4 * (int64_t)device_info().sm_count;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(1 + rot_ctas));
+        cfg.blockDim = dim3(1024);
+        cfg.stream = s;
+        cfg.attrs = pdl_attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, route_rotate_kernel, ra, pr)) != cudaSuccess)
+            return cuda_fail(e, "moe_grouped: route");
+        GroupGemmArgs g1 = {};
+        g1.u = u13;
+        g1.IC = H;
+        g1.mode = kModeRows;
+        g1.entries = ent1;
+        g1.n_entries_dev = counts + 1;
+        g1.n_groups_per_entry = I / kHad;
+        g1.out_rows = st1;
+        g1.partials = slab;
+        g1.counters = counters;
+        g1.gather = 1;
+        g1.R = R;
+        g1.topk = topk;
+        g1.row_pair = row_pair;
+        if ((e = launch_group_gemm(g1, 1, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC1");
+        {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(warp_grid((int64_t)R * (I / kHad)));
+            cfg.blockDim = dim3(256);
+            cfg.stream = s;
+            cfg.attrs = pdl_attr;
+            cfg.numAttrs = 1;
+            if ((e = cudaLaunchKernelEx(&cfg, act_kernel, (const float *)st1, I, R, b.w2_suh, (const int32_t *)row_slot,
+                                        (const int32_t *)counts, h2)) != cudaSuccess)
+                return cuda_fail(e, "moe_grouped: act");
+        }
+        GroupGemmArgs g2 = {};
+        g2.u = h2;
+        g2.IC = I;
+        g2.mode = kModeRows;
+        g2.entries = ent2;
+        g2.n_entries_dev = counts + 2;
+        g2.n_groups_per_entry = GH;
+        g2.out_rows = st2;
+        g2.partials = slab;
+        g2.counters = counters;
+        g2.R = R;
+        g2.topk = topk;
+        g2.row_pair = row_pair;
+        g2.comb = 1;
+        g2.comb_w = w;
+        g2.comb_pos = pos;
+        g2.comb_y = y;
+        g2.comb_counters = counters + kCombCounterBase;
+        if ((e = launch_group_gemm(g2, 1, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC2");
+        trace("moe_grouped T=%d H=%d I=%d E=%d topk=%d rows<=%d gemm=decode (4 launches)", T, H, I, E, topk, R);
+        return EXL3_OK;
+    }
     route_kernel<<<1, 1024, 0, s>>>(ra);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "moe_grouped: route");
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "moe_grouped: route");
 
     // warps per row: enough warps to fill the GPU when few rows are routed, whole rows otherwise
     int parts = 1;
