@@ -1,4 +1,4 @@
-"""CPU oracle for the EXL3 trellis linear, MoE and int8-gather path.
+"""CPU oracle for the EXL3 trellis linear, MoE, int8 gather and int8 output head.
 
 TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg call this module; the product package never
@@ -77,6 +77,9 @@ def lib():
                                             _P(u16), _P(u16), _P(u16), ctypes.c_long,
                                             ctypes.c_long]
             L.exl3o_linear_into.restype = ctypes.c_int
+            L.exl3o_lm_head_f64.argtypes = [_P(u16), ctypes.c_long, ctypes.c_int, _P(i8), _P(u16), ctypes.c_long,
+                                            ctypes.c_long, ctypes.c_long, _P(f64)]
+            L.exl3o_lm_head_f64.restype = ctypes.c_int
             L.exl3o_topk_softmax.argtypes = [_P(f32), ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              _P(i32), _P(f32)]
             L.exl3o_topk_softmax.restype = ctypes.c_int
@@ -277,3 +280,19 @@ def gather(q: np.ndarray, s, ids: np.ndarray):
                               _ptr(ids, ctypes.c_int32), N, _ptr(out, ctypes.c_uint16),
                               ctypes.byref(bad)), "gather")
     return out, int(bad.value)
+
+
+# ---------------------------------------------------------------- int8 output head
+def lm_head_f64(x, q: np.ndarray, s, v0: int = 0, nv: int | None = None) -> np.ndarray:
+    """fp64 y[M][nv] = s[v] * sum_h x[m][h] * q[v][h] for vocabulary rows [v0, v0 + nv) (unrounded)."""
+    x = _u16(x)
+    q = np.ascontiguousarray(q, np.int8)
+    s = _u16(s)
+    M, H = x.shape
+    V = q.shape[0]
+    assert q.shape[1] == H
+    nv = V - v0 if nv is None else nv
+    y = np.empty((M, nv), np.float64)
+    _check(lib().exl3o_lm_head_f64(_ptr(x, ctypes.c_uint16), M, H, _ptr(q, ctypes.c_int8),
+                                   _ptr(s, ctypes.c_uint16), V, v0, nv, _ptr(y, ctypes.c_double)), "lm_head")
+    return y

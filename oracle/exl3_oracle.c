@@ -546,3 +546,31 @@ int exl3o_gather(const int8_t *q, const uint16_t *s, long V, int H,
         *n_bad = bad;
     return EXL3O_OK;
 }
+
+/* ------------------------------------------------------------------ int8 output head
+ * The int8 table used as the output projection (vllm-quantpack exl3/embedding.py,
+ * Exl3EmbeddingMethod.apply: the linear layer's weight is the int8 table times its
+ * per-row scale, w[v][h] = q[v][h] * s[v], and the head computes x @ w^T).
+ * Reading: the per-row scale is factored out of the sum and the product is rounded
+ * once, as the gather above does:
+ *     y[m][v] = s[v] * sum_h x[m][h] * q[v][h]       (fp64, unrounded)
+ * for vocabulary rows v in [v0, v0 + nv); y is [M][nv].  x is bf16 [M][H], q int8
+ * [V][H] row-major, s fp16 [V].
+ */
+int exl3o_lm_head_f64(const uint16_t *x, long M, int H, const int8_t *q, const uint16_t *s, long V,
+                      long v0, long nv, double *y)
+{
+    if (M < 0 || H <= 0 || V <= 0 || v0 < 0 || nv < 0 || v0 + nv > V)
+        return EXL3O_EINVAL;
+#pragma omp parallel for schedule(static)
+    for (long v = v0; v < v0 + nv; v++) {
+        const double sc = exl3o_f16_to_f64(s[v]);
+        for (long m = 0; m < M; m++) {
+            double acc = 0.0;
+            for (int h = 0; h < H; h++)
+                acc += exl3o_bf16_to_f64(x[m * H + h]) * (double)q[v * H + h];
+            y[m * nv + (v - v0)] = sc * acc;
+        }
+    }
+    return EXL3O_OK;
+}
