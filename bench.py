@@ -9,7 +9,8 @@ trellis GEMM, output transform into the slices).  Metric: tokens/s.
 Other workloads (--workload): prefill (5120 -> 17408 at M = 8192, K per
 --k), moe (128 experts, H 2048, I 768, top-8, T tokens per --t), gather
 (8192 ids from a 248,320 x 5120 int8 table), layer (the five projections of a
-hidden-5120 decoder layer at --m rows).
+hidden-5120 decoder layer at --m rows), lm_head (that int8 table as the output
+projection at --m rows).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload W] [--impl ours|reference]
 
@@ -551,7 +552,70 @@ class Layer:
         return self.M / t, "2 output blocks of each projection (<= 8 rows), scaled to all blocks and rows"
 
 
-WORKLOADS = {"gate_up": GateUp, "prefill": Prefill, "moe": Moe, "gather": Gather, "layer": Layer}
+class LmHead:
+    """int8 output head: the 248,320 x 5120 int8 table (fp16 row scale) as the output projection."""
+    V, H = 248320, 5120
+
+    def __init__(self, args):
+        self.M = args.m
+        self.metric = f"int8 output head tokens/s (M={self.M}, 248320 x 5120)"
+        self.unit = "tokens/s"
+        self.units_per_step = self.M
+
+    def config(self):
+        return {"workload": f"lm_head int8 [248320, 5120] + fp16 row scale, M={self.M} -> bf16 logits", "M": self.M}
+
+    def setup(self, torch, m, syn, dev):
+        q, s, _ = syn.embedding(5)
+        self.q = t16(torch, q, dev, torch.int8)
+        self.s = t16(torch, s, dev, torch.float16)
+        self.R = R = 4
+        g = syn.rng(78)
+        self.xnp = [syn.normal_bf16(g, self.M, self.H) for _ in range(R)]
+        self.xs = [t16(torch, x, dev, torch.bfloat16) for x in self.xnp]
+        self.out = torch.empty((self.M, self.V), dtype=torch.bfloat16, device=dev)
+        self.ws = m.workspace(m.exl3_lm_head_workspace_bytes(self.M, self.H, self.V), dev)
+        self.m = m
+        self.l2 = "table 1.27 GB >> L2"
+        self.launches_per_step = 1 if self.M <= 32 else 1 + 2 * -(-self.V // 16384)
+
+    def step(self, r, x=None):
+        self.m.exl3_lm_head_int8(self.xs[r] if x is None else x, self.q, self.s, self.ws, out=self.out)
+
+    def roofline(self, torch, stream):
+        ms = kernel_time_ms(torch, stream, lambda j: self.step(j % self.R), 4 * self.R)
+        hbm, tf, src = peaks()
+        if self.M <= 32:
+            alg = self.V * self.H + 2 * self.V + 2 * self.M * self.H + 2 * self.M * self.V
+            a = alg / (ms * 1e-3) / 1e9
+            return {"bound": "hbm", "kernel": "lm_head_decode_kernel (int8 table streamed, mma.sync)",
+                    "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
+                    "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)", "traffic": None,
+                    "per_launch_us": round(ms * 1e3, 2), "algorithmic_bytes_per_launch": alg}
+        fl = 2.0 * self.M * self.H * self.V
+        a = fl / (ms * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": "int8->fp16 chunks + prefill_gemm_kernel (row-scale epilogue)",
+                "achieved": round(a, 1), "peak": tf, "unit": "TFLOP/s", "frac": round(a / tf, 4),
+                "peak_source": src, "traffic": None, "per_call_us": round(ms * 1e3, 1)}
+
+    def e2e_io(self, torch, dev):
+        xh = torch.from_numpy(self.xnp[0].view(np.int16)).view(torch.bfloat16).pin_memory()
+        oh = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        return xh, torch.empty_like(self.xs[0]), oh, self.out
+
+    def cpu_sample(self, budget):
+        import oracle
+        import synthetic as syn
+        q, s, _ = syn.embedding(5)
+        x = self.xnp[0]
+        nv = 2048
+        t0 = time.perf_counter()
+        oracle.lm_head_f64(x, q, s, v0=0, nv=nv)
+        t = (time.perf_counter() - t0) * self.V / nv
+        return self.M / t, f"vocabulary rows 0..{nv - 1} of {self.V}, scaled linearly to the whole table"
+
+
+WORKLOADS = {"gate_up": GateUp, "prefill": Prefill, "moe": Moe, "gather": Gather, "layer": Layer, "lm_head": LmHead}
 
 
 # ------------------------------------------------------------------ our arm
@@ -613,7 +677,7 @@ def secondary_workloads():
     ns = argparse.Namespace
     return [("gate_up", ns(m=1)), ("gate_up", ns(m=64)), ("prefill", ns(m=8192, k=2)),
             ("moe", ns(t=1)), ("moe", ns(t=16)), ("moe", ns(t=512)), ("gather", ns()),
-            ("layer", ns(m=8)), ("layer", ns(m=8192))]
+            ("layer", ns(m=8)), ("layer", ns(m=8192)), ("lm_head", ns(m=1)), ("lm_head", ns(m=8))]
 
 
 def run_secondary(torch, m, syn, dev, stream, local, K, W, min_seconds):

@@ -341,6 +341,32 @@ exl3_status exl3_embed_int8_gather(const int8_t *q, const uint16_t *scale, int64
                                    int32_t H, const int32_t *ids, int64_t N,
                                    uint16_t *out, int32_t *n_bad, exl3_stream stream);
 
+/* ------------------------------------------------------------ output head */
+
+/*
+ * The int8 table as the output projection (vllm-quantpack exl3/embedding.py,
+ * Exl3EmbeddingMethod.apply: the weight is the int8 table times its per-row
+ * scale, and the head computes x @ weight^T):
+ *     out[m][v] = bf16( scale[v] * sum_h x[m][h] * q[v][h] )
+ * with the row scale taken out of the sum and one rounding of the result.
+ *   x      bf16 [M][H], 16-byte aligned; its values are multiplied as fp16 (exact
+ *          for magnitudes in fp16's normal range, 2^-14 .. 65504)
+ *   q      int8 [V][H] row-major (the embedding table's layout), 16-byte aligned
+ *   scale  fp16 [V]
+ *   out    bf16 [M][ldo], columns [0, V) written, ldo >= V
+ *   ws     exl3_lm_head_workspace_bytes(M, H, V) bytes, prepared by
+ *          exl3_workspace_init (counters that return to zero after each call)
+ * Requires H a multiple of 256.  Up to 32 rows stream the table once through
+ * registers (HBM-bound); more rows run on the tensor cores over table chunks
+ * converted to fp16 in the workspace.
+ */
+size_t exl3_lm_head_workspace_bytes(int64_t max_M, int32_t H, int64_t V);
+
+exl3_status exl3_lm_head_int8(const uint16_t *x, int64_t M, int32_t H,
+                              const int8_t *q, const uint16_t *scale, int64_t V,
+                              uint16_t *out, int64_t ldo,
+                              void *ws, size_t ws_bytes, exl3_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,7 +27,8 @@ EXPORTS = ("exl3_last_error", "exl3_version", "exl3_linear_workspace_bytes", "ex
            "exl3_workspace_error", "exl3_set_gemm_path", "exl3_linear_into", "exl3_linear", "exl3_gemm_into", "exl3_linear_into_noalloc",
            "exl3_linear_shards_workspace_bytes", "exl3_linear_into_shards", "exl3_gemm_into_shards", "exl3_pretransform",
            "exl3_reconstruct", "exl3_codebook_table", "exl3_moe_topk_softmax",
-           "exl3_moe_workspace_bytes", "exl3_moe_grouped", "exl3_embed_int8_gather")
+           "exl3_moe_workspace_bytes", "exl3_moe_grouped", "exl3_embed_int8_gather",
+           "exl3_lm_head_workspace_bytes", "exl3_lm_head_int8")
 
 
 class Exl3Error(RuntimeError):
@@ -91,6 +92,8 @@ def lib() -> ctypes.CDLL:
                 "exl3_moe_grouped": ([vp, i32, i32, i32, i32, i32, vp, vp, ctypes.POINTER(MoeBank), vp,
                                       vp, sz, vp], ctypes.c_int),
                 "exl3_embed_int8_gather": ([vp, vp, i64, i32, vp, i64, vp, vp, vp], ctypes.c_int),
+                "exl3_lm_head_workspace_bytes": ([i64, i32, i64], sz),
+                "exl3_lm_head_int8": ([vp, i64, i32, vp, vp, i64, vp, i64, vp, sz, vp], ctypes.c_int),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -358,4 +361,25 @@ def exl3_embed_int8_gather(q: torch.Tensor, scale: torch.Tensor, ids: torch.Tens
                                         _ptr(out, torch.bfloat16, "out"),
                                         _ptr(n_bad, torch.int32, "n_bad"), _stream(q.device)),
            "exl3_embed_int8_gather")
+    return out
+
+
+# ---------------------------------------------------------------- output head
+def exl3_lm_head_workspace_bytes(max_M: int, H: int, V: int) -> int:
+    return int(lib().exl3_lm_head_workspace_bytes(max_M, H, V))
+
+
+def exl3_lm_head_int8(x: torch.Tensor, q: torch.Tensor, scale: torch.Tensor, ws: torch.Tensor,
+                      out=None) -> torch.Tensor:
+    """out[m][v] = bf16(scale[v] * sum_h x[m][h] q[v][h]): the int8 table as the output projection."""
+    M, H = x.shape
+    V = q.shape[0]
+    if q.shape[1] != H:
+        raise ValueError(f"q is {tuple(q.shape)}, x has {H} channels")
+    if out is None:
+        out = torch.empty((M, V), dtype=torch.bfloat16, device=x.device)
+    _check(lib().exl3_lm_head_int8(_ptr(x, torch.bfloat16, "x"), M, H, _ptr(q, torch.int8, "q"),
+                                   _ptr(scale, torch.float16, "scale"), V, _ptr(out, torch.bfloat16, "out"),
+                                   out.stride(0), _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(x.device)),
+           "exl3_lm_head_int8")
     return out

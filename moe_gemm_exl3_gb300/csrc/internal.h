@@ -166,9 +166,19 @@ cudaError_t launch_fused_rows(FusedArgs &a, const uint16_t *u, int64_t u_rows, i
 int forced_mode();
 
 bool prefill_supported();
+// epi 0: the EXL3 output transform (OC a multiple of 128); epi 1: a per-column
+// scale rout, no transform (any OC).
 cudaError_t launch_prefill(const uint16_t *u, const uint16_t *wt, int64_t M, int IC, int OC,
                            const uint16_t *rout, const uint16_t *s_out, uint16_t *out,
-                           int64_t ldo, int32_t *err, cudaStream_t s, bool *launched);
+                           int64_t ldo, int32_t *err, cudaStream_t s, bool *launched, int epi = 0);
+
+// int8 output head, few rows (M <= 32), x16 the fp16 activations: ctr = two
+// zeroed workspace counters.
+cudaError_t launch_lm_head_decode(const uint16_t *x16, int M, int H, const int8_t *q, const uint16_t *scale, int64_t V,
+                                  uint16_t *out, int64_t ldo, int32_t *ctr, cudaStream_t s);
+// Conversions for the tensor-core head: int8 rows -> fp16, bf16 rows -> fp16 (exact).
+cudaError_t launch_i8_to_f16(const int8_t *q, int64_t n, uint16_t *dst, cudaStream_t s);
+cudaError_t launch_bf16_to_f16(const uint16_t *x, int64_t n, uint16_t *dst, cudaStream_t s);
 
 cudaError_t launch_gather(const int8_t *q, const uint16_t *scale, int64_t V, int H,
                           const int32_t *ids, int64_t N, uint16_t *out, int32_t *n_bad,

@@ -50,7 +50,9 @@ __device__ __forceinline__ void tile_coords(int t, int MT, int NT, int &mt, int 
 
 // Persistent: one CTA per SM walks tiles blockIdx.x, + gridDim.x, ...  Two TMEM
 // accumulators (2 x 256 columns) let the epilogue of one tile overlap the MMAs of
-// the next.
+// the next.  EPI 0: y = (Had128(v) * rout) * s_out (the EXL3 output transform);
+// EPI 1: y = v * rout per column (the int8 output head's row scale; s_out unused).
+template <int EPI>
 __global__ void __launch_bounds__(192, 1)
 prefill_gemm_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_w,
                     int M, int IC, int OC, const uint16_t *__restrict__ rout, const uint16_t *__restrict__ s_out,
@@ -168,6 +170,32 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_const
                 }
                 tmem_ld_wait();
                 if (m >= M) continue;
+                uint16_t *dst = out + (int64_t)m * ldo + col;
+                if constexpr (EPI == 1) {
+                    // per-column scale, no transform; a partial last block stores its columns one by one
+                    const int ncol = OC - col < kHad ? OC - col : kHad;
+                    if (ncol == kHad && ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(rout + col)) & 15u) == 0) {
+#pragma unroll
+                        for (int c8 = 0; c8 < 16; c8++) {
+                            const uint4 sc = __ldg(reinterpret_cast<const uint4 *>(rout + col) + c8);
+                            const uint32_t sw[4] = {sc.x, sc.y, sc.z, sc.w};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int qq = 0; qq < 4; qq++) {
+                                const int c = c8 * 8 + 2 * qq;
+                                const float y0 = v[c] * f16_bits_to_f32((uint16_t)(sw[qq] & 0xFFFFu));
+                                const float y1 = v[c + 1] * f16_bits_to_f32((uint16_t)(sw[qq] >> 16));
+                                o[qq] = (uint32_t)f32_to_bf16_bits(y0) | ((uint32_t)f32_to_bf16_bits(y1) << 16);
+                            }
+                            reinterpret_cast<uint4 *>(dst)[c8] = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < kHad; c++)
+                            if (c < ncol) dst[c] = f32_to_bf16_bits(v[c] * f16_bits_to_f32(__ldg(rout + col + c)));
+                    }
+                    continue;
+                }
 #pragma unroll
                 for (int hs = 1; hs < 128; hs <<= 1) {
 #pragma unroll
@@ -178,7 +206,6 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_const
                         v[q + hs] = a - c2;
                     }
                 }
-                uint16_t *dst = out + (int64_t)m * ldo + col;
 #pragma unroll
                 for (int c8 = 0; c8 < 16; c8++) {
                     // scale vectors are only 8-byte aligned
@@ -229,19 +256,24 @@ bool prefill_supported() { return tma_encode_available(); }
 
 cudaError_t launch_prefill(const uint16_t *u, const uint16_t *wt, int64_t M, int IC, int OC, const uint16_t *rout,
                            const uint16_t *s_out, uint16_t *out, int64_t ldo, int32_t *err, cudaStream_t s,
-                           bool *launched) {
+                           bool *launched, int epi) {
     *launched = false;
-    if (M <= 0 || IC % BK || OC % kHad || M > INT32_MAX) return cudaErrorInvalidValue;
+    if (M <= 0 || IC % BK || (epi == 0 && OC % kHad) || M > INT32_MAX) return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(u) | reinterpret_cast<uintptr_t>(wt)) & 15u) return cudaErrorInvalidValue;
     CUtensorMap tm_u, tm_w;
     if (!make_map_f16(&tm_u, u, M, IC, BM) || !make_map_f16(&tm_w, wt, OC, IC, BN)) return cudaErrorInvalidValue;
-    cudaError_t ea = kernel_smem_optin((const void *)prefill_gemm_kernel, SMEM_BYTES);
+    const void *fn = epi == 0 ? (const void *)prefill_gemm_kernel<0> : (const void *)prefill_gemm_kernel<1>;
+    cudaError_t ea = kernel_smem_optin(fn, SMEM_BYTES);
     if (ea != cudaSuccess) return ea;
     const int64_t tiles = ((M + BM - 1) / BM) * (int64_t)((OC + BN - 1) / BN);
     int64_t grid = device_info().sm_count;   // persistent: one CTA per SM
     if (grid > tiles) grid = tiles;
-    prefill_gemm_kernel<<<(unsigned)grid, 192, SMEM_BYTES, s>>>(tm_u, tm_w, (int)M, IC, OC, rout, s_out, out, ldo,
-                                                                err);
+    if (epi == 0)
+        prefill_gemm_kernel<0><<<(unsigned)grid, 192, SMEM_BYTES, s>>>(tm_u, tm_w, (int)M, IC, OC, rout, s_out, out,
+                                                                       ldo, err);
+    else
+        prefill_gemm_kernel<1><<<(unsigned)grid, 192, SMEM_BYTES, s>>>(tm_u, tm_w, (int)M, IC, OC, rout, s_out, out,
+                                                                       ldo, err);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) *launched = true;
     return e;
