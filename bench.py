@@ -497,9 +497,7 @@ class Layer:
                      "o": torch.empty((self.M, 5120), dtype=torch.bfloat16, device=dev),
                      "gu": torch.empty((self.M, 34816), dtype=torch.bfloat16, device=dev),
                      "down": torch.empty((self.M, 5120), dtype=torch.bfloat16, device=dev)}
-        self.ws = m.workspace(max(m.exl3_linear_workspace_bytes(self.M, 17408, 17408),
-                                  m.exl3_linear_shards_workspace_bytes(
-                                      self.M, 5120, [self._sh("gate", 0), self._sh("up", 0)])), dev)
+        self.ws = m.workspace(m.exl3_projections_workspace_bytes(self.M, self._projs(0)), dev)
         self.l2 = (f"{R} rotating code copies ({R * self.code_bytes / 1e6:.0f} MB)" if R > 1
                    else "inputs larger than L2")
         self.launches_per_step = sum(linear_launches(self.M, n) for n in (1, 1, 2, 1))
@@ -509,16 +507,15 @@ class Layer:
         t = (c[r], K, *sc)
         return t + ((col0,) if col0 is not None else ())
 
+    def _projs(self, r, x=None):
+        return [(self.x0 if x is None else x, [self._sh("qkv", r, 0)], self.outs["qkv"]),
+                (self.xs["o"], [self._sh("o", r, 0)], self.outs["o"]),
+                (self.xs["gate"], [self._sh("gate", r, 0), self._sh("up", r, 17408)], self.outs["gu"]),
+                (self.xs["down"], [self._sh("down", r, 0)], self.outs["down"])]
+
     def step(self, r, x=None):
-        m = self.m
-        c, K, sc = self.dsh["qkv"]
-        m.exl3_linear_into(self.x0 if x is None else x, c[r], K, *sc, self.outs["qkv"], 0, self.ws)
-        c, K, sc = self.dsh["o"]
-        m.exl3_linear_into(self.xs["o"], c[r], K, *sc, self.outs["o"], 0, self.ws)
-        m.exl3_linear_into_shards(self.xs["gate"], [self._sh("gate", r, 0), self._sh("up", r, 17408)],
-                                  self.outs["gu"], self.ws)
-        c, K, sc = self.dsh["down"]
-        m.exl3_linear_into(self.xs["down"], c[r], K, *sc, self.outs["down"], 0, self.ws)
+        # the layer's projections in one library call on one workspace
+        self.m.exl3_linear_projections(self._projs(r, x), self.ws)
 
     def roofline(self, torch, stream):
         ms = kernel_time_ms(torch, stream, lambda j: self.step(j % self.R), 4 * self.R)

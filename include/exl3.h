@@ -232,6 +232,33 @@ exl3_status exl3_gemm_into_shards(const uint16_t *u, int64_t M, int32_t IC,
                                   uint16_t *out, int64_t ldo,
                                   void *ws, size_t ws_bytes, exl3_stream stream);
 
+/*
+ * Several projections of one layer (for a decoder layer: qkv, o, gate_up, down)
+ * in one call on one workspace, in order: projection i is exl3_linear_into_shards
+ * on its own x_i, IC_i, shards and out_i.  Inputs that several projections read
+ * are transformed once: projections with the same x pointer share the
+ * pre-transformed rows of every distinct (s_in, rin) pointer pair among their
+ * shards (equal values under different pointers are not detected).  All
+ * projections have M rows.  The call only enqueues work (graph-capturable);
+ * a projection's x may be the output of an earlier one in the same call.
+ *   projs     HOST array of n descriptors, 1 <= n <= 16; shards HOST arrays
+ *   ws        exl3_projections_workspace_bytes(M, projs, n) bytes, prepared by
+ *             exl3_workspace_init
+ */
+typedef struct exl3_projection {
+    const uint16_t *x;          /* bf16 [M][IC] */
+    int32_t IC;
+    int32_t n_shards;           /* 1..4 */
+    const exl3_shard *shards;   /* HOST array of n_shards descriptors */
+    uint16_t *out;              /* bf16 [M][ldo] */
+    int64_t ldo;
+} exl3_projection;
+
+size_t exl3_projections_workspace_bytes(int64_t max_M, const exl3_projection *projs, int32_t n);
+
+exl3_status exl3_linear_projections(const exl3_projection *projs, int32_t n, int64_t M,
+                                    void *ws, size_t ws_bytes, exl3_stream stream);
+
 /* exl3_linear_into with out = y [M][OC] contiguous (ldo = OC, col0 = 0). */
 exl3_status exl3_linear(const uint16_t *x, int64_t M, int32_t IC,
                         const int16_t *code, int32_t OC, int32_t K,

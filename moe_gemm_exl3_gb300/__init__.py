@@ -28,7 +28,8 @@ EXPORTS = ("exl3_last_error", "exl3_version", "exl3_linear_workspace_bytes", "ex
            "exl3_linear_shards_workspace_bytes", "exl3_linear_into_shards", "exl3_gemm_into_shards", "exl3_pretransform",
            "exl3_reconstruct", "exl3_codebook_table", "exl3_moe_topk_softmax",
            "exl3_moe_workspace_bytes", "exl3_moe_grouped", "exl3_embed_int8_gather",
-           "exl3_lm_head_workspace_bytes", "exl3_lm_head_int8")
+           "exl3_lm_head_workspace_bytes", "exl3_lm_head_int8", "exl3_projections_workspace_bytes",
+           "exl3_linear_projections")
 
 
 class Exl3Error(RuntimeError):
@@ -42,6 +43,12 @@ class Shard(ctypes.Structure):
     _fields_ = [("code", ctypes.c_void_p), ("s_in", ctypes.c_void_p), ("rin", ctypes.c_void_p),
                 ("rout", ctypes.c_void_p), ("s_out", ctypes.c_void_p), ("OC", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("col0", ctypes.c_int64)]
+
+
+class Projection(ctypes.Structure):
+    """exl3_projection: one projection of a layer (input, shards, output)."""
+    _fields_ = [("x", ctypes.c_void_p), ("IC", ctypes.c_int32), ("n_shards", ctypes.c_int32),
+                ("shards", ctypes.POINTER(Shard)), ("out", ctypes.c_void_p), ("ldo", ctypes.c_int64)]
 
 
 class MoeBank(ctypes.Structure):
@@ -93,6 +100,8 @@ def lib() -> ctypes.CDLL:
                                       vp, sz, vp], ctypes.c_int),
                 "exl3_embed_int8_gather": ([vp, vp, i64, i32, vp, i64, vp, vp, vp], ctypes.c_int),
                 "exl3_lm_head_workspace_bytes": ([i64, i32, i64], sz),
+                "exl3_projections_workspace_bytes": ([i64, ctypes.POINTER(Projection), i32], sz),
+                "exl3_linear_projections": ([ctypes.POINTER(Projection), i32, i64, vp, sz, vp], ctypes.c_int),
                 "exl3_lm_head_int8": ([vp, i64, i32, vp, vp, i64, vp, i64, vp, sz, vp], ctypes.c_int),
             }
             for name, (args, res) in sig.items():
@@ -240,6 +249,33 @@ def exl3_linear_into_shards(x: torch.Tensor, shards, out: torch.Tensor, ws: torc
                                          _ptr(out, torch.bfloat16, "out"), out.shape[-1],
                                          _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(x.device)),
            "exl3_linear_into_shards")
+
+
+def _projection_array(projs):
+    """projs: sequence of (x [M][IC] bf16, shards, out [M][ldo] bf16); keeps the shard arrays alive."""
+    arr = (Projection * len(projs))()
+    keep = []
+    for i, (x, shards, out) in enumerate(projs):
+        IC = x.shape[-1]
+        sa = _shard_array(shards, IC)
+        keep.append(sa)
+        arr[i] = Projection(_ptr(x, torch.bfloat16, "x"), IC, len(shards), sa, _ptr(out, torch.bfloat16, "out"),
+                            out.shape[-1])
+    return arr, keep
+
+
+def exl3_projections_workspace_bytes(max_M: int, projs) -> int:
+    arr, keep = _projection_array(projs)
+    return int(lib().exl3_projections_workspace_bytes(max_M, arr, len(projs)))
+
+
+def exl3_linear_projections(projs, ws: torch.Tensor) -> None:
+    """Several projections of one layer in one call (see include/exl3.h): projs is a
+    sequence of (x, shards, out); inputs read by several projections are transformed once."""
+    arr, keep = _projection_array(projs)
+    M = projs[0][0].shape[0]
+    _check(lib().exl3_linear_projections(arr, len(projs), M, _ptr(ws, torch.uint8, "ws"), ws.numel(),
+                                         _stream(projs[0][0].device)), "exl3_linear_projections")
 
 
 def exl3_gemm_into_shards(u: torch.Tensor, shards, out: torch.Tensor, ws: torch.Tensor) -> None:

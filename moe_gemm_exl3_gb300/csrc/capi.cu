@@ -289,10 +289,12 @@ struct ShardDesc {
 };
 
 // Trellis GEMM + epilogue for n shards whose pre-transformed activations sit
-// in u as [shard][M][IC] (fp16).
+// in u as [slot][M][IC] (fp16); shard i uses slot slots[i] (i if slots is null).
 static exl3_status run_gemm(const char *fn, const uint16_t *u, int64_t M, int32_t IC, const ShardDesc *sh, int n,
-                            uint16_t *out, int64_t ldo, const LinearWorkspace &ws, bool pdl, cudaStream_t s) {
+                            uint16_t *out, int64_t ldo, const LinearWorkspace &ws, bool pdl, cudaStream_t s,
+                            const int *slots = nullptr) {
     cudaError_t e;
+    auto slot = [&](int i) { return slots ? slots[i] : i; };
     const GemmMode mode = gemm_mode(M);
     if (mode == GemmMode::kFused) {
         FusedArgs a = {};
@@ -309,6 +311,7 @@ static exl3_status run_gemm(const char *fn, const uint16_t *u, int64_t M, int32_
             f.K = sh[i].K;
             f.OC = sh[i].OC;
             f.g0 = g0;
+            f.u_slot = slot(i);
             g0 += sh[i].OC / 128;
         }
         a.out = out;
@@ -326,7 +329,7 @@ static exl3_status run_gemm(const char *fn, const uint16_t *u, int64_t M, int32_
             bool launched = false;
             e = launch_reconstruct(sh[i].code, IC, sh[i].OC, sh[i].K, ws.wt, /*transposed=*/true, s);
             if (e != cudaSuccess) return cuda_fail(e, fn);
-            e = launch_prefill(u + (int64_t)i * M * IC, ws.wt, M, IC, sh[i].OC, sh[i].rout, sh[i].s_out,
+            e = launch_prefill(u + (int64_t)slot(i) * M * IC, ws.wt, M, IC, sh[i].OC, sh[i].rout, sh[i].s_out,
                                out + sh[i].col0, ldo, ws.err, s, &launched);
             if (e != cudaSuccess) return cuda_fail(e, fn);
             if (!launched) return fail(EXL3_EUNSUPPORTED, "%s: prefill path unavailable", fn);
@@ -351,7 +354,7 @@ static exl3_status run_gemm(const char *fn, const uint16_t *u, int64_t M, int32_
             ge.out_off = sh[i].col0;
             ge.K = sh[i].K;
             ge.OC = sh[i].OC;
-            ge.u_row0 = (int32_t)((int64_t)i * M + r0);
+            ge.u_row0 = (int32_t)((int64_t)slot(i) * M + r0);
             ge.nrows = rows;
             ge.g0 = g0;
             g0 += sh[i].OC / 128;
@@ -522,6 +525,164 @@ exl3_status exl3_embed_int8_gather(const int8_t *q, const uint16_t *scale, int64
         return fail(EXL3_EINVAL, "embed_int8_gather: q (%p) and out (%p) must be 16-byte aligned", q, out);
     cudaError_t e = launch_gather(q, scale, V, H, ids, N, out, n_bad, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "embed_int8_gather");
+    return EXL3_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ projections
+namespace {
+
+constexpr int kMaxProjections = 16;
+constexpr int kMaxSlots = 16;   // distinct (s_in, rin) pre-transforms of one input
+
+// A call's plan: projections that read the same x share one group of
+// pre-transformed rows, one slot per distinct (s_in, rin) pair (pointer equality).
+struct ProjPlan {
+    struct Group {
+        const uint16_t *x;
+        int32_t IC;
+        int nslots;
+        const uint16_t *s_in[kMaxSlots], *rin[kMaxSlots];
+        size_t off;          // byte offset of its rows [slot][M][IC] in the u region
+        int first_proj;      // the projection that transforms it
+    } g[kMaxProjections];
+    int ng = 0;
+    int group_of[kMaxProjections];
+    int slot_of[kMaxProjections][kMaxInlineEntries];
+    size_t u_bytes = 0, part_elems = 0, wt_elems = 0;
+};
+
+const char *plan_projections(const exl3_projection *p, int32_t n, int64_t M, ProjPlan *pl) {
+    if (!p || n < 1 || n > kMaxProjections) return "need 1..16 projections";
+    for (int i = 0; i < n; i++) {
+        const exl3_projection &pr = p[i];
+        int groups;
+        int32_t max_oc;
+        if (pr.IC <= 0 || pr.IC % 128 || !shards_shape(pr.shards, pr.n_shards, &groups, &max_oc))
+            return "a projection needs IC a positive multiple of 128 and 1..4 shards of OC a multiple of 128";
+        int gi = 0;
+        while (gi < pl->ng && !(pl->g[gi].x == pr.x && pl->g[gi].IC == pr.IC)) gi++;
+        if (gi == pl->ng) {
+            ProjPlan::Group &g = pl->g[pl->ng++];
+            g.x = pr.x;
+            g.IC = pr.IC;
+            g.nslots = 0;
+            g.first_proj = i;
+        }
+        ProjPlan::Group &g = pl->g[gi];
+        pl->group_of[i] = gi;
+        for (int k = 0; k < pr.n_shards; k++) {
+            int sl = 0;
+            while (sl < g.nslots && !(g.s_in[sl] == pr.shards[k].s_in && g.rin[sl] == pr.shards[k].rin)) sl++;
+            if (sl == g.nslots) {
+                if (g.nslots == kMaxSlots) return "more than 16 distinct (s_in, rin) pairs on one input";
+                g.s_in[sl] = pr.shards[k].s_in;
+                g.rin[sl] = pr.shards[k].rin;
+                g.nslots++;
+            }
+            pl->slot_of[i][k] = sl;
+        }
+        // split-K slab and prefill staging of this projection's GEMM (shared, used in turn)
+        const int64_t dec_rows = M < kDecodeMaxRows ? M : kDecodeMaxRows;
+        const int nb = (int)((dec_rows + 7) / 8 > 0 ? (dec_rows + 7) / 8 : 1);
+        size_t part = group_slab_floats(groups, nb);
+        if (fused_supported() && M > 0) {
+            const size_t f = fused_slab_floats(groups, M);
+            if (f > part) part = f;
+        }
+        if (part > pl->part_elems) pl->part_elems = part;
+        if ((M > kFusedMaxRows || (M > 0 && forced_mode() == 3)) && prefill_supported()) {
+            const size_t wt = (size_t)max_oc * pr.IC;
+            if (wt > pl->wt_elems) pl->wt_elems = wt;
+        }
+    }
+    size_t off = 0;
+    for (int gi = 0; gi < pl->ng; gi++) {
+        pl->g[gi].off = off;
+        off = align256(off + sizeof(uint16_t) * (size_t)pl->g[gi].nslots * M * pl->g[gi].IC);
+    }
+    pl->u_bytes = off;
+    return nullptr;
+}
+
+// Workspace: fixed header | u region | split-K slab | prefill staging.
+size_t projections_layout(const ProjPlan &pl, size_t *u_off, size_t *part_off, size_t *wt_off) {
+    size_t off = kFixedBytes;
+    *u_off = off;
+    off = align256(off + pl.u_bytes);
+    *part_off = off;
+    off = align256(off + sizeof(float) * pl.part_elems);
+    *wt_off = off;
+    off = align256(off + sizeof(uint16_t) * pl.wt_elems);
+    return off;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t exl3_projections_workspace_bytes(int64_t max_M, const exl3_projection *p, int32_t n) {
+    if (max_M < 0) return 0;
+    ProjPlan pl;
+    if (plan_projections(p, n, max_M, &pl)) return 0;
+    size_t a, b, c;
+    return projections_layout(pl, &a, &b, &c);
+}
+
+exl3_status exl3_linear_projections(const exl3_projection *p, int32_t n, int64_t M, void *wsp, size_t ws_bytes,
+                                    exl3_stream stream) {
+    const char *fn = "linear_projections";
+    if (M < 0) return fail(EXL3_EINVAL, "%s: M = %lld is negative", fn, (long long)M);
+    ProjPlan pl;
+    if (const char *why = plan_projections(p, n, M, &pl)) return fail(EXL3_EINVAL, "%s: %s", fn, why);
+    size_t u_off, part_off, wt_off;
+    const size_t need = projections_layout(pl, &u_off, &part_off, &wt_off);
+    for (int i = 0; i < n; i++) {
+        const exl3_projection &pr = p[i];
+        for (int k = 0; k < pr.n_shards; k++) {
+            const exl3_shard &h = pr.shards[k];
+            exl3_status st = check_linear_args(fn, pr.x, M, pr.IC, h.code, h.OC, h.K, h.s_in, h.rin, h.rout, h.s_out);
+            if (st == EXL3_OK) st = check_out_ws(fn, M, h.OC, pr.out, pr.ldo, h.col0, wsp, ws_bytes, need);
+            if (st != EXL3_OK) return st;
+        }
+    }
+    if (M == 0) return EXL3_OK;
+    char *b = static_cast<char *>(wsp);
+    LinearWorkspace ws;
+    ws.err = workspace_err(wsp);
+    ws.counters = workspace_counters(wsp);
+    ws.counters_n = kCounterCount;
+    ws.partials = reinterpret_cast<float *>(b + part_off);
+    ws.partial_elems = pl.part_elems;
+    ws.wt = pl.wt_elems ? reinterpret_cast<uint16_t *>(b + wt_off) : nullptr;
+    ws.wt_elems = pl.wt_elems;
+    cudaStream_t s = (cudaStream_t)stream;
+    for (int i = 0; i < n; i++) {
+        const exl3_projection &pr = p[i];
+        const ProjPlan::Group &g = pl.g[pl.group_of[i]];
+        uint16_t *u = reinterpret_cast<uint16_t *>(b + u_off + g.off);
+        if (g.first_proj == i) {
+            // every pre-transform of this input, once (up to four per launch)
+            for (int s0 = 0; s0 < g.nslots; s0 += 4) {
+                PretransformShards pt = {};
+                pt.n = g.nslots - s0 < 4 ? g.nslots - s0 : 4;
+                for (int k = 0; k < pt.n; k++) {
+                    pt.s_in[k] = g.s_in[s0 + k];
+                    pt.rin[k] = g.rin[s0 + k];
+                }
+                cudaError_t e = launch_pretransform_shards(pr.x, M, pr.IC, pt, u + (int64_t)s0 * M * pr.IC, s);
+                if (e != cudaSuccess) return cuda_fail(e, "linear_projections: pretransform");
+            }
+        }
+        ShardDesc d[kMaxInlineEntries];
+        for (int k = 0; k < pr.n_shards; k++) {
+            const exl3_shard &h = pr.shards[k];
+            d[k] = {h.code, h.s_in, h.rin, h.rout, h.s_out, h.OC, h.K, h.col0};
+        }
+        exl3_status st = run_gemm(fn, u, M, pr.IC, d, pr.n_shards, pr.out, pr.ldo, ws, true, s, pl.slot_of[i]);
+        if (st != EXL3_OK) return st;
+    }
     return EXL3_OK;
 }
 

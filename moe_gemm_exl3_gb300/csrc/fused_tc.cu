@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
             d.K = sh.K;
             d.TO = sh.OC / kTile;
             d.G = gi - sh.g0;
-            d.u_row = sidx * M;
+            d.u_row = sh.u_slot * M;
             d.rows = M;
             d.out0 = sh.col0;
             d.tm = sidx;
@@ -683,7 +683,11 @@ cudaError_t launch_fused(FusedArgs &a, const uint16_t *u, cudaStream_t s) {
     if (a.M <= 0 || a.M > kFusedMaxRows || a.IC <= 0 || a.IC % 128 || a.n_shards < 1 || a.n_shards > 4)
         return cudaErrorInvalidValue;
     const int nt = a.M <= 16 ? 16 : (a.M <= 32 ? 32 : (a.M <= 64 ? 64 : 128));
-    if (!make_map_f16(&a.tm_u, u, (int64_t)a.n_shards * a.M, a.IC, nt)) return cudaErrorInvalidValue;
+    int slots = 0;
+    for (int i = 0; i < a.n_shards; i++)
+        if (a.sh[i].u_slot < 0) return cudaErrorInvalidValue;
+        else if (a.sh[i].u_slot + 1 > slots) slots = a.sh[i].u_slot + 1;
+    if (!make_map_f16(&a.tm_u, u, (int64_t)slots * a.M, a.IC, nt)) return cudaErrorInvalidValue;
     for (int i = 0; i < a.n_shards; i++)
         if (!make_map_code(&a.tm_code[i], a.sh[i].code, a.IC, a.sh[i].OC, a.sh[i].K)) return cudaErrorInvalidValue;
     a.entries = nullptr;

@@ -129,7 +129,7 @@ struct FusedShard {
     int64_t col0;        // first output column of this shard
     int32_t K, OC;
     int32_t g0;          // first global column-group index
-    int32_t pad_;
+    int32_t u_slot;      // this shard's activations are rows [u_slot * M, (u_slot + 1) * M) of u
 };
 struct FusedArgs {
     CUtensorMap tm_u;        // u [n_shards * M][IC], box 64 channels x rows-per-tile
