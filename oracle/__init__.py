@@ -77,6 +77,10 @@ def lib():
                                             _P(u16), _P(u16), _P(u16), ctypes.c_long,
                                             ctypes.c_long]
             L.exl3o_linear_into.restype = ctypes.c_int
+            L.exl3o_linear_a8_f64.argtypes = [_P(u16), ctypes.c_long, ctypes.c_int, _P(i16), ctypes.c_int,
+                                              ctypes.c_int, _P(u16), _P(u16), _P(u16), _P(u16), ctypes.c_int,
+                                              ctypes.c_int, _P(f64), _P(ctypes.c_uint8), _P(f64)]
+            L.exl3o_linear_a8_f64.restype = ctypes.c_int
             L.exl3o_lm_head_f64.argtypes = [_P(u16), ctypes.c_long, ctypes.c_int, _P(i8), _P(u16), ctypes.c_long,
                                             ctypes.c_long, ctypes.c_long, _P(f64)]
             L.exl3o_lm_head_f64.restype = ctypes.c_int
@@ -211,6 +215,26 @@ def linear_f64(x, code, K, s_in, rin, rout, s_out, blk0=0, nblk=None) -> np.ndar
                                   _ptr(_u16(s_out), ctypes.c_uint16), blk0, nblk,
                                   _ptr(y, ctypes.c_double)), "linear")
     return y
+
+
+def linear_a8_f64(x, code, K, s_in, rin, rout, s_out, blk0=0, nblk=None):
+    """The 8-bit activation variant (see exl3_oracle.c): fp64 y[M][nblk*128] (unrounded),
+    the activation codes A uint8 [M][IC] (q + 128) and the row scales As [M]."""
+    x = _u16(x)
+    code = np.ascontiguousarray(code, dtype=np.int16)
+    M, IC = x.shape
+    OC = code.shape[1] * 16
+    assert code.shape[0] * 16 == IC and code.shape[2] == 16 * K
+    nblk = OC // 128 - blk0 if nblk is None else nblk
+    y = np.empty((M, nblk * 128), np.float64)
+    A = np.empty((M, IC), np.uint8)
+    As = np.empty(M, np.float64)
+    _check(lib().exl3o_linear_a8_f64(_ptr(x, ctypes.c_uint16), M, IC, _ptr(code, ctypes.c_int16), OC, K,
+                                     _ptr(_u16(s_in), ctypes.c_uint16), _ptr(_u16(rin), ctypes.c_uint16),
+                                     _ptr(_u16(rout), ctypes.c_uint16), _ptr(_u16(s_out), ctypes.c_uint16),
+                                     blk0, nblk, _ptr(y, ctypes.c_double), _ptr(A, ctypes.c_uint8),
+                                     _ptr(As, ctypes.c_double)), "linear_a8")
+    return y, A, As
 
 
 def linear_into(out: np.ndarray, x, code, K, s_in, rin, rout, s_out, col0: int) -> None:

@@ -574,3 +574,97 @@ int exl3o_lm_head_f64(const uint16_t *x, long M, int H, const int8_t *q, const u
     }
     return EXL3O_OK;
 }
+
+/* ------------------------------------------------------------------ 8-bit activations
+ * The 8-bit activation variant ([escha] escha_linear_into: escha_pre_quant fills
+ * an A buffer of uint8 [M][IC] with a float32 scale As [M] from a per-row amax
+ * [M]; the pages give the buffers, not the encoding).  Reading: per row of the
+ * pre-transformed activations u,
+ *     amax = max_c |u[c]|,  As = amax / 127,
+ *     q[c] = round_half_even(u[c] / As) clipped to [-127, 127]   (q = 0 if amax = 0)
+ *     A[c] = q[c] + 128  (offset binary in a byte)
+ * and the GEMM multiplies q * As in place of u:
+ *     y = (Had128((q * As) @ decode(code)) * rout) * s_out.
+ * Codes and scales are returned if the pointers are non-null (A [M][IC],
+ * As [M]); y as in exl3o_linear_f64.
+ */
+int exl3o_quantize_a8(const double *u, long M, int IC, uint8_t *A, double *As)
+{
+    for (long m = 0; m < M; m++) {
+        double amax = 0.0;
+        for (int c = 0; c < IC; c++)
+            if (fabs(u[m * IC + c]) > amax)
+                amax = fabs(u[m * IC + c]);
+        const double s = amax / 127.0;
+        As[m] = s;
+        for (int c = 0; c < IC; c++) {
+            double q = 0.0;
+            if (s > 0.0) {
+                q = nearbyint(u[m * IC + c] / s);   /* default rounding mode: half to even */
+                if (q > 127.0) q = 127.0;
+                if (q < -127.0) q = -127.0;
+            }
+            A[m * IC + c] = (uint8_t)((int)q + 128);
+        }
+    }
+    return EXL3O_OK;
+}
+
+int exl3o_linear_a8_f64(const uint16_t *x, long M, int IC,
+                        const int16_t *code, int OC, int K,
+                        const uint16_t *s_in, const uint16_t *rin,
+                        const uint16_t *rout, const uint16_t *s_out,
+                        int blk0, int nblk, double *y, uint8_t *A_out, double *As_out)
+{
+    if (!valid_k(K) || IC % 128 || OC % 128 || M < 0 || blk0 < 0 || nblk < 0 ||
+        (long)(blk0 + nblk) * 128 > OC)
+        return EXL3O_EINVAL;
+    if (M == 0)
+        return EXL3O_OK;
+    int noc = nblk * 128, oc0 = blk0 * 128;
+    double *u = malloc(sizeof(double) * (size_t)M * IC);
+    uint8_t *A = malloc((size_t)M * IC);
+    double *As = malloc(sizeof(double) * M);
+    uint16_t *Wh = malloc(sizeof(uint16_t) * (size_t)IC * (noc > 0 ? noc : 1));
+    double *W = malloc(sizeof(double) * (size_t)IC * (noc > 0 ? noc : 1));
+    double *H = malloc(sizeof(double) * 128 * 128);
+    if (!u || !A || !As || !Wh || !W || !H) {
+        free(u); free(A); free(As); free(Wh); free(W); free(H);
+        return EXL3O_EINVAL;
+    }
+    /* step 1: the activations, transformed, then quantized per row */
+    exl3o_pretransform_f64(x, M, IC, s_in, rin, u);
+    exl3o_quantize_a8(u, M, IC, A, As);
+    if (A_out)
+        memcpy(A_out, A, (size_t)M * IC);
+    if (As_out)
+        memcpy(As_out, As, sizeof(double) * M);
+    if (noc > 0) {
+        exl3o_hadamard128(H);
+        exl3o_reconstruct_cols(code, IC, OC, K, oc0, noc, Wh);
+        for (long i = 0; i < (long)IC * noc; i++)
+            W[i] = exl3o_f16_to_f64(Wh[i]);
+#pragma omp parallel for schedule(dynamic)
+        for (long m = 0; m < M; m++) {
+            double *v = malloc(sizeof(double) * noc);
+            double *hv = malloc(sizeof(double) * noc);
+            /* step 2: GEMM of the dequantized activations q * As */
+            for (int j = 0; j < noc; j++)
+                v[j] = 0.0;
+            for (int c = 0; c < IC; c++) {
+                const double uc = ((int)A[m * IC + c] - 128) * As[m];
+                const double *wr = W + (long)c * noc;
+                for (int j = 0; j < noc; j++)
+                    v[j] += uc * wr[j];
+            }
+            /* step 3: output Hadamard, then rout, then s_out */
+            had_blocks(H, v, hv, noc);
+            for (int j = 0; j < noc; j++)
+                y[m * noc + j] = (hv[j] * exl3o_f16_to_f64(rout[oc0 + j]))
+                                 * exl3o_f16_to_f64(s_out[oc0 + j]);
+            free(v); free(hv);
+        }
+    }
+    free(u); free(A); free(As); free(Wh); free(W); free(H);
+    return EXL3O_OK;
+}
