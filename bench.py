@@ -268,6 +268,69 @@ class GateUp:
                             f"shards, scaled linearly to all {nblk_total} blocks")
 
 
+class GateUpA8(GateUp):
+    """The gate/up projection with 8-bit activations: each shard's activations
+    are quantized per row (uint8 codes + fp32 row scale), then one grouped GEMM
+    launch multiplies the codes of both shards."""
+
+    def __init__(self, args):
+        super().__init__(args)
+        self.metric = "EXL3 linear tokens/s (decode-shaped gate_up, 8-bit activations)"
+
+    def config(self):
+        c = super().config()
+        c["workload"] = c["workload"].replace("gate_up", "gate_up a8", 1)
+        c["activations"] = "uint8 codes + fp32 row scale"
+        return c
+
+    def setup(self, torch, m, syn, dev):
+        super().setup(torch, m, syn, dev)
+        self.ws8 = m.workspace(m.exl3_linear_shards_a8_workspace_bytes(self.M, self.IC, self.sets[0]), dev)
+        self.A = torch.empty((2, self.M, self.IC), dtype=torch.uint8, device=dev)
+        self.As = torch.empty((2, self.M), dtype=torch.float32, device=dev)
+        for i, st in enumerate(self.sets[0]):
+            m.exl3_quantize_a8(self.xd, *st[2:4], A=self.A[i], As=self.As[i])
+        self.launches_per_step = linear_launches(self.M, 2)
+
+    def step(self, r, x=None):
+        self.m.exl3_linear_into_shards_a8(self.xd if x is None else x, self.sets[r], self.out, self.ws8)
+
+    def roofline(self, torch, stream):
+        R, m = self.R, self.m
+        ms = kernel_time_ms(torch, stream,
+                            lambda j: m.exl3_gemm_a8_into_shards(self.A, self.As, self.sets[j % R], self.out,
+                                                                 self.ws8), 4 * R)
+        hbm, _, src = peaks()
+        alg = sum(self.code_bytes(K) + self.M * self.IC + 4 * self.M + 2 * self.M * self.OC + 2 * 2 * self.OC
+                  for K in self.KS)
+        a = alg / (ms * 1e-3) / 1e9
+        kernel = {"decode": "group_gemm_kernel (8-bit codes)" if self.M <= 8 else "group_gemm_kernel",
+                  "fused": "codes_to_f16 + fused_tc_kernel",
+                  "prefill": "codes_to_f16 + reconstruct + prefill_gemm_kernel"}[gemm_path(self.M)]
+        return {"bound": "hbm", "kernel": kernel + " (gate K=2 + up K=3 in one call)",
+                "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
+                "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)", "traffic": None,
+                "per_launch_us": round(ms * 1e3, 2), "algorithmic_bytes_per_launch": alg}
+
+    def cpu_sample(self, budget):
+        import oracle
+        import synthetic as syn
+        x, shards = syn.gate_up(1, M=self.M)
+        nblk_total = self.OC // 128
+        oracle.lib()
+        t0 = time.perf_counter()
+        for sh in shards:
+            oracle.linear_a8_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=0, nblk=1)
+        per_blk = (time.perf_counter() - t0) / 2
+        nblk = int(min(nblk_total, max(1, budget / max(per_blk, 1e-6) / 2)))
+        t0 = time.perf_counter()
+        for sh in shards:
+            oracle.linear_a8_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out, blk0=0, nblk=nblk)
+        t = (time.perf_counter() - t0) * nblk_total / nblk
+        return self.M / t, (f"M={self.M}, output blocks 0..{nblk - 1} of {nblk_total} (128 columns each) of both "
+                            f"shards, scaled linearly to all {nblk_total} blocks")
+
+
 class Prefill:
     """Prefill-shaped linear 5120 -> 17408 at M = 8192 (1 % outlier channels)."""
     IC, OC = 5120, 17408
@@ -612,7 +675,7 @@ class LmHead:
         return self.M / t, f"vocabulary rows 0..{nv - 1} of {self.V}, scaled linearly to the whole table"
 
 
-WORKLOADS = {"gate_up": GateUp, "prefill": Prefill, "moe": Moe, "gather": Gather, "layer": Layer, "lm_head": LmHead}
+WORKLOADS = {"gate_up": GateUp, "gate_up_a8": GateUpA8, "prefill": Prefill, "moe": Moe, "gather": Gather, "layer": Layer, "lm_head": LmHead}
 
 
 # ------------------------------------------------------------------ our arm
@@ -674,7 +737,8 @@ def secondary_workloads():
     ns = argparse.Namespace
     return [("gate_up", ns(m=1)), ("gate_up", ns(m=64)), ("prefill", ns(m=8192, k=2)),
             ("moe", ns(t=1)), ("moe", ns(t=16)), ("moe", ns(t=512)), ("gather", ns()),
-            ("layer", ns(m=8)), ("layer", ns(m=8192)), ("lm_head", ns(m=1)), ("lm_head", ns(m=8))]
+            ("layer", ns(m=8)), ("layer", ns(m=8192)), ("lm_head", ns(m=1)), ("lm_head", ns(m=8)),
+            ("gate_up_a8", ns(m=8)), ("gate_up_a8", ns(m=64))]
 
 
 def run_secondary(torch, m, syn, dev, stream, local, K, W, min_seconds):
@@ -691,7 +755,7 @@ def run_secondary(torch, m, syn, dev, stream, local, K, W, min_seconds):
                     "unit": wl.unit, "steps": k, "trials": len(trials), "ms_per_step": round(ms / k, 5),
                     "roofline": wl.roofline(torch, stream), "clocks": clk.summary()})
         del wl
-        GateUp._codes.clear() if name == "gate_up" and a.m == 64 else None
+        GateUp._codes.clear() if name.startswith("gate_up") and a.m == 64 else None
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
     return out

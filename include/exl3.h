@@ -289,6 +289,85 @@ exl3_status exl3_reconstruct(const int16_t *code, int32_t IC, int32_t OC, int32_
  * table has 65536 entries. */
 exl3_status exl3_codebook_table(uint16_t *table, exl3_stream stream);
 
+/* ------------------------------------------------------- 8-bit activations */
+
+/*
+ * The 8-bit activation variant (radiance_escha.py, escha_linear_into: the
+ * projection fills a uint8 activation buffer A [M][IC] and a float32 scale
+ * As [M] from a per-row amax before its GEMM; the page gives the buffers, not
+ * the encoding).  The encoding read here, per row of the pre-transformed
+ * activations u = Had128((x * s_in) * rin):
+ *   As = amax / 127 (amax = max_c |u[c]|),
+ *   q[c] = u[c] / As rounded half to even, clamped to [-127, 127] (0 if amax = 0),
+ *   A[c] = q[c] + 128,
+ * and the projection multiplies q * As in place of u:
+ *   out[:, col0:col0+OC] = bf16( (Had128((q * As) @ decode(code)) * rout) * s_out ).
+ * u, amax, As and q / As are computed in fp32 on the device.
+ */
+
+/* Bytes of workspace for exl3_linear_into_a8 / exl3_gemm_a8_into with up to
+ * max_M rows (0 on invalid sizes); never decreases as max_M grows. */
+size_t exl3_linear_a8_workspace_bytes(int64_t max_M, int32_t max_IC, int32_t max_OC);
+
+/*
+ * The quantizer on its own: x bf16 [M][IC] -> A uint8 [M][IC], As fp32 [M]
+ * (device pointers; x, s_in, rin 8-byte aligned, A and As 4-byte aligned).
+ * IC * 4 bytes of shared memory serve one row: EXL3_EUNSUPPORTED past the
+ * device's limit (IC above about 56000 on this GPU).
+ */
+exl3_status exl3_quantize_a8(const uint16_t *x, int64_t M, int32_t IC,
+                             const uint16_t *s_in, const uint16_t *rin,
+                             uint8_t *A, float *As, exl3_stream stream);
+
+/*
+ * exl3_linear_into with 8-bit activations: same arguments, requirements and
+ * GEMM paths; ws of at least exl3_linear_a8_workspace_bytes(M, IC, OC) bytes.
+ * M <= 8 rows on the decode path multiply the codes straight from the
+ * workspace; other paths expand them to exact fp16 values first.
+ */
+exl3_status exl3_linear_into_a8(const uint16_t *x, int64_t M, int32_t IC,
+                                const int16_t *code, int32_t OC, int32_t K,
+                                const uint16_t *s_in, const uint16_t *rin,
+                                const uint16_t *rout, const uint16_t *s_out,
+                                uint16_t *out, int64_t ldo, int64_t col0,
+                                void *ws, size_t ws_bytes, exl3_stream stream);
+
+/*
+ * The GEMM and output transform on activations already quantized (A, As as
+ * exl3_quantize_a8 writes them; A 16-byte aligned): exl3_gemm_into with
+ * q * As in place of u.  ws of at least exl3_linear_a8_workspace_bytes(M, IC,
+ * OC) bytes.
+ */
+exl3_status exl3_gemm_a8_into(const uint8_t *A, const float *As, int64_t M, int32_t IC,
+                              const int16_t *code, int32_t OC, int32_t K,
+                              const uint16_t *rout, const uint16_t *s_out,
+                              uint16_t *out, int64_t ldo, int64_t col0,
+                              void *ws, size_t ws_bytes, exl3_stream stream);
+
+/*
+ * exl3_linear_into_shards with 8-bit activations: every shard's activations
+ * are quantized with its own (s_in, rin), then one grouped GEMM launch serves
+ * all shards.  ws of at least exl3_linear_shards_a8_workspace_bytes(M, IC,
+ * shards, n_shards) bytes.
+ */
+size_t exl3_linear_shards_a8_workspace_bytes(int64_t max_M, int32_t IC, const exl3_shard *shards,
+                                             int32_t n_shards);
+exl3_status exl3_linear_into_shards_a8(const uint16_t *x, int64_t M, int32_t IC,
+                                       const exl3_shard *shards, int32_t n_shards,
+                                       uint16_t *out, int64_t ldo,
+                                       void *ws, size_t ws_bytes, exl3_stream stream);
+
+/*
+ * exl3_gemm_into_shards on 8-bit activations: A uint8 [n_shards][M][IC] (16-byte
+ * aligned) and As fp32 [n_shards][M], shard i's rows quantized with its own
+ * (s_in, rin) as exl3_quantize_a8 writes them; the shards' s_in / rin pointers
+ * are ignored.  ws as for exl3_linear_into_shards_a8.
+ */
+exl3_status exl3_gemm_a8_into_shards(const uint8_t *A, const float *As, int64_t M, int32_t IC,
+                                     const exl3_shard *shards, int32_t n_shards,
+                                     uint16_t *out, int64_t ldo,
+                                     void *ws, size_t ws_bytes, exl3_stream stream);
+
 /* -------------------------------------------------------------------- MoE */
 
 /*

@@ -29,7 +29,9 @@ EXPORTS = ("exl3_last_error", "exl3_version", "exl3_linear_workspace_bytes", "ex
            "exl3_reconstruct", "exl3_codebook_table", "exl3_moe_topk_softmax",
            "exl3_moe_workspace_bytes", "exl3_moe_grouped", "exl3_embed_int8_gather",
            "exl3_lm_head_workspace_bytes", "exl3_lm_head_int8", "exl3_projections_workspace_bytes",
-           "exl3_linear_projections")
+           "exl3_linear_projections", "exl3_linear_a8_workspace_bytes", "exl3_quantize_a8",
+           "exl3_linear_into_a8", "exl3_gemm_a8_into", "exl3_linear_shards_a8_workspace_bytes",
+           "exl3_linear_into_shards_a8", "exl3_gemm_a8_into_shards")
 
 
 class Exl3Error(RuntimeError):
@@ -103,6 +105,17 @@ def lib() -> ctypes.CDLL:
                 "exl3_projections_workspace_bytes": ([i64, ctypes.POINTER(Projection), i32], sz),
                 "exl3_linear_projections": ([ctypes.POINTER(Projection), i32, i64, vp, sz, vp], ctypes.c_int),
                 "exl3_lm_head_int8": ([vp, i64, i32, vp, vp, i64, vp, i64, vp, sz, vp], ctypes.c_int),
+                "exl3_linear_a8_workspace_bytes": ([i64, i32, i32], sz),
+                "exl3_quantize_a8": ([vp, i64, i32, vp, vp, vp, vp, vp], ctypes.c_int),
+                "exl3_linear_into_a8": ([vp, i64, i32, vp, i32, i32, vp, vp, vp, vp, vp, i64, i64, vp, sz,
+                                         vp], ctypes.c_int),
+                "exl3_gemm_a8_into": ([vp, vp, i64, i32, vp, i32, i32, vp, vp, vp, i64, i64, vp, sz, vp],
+                                      ctypes.c_int),
+                "exl3_linear_shards_a8_workspace_bytes": ([i64, i32, ctypes.POINTER(Shard), i32], sz),
+                "exl3_linear_into_shards_a8": ([vp, i64, i32, ctypes.POINTER(Shard), i32, vp, i64, vp, sz, vp],
+                                               ctypes.c_int),
+                "exl3_gemm_a8_into_shards": ([vp, vp, i64, i32, ctypes.POINTER(Shard), i32, vp, i64, vp, sz, vp],
+                                             ctypes.c_int),
             }
             for name, (args, res) in sig.items():
                 f = getattr(L, name)
@@ -325,6 +338,80 @@ def exl3_pretransform(x, s_in, rin, u=None) -> torch.Tensor:
                                    _ptr(u, torch.float16, "u"), _stream(x.device)),
            "exl3_pretransform")
     return u
+
+
+# ------------------------------------------------------ 8-bit activations
+def exl3_linear_a8_workspace_bytes(max_M: int, max_IC: int, max_OC: int) -> int:
+    return int(lib().exl3_linear_a8_workspace_bytes(max_M, max_IC, max_OC))
+
+
+def exl3_quantize_a8(x, s_in, rin, A=None, As=None):
+    """Pre-transform and quantize x per row: (A uint8 [M, IC] codes q + 128, As fp32 [M])."""
+    IC = x.shape[-1]
+    M = x.numel() // IC
+    if A is None:
+        A = torch.empty((M, IC), dtype=torch.uint8, device=x.device)
+    if As is None:
+        As = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _check(lib().exl3_quantize_a8(_ptr(x, torch.bfloat16, "x"), M, IC, _ptr(s_in, torch.float16, "s_in"),
+                                  _ptr(rin, torch.float16, "rin"), _ptr(A, torch.uint8, "A"),
+                                  _ptr(As, torch.float32, "As"), _stream(x.device)), "exl3_quantize_a8")
+    return A, As
+
+
+def exl3_linear_into_a8(x: torch.Tensor, code: torch.Tensor, K: int, s_in, rin, rout, s_out,
+                        out: torch.Tensor, col0: int, ws: torch.Tensor) -> None:
+    """exl3_linear_into with the activations quantized to 8 bits per row."""
+    IC, OC = _linear_shapes(x, code, K)
+    M = x.numel() // IC
+    _check(lib().exl3_linear_into_a8(
+        _ptr(x, torch.bfloat16, "x"), M, IC, _ptr(code, torch.int16, "code"), OC, K,
+        _ptr(s_in, torch.float16, "s_in"), _ptr(rin, torch.float16, "rin"),
+        _ptr(rout, torch.float16, "rout"), _ptr(s_out, torch.float16, "s_out"),
+        _ptr(out, torch.bfloat16, "out"), out.shape[-1], col0, _ptr(ws, torch.uint8, "ws"), ws.numel(),
+        _stream(x.device)), "exl3_linear_into_a8")
+
+
+def exl3_gemm_a8_into(A: torch.Tensor, As: torch.Tensor, code: torch.Tensor, K: int, rout, s_out,
+                      out: torch.Tensor, col0: int, ws: torch.Tensor) -> None:
+    """Trellis GEMM + output transform of 8-bit activations (A, As from exl3_quantize_a8)."""
+    IC, OC = _linear_shapes(A, code, K)
+    M = A.numel() // IC
+    if As.numel() != M:
+        raise ValueError(f"As has {As.numel()} entries, A has {M} rows")
+    _check(lib().exl3_gemm_a8_into(
+        _ptr(A, torch.uint8, "A"), _ptr(As, torch.float32, "As"), M, IC, _ptr(code, torch.int16, "code"), OC, K,
+        _ptr(rout, torch.float16, "rout"), _ptr(s_out, torch.float16, "s_out"),
+        _ptr(out, torch.bfloat16, "out"), out.shape[-1], col0, _ptr(ws, torch.uint8, "ws"),
+        ws.numel(), _stream(A.device)), "exl3_gemm_a8_into")
+
+
+def exl3_linear_shards_a8_workspace_bytes(max_M: int, IC: int, shards) -> int:
+    return int(lib().exl3_linear_shards_a8_workspace_bytes(max_M, IC, _shard_array(shards, IC), len(shards)))
+
+
+def exl3_linear_into_shards_a8(x: torch.Tensor, shards, out: torch.Tensor, ws: torch.Tensor) -> None:
+    """exl3_linear_into_shards with 8-bit activations (each shard quantized with its own s_in, rin)."""
+    IC = x.shape[-1]
+    M = x.numel() // IC
+    arr, n = _shard_array(shards, IC), len(shards)
+    _check(lib().exl3_linear_into_shards_a8(_ptr(x, torch.bfloat16, "x"), M, IC, arr, n,
+                                            _ptr(out, torch.bfloat16, "out"), out.shape[-1],
+                                            _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(x.device)),
+           "exl3_linear_into_shards_a8")
+
+
+def exl3_gemm_a8_into_shards(A: torch.Tensor, As: torch.Tensor, shards, out: torch.Tensor, ws: torch.Tensor) -> None:
+    """Grouped GEMM on 8-bit activations A uint8 [n, M, IC], As fp32 [n, M]."""
+    IC = A.shape[-1]
+    arr, n = _shard_array(shards, IC), len(shards)
+    M = A.numel() // (IC * n)
+    if As.numel() != n * M:
+        raise ValueError(f"As has {As.numel()} entries, A has {n} x {M} rows")
+    _check(lib().exl3_gemm_a8_into_shards(_ptr(A, torch.uint8, "A"), _ptr(As, torch.float32, "As"), M, IC, arr, n,
+                                          _ptr(out, torch.bfloat16, "out"), out.shape[-1],
+                                          _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(A.device)),
+           "exl3_gemm_a8_into_shards")
 
 
 def exl3_reconstruct(code: torch.Tensor, K: int, W=None) -> torch.Tensor:

@@ -290,14 +290,19 @@ struct ShardDesc {
 
 // Trellis GEMM + epilogue for n shards whose pre-transformed activations sit
 // in u as [slot][M][IC] (fp16); shard i uses slot slots[i] (i if slots is null).
+// 8-bit activations: row_scale [slots][M] multiplies each output row; with
+// codes, u holds uint8 codes (q + 128, M <= 8 rows per decode pass) instead of
+// fp16 values.
 static exl3_status run_gemm(const char *fn, const uint16_t *u, int64_t M, int32_t IC, const ShardDesc *sh, int n,
                             uint16_t *out, int64_t ldo, const LinearWorkspace &ws, bool pdl, cudaStream_t s,
-                            const int *slots = nullptr) {
+                            const int *slots = nullptr, const float *row_scale = nullptr, bool codes = false) {
     cudaError_t e;
     auto slot = [&](int i) { return slots ? slots[i] : i; };
     const GemmMode mode = gemm_mode(M);
+    if (codes && mode != GemmMode::kDecode) return fail(EXL3_EINVAL, "%s: 8-bit codes need the decode path", fn);
     if (mode == GemmMode::kFused) {
         FusedArgs a = {};
+        a.row_scale = row_scale;
         a.n_shards = n;
         a.M = (int32_t)M;
         a.IC = IC;
@@ -330,20 +335,25 @@ static exl3_status run_gemm(const char *fn, const uint16_t *u, int64_t M, int32_
             e = launch_reconstruct(sh[i].code, IC, sh[i].OC, sh[i].K, ws.wt, /*transposed=*/true, s);
             if (e != cudaSuccess) return cuda_fail(e, fn);
             e = launch_prefill(u + (int64_t)slot(i) * M * IC, ws.wt, M, IC, sh[i].OC, sh[i].rout, sh[i].s_out,
-                               out + sh[i].col0, ldo, ws.err, s, &launched);
+                               out + sh[i].col0, ldo, ws.err, s, &launched, 0,
+                               row_scale ? row_scale + (int64_t)slot(i) * M : nullptr);
             if (e != cudaSuccess) return cuda_fail(e, fn);
             if (!launched) return fail(EXL3_EUNSUPPORTED, "%s: prefill path unavailable", fn);
         }
         trace("%s M=%lld IC=%d shards=%d mode=prefill", fn, (long long)M, IC, n);
         return EXL3_OK;
     }
-    // decode mode: passes of up to kDecodeMaxRows rows, all shards in one launch per pass
-    for (int64_t r0 = 0; r0 < M; r0 += kDecodeMaxRows) {
-        const int rows = (int)((M - r0) < kDecodeMaxRows ? (M - r0) : kDecodeMaxRows);
+    // decode mode: passes of up to kDecodeMaxRows rows (8 with codes), all shards in
+    // one launch per pass
+    const int64_t pass_rows = codes ? 8 : kDecodeMaxRows;
+    for (int64_t r0 = 0; r0 < M; r0 += pass_rows) {
+        const int rows = (int)((M - r0) < pass_rows ? (M - r0) : pass_rows);
         GroupGemmArgs a = {};
         a.u = u;
         a.IC = IC;
         a.mode = kModeDense;
+        a.codes = codes ? 1 : 0;
+        a.row_scale = row_scale;
         a.n_inline = n;
         int g0 = 0;
         for (int i = 0; i < n; i++) {
@@ -416,6 +426,98 @@ exl3_status exl3_gemm_into(const uint16_t *u, int64_t M, int32_t IC, const int16
     return run_gemm("gemm_into", u, M, IC, &d, 1, out, ldo, ws, false, (cudaStream_t)stream);
 }
 
+// ---------------------------------------------------------------- 8-bit activations
+// Workspace: the linear layout, then As [max_M] (fp32).  M <= 8 rows on the
+// decode path keep the uint8 codes in the activation region; other paths keep
+// the codes' exact fp16 values there.
+static size_t a8_layout(int64_t max_M, int32_t IC, int32_t OC, LinearWorkspace *ws, void *base, float **As) {
+    const size_t off = linear_workspace_layout(max_M, IC, OC, ws, base);
+    if (!off) return 0;
+    if (As) *As = reinterpret_cast<float *>(static_cast<char *>(base) + off);
+    return off + align256((size_t)max_M * sizeof(float));
+}
+
+size_t exl3_linear_a8_workspace_bytes(int64_t max_M, int32_t max_IC, int32_t max_OC) {
+    if (!exl3_linear_workspace_bytes(max_M, max_IC, max_OC)) return 0;
+    return a8_layout(max_M, max_IC, max_OC, nullptr, nullptr, nullptr);
+}
+
+static exl3_status check_a8_ic(const char *fn, int32_t IC) {
+    const size_t smem = quantize_a8_smem_bytes(IC);
+    if (smem + 1024 > (size_t)device_info().max_smem_optin)
+        return fail(EXL3_EUNSUPPORTED, "%s: IC = %d needs %zu bytes of shared memory per row (%d available)", fn, IC,
+                    smem, device_info().max_smem_optin);
+    return EXL3_OK;
+}
+
+exl3_status exl3_quantize_a8(const uint16_t *x, int64_t M, int32_t IC, const uint16_t *s_in, const uint16_t *rin,
+                             uint8_t *A, float *As, exl3_stream stream) {
+    if (M < 0 || IC <= 0 || IC % 128)
+        return fail(EXL3_EINVAL, "quantize_a8: M = %lld, IC = %d (IC must be a positive multiple of 128)",
+                    (long long)M, IC);
+    if (M == 0) return EXL3_OK;
+    if (!x || !s_in || !rin || !A || !As) return fail(EXL3_EINVAL, "quantize_a8: null pointer");
+    if (((uintptr_t)x | (uintptr_t)s_in | (uintptr_t)rin) & 7u || ((uintptr_t)A | (uintptr_t)As) & 3u)
+        return fail(EXL3_EINVAL, "quantize_a8: x, s_in, rin must be 8-byte aligned and A, As 4-byte aligned");
+    exl3_status st = check_a8_ic("quantize_a8", IC);
+    if (st != EXL3_OK) return st;
+    PretransformShards p = {};
+    p.s_in[0] = s_in;
+    p.rin[0] = rin;
+    p.n = 1;
+    cudaError_t e = launch_quantize_a8(x, M, IC, p, A, false, As, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize_a8");
+    return EXL3_OK;
+}
+
+exl3_status exl3_linear_into_a8(const uint16_t *x, int64_t M, int32_t IC, const int16_t *code, int32_t OC,
+                                int32_t K, const uint16_t *s_in, const uint16_t *rin, const uint16_t *rout,
+                                const uint16_t *s_out, uint16_t *out, int64_t ldo, int64_t col0, void *wsp,
+                                size_t ws_bytes, exl3_stream stream) {
+    exl3_status st = check_linear_args("linear_into_a8", x, M, IC, code, OC, K, s_in, rin, rout, s_out);
+    if (st == EXL3_OK)
+        st = check_out_ws("linear_into_a8", M, OC, out, ldo, col0, wsp, ws_bytes,
+                          exl3_linear_a8_workspace_bytes(M, IC, OC));
+    if (st == EXL3_OK && M > 0) st = check_a8_ic("linear_into_a8", IC);
+    if (st != EXL3_OK || M == 0) return st;
+    LinearWorkspace ws;
+    float *As = nullptr;
+    a8_layout(M, IC, OC, &ws, wsp, &As);
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool codes = gemm_mode(M) == GemmMode::kDecode && M <= 8;
+    PretransformShards p = {};
+    p.s_in[0] = s_in;
+    p.rin[0] = rin;
+    p.n = 1;
+    cudaError_t e = launch_quantize_a8(x, M, IC, p, ws.u, !codes, As, s);
+    if (e != cudaSuccess) return cuda_fail(e, "linear_into_a8: quantize");
+    ShardDesc d = {code, s_in, rin, rout, s_out, OC, K, col0};
+    return run_gemm("linear_into_a8", ws.u, M, IC, &d, 1, out, ldo, ws, true, s, nullptr, As, codes);
+}
+
+exl3_status exl3_gemm_a8_into(const uint8_t *A, const float *As, int64_t M, int32_t IC, const int16_t *code,
+                              int32_t OC, int32_t K, const uint16_t *rout, const uint16_t *s_out, uint16_t *out,
+                              int64_t ldo, int64_t col0, void *wsp, size_t ws_bytes, exl3_stream stream) {
+    exl3_status st = check_linear_args("gemm_a8_into", reinterpret_cast<const uint16_t *>(A), M, IC, code, OC, K,
+                                       rout, rout, rout, s_out);
+    if (st == EXL3_OK && M > 0 && (!As || ((uintptr_t)As & 3u)))
+        return fail(EXL3_EINVAL, "gemm_a8_into: As (%p) must be a non-null 4-byte aligned pointer", (const void *)As);
+    if (st == EXL3_OK)
+        st = check_out_ws("gemm_a8_into", M, OC, out, ldo, col0, wsp, ws_bytes,
+                          exl3_linear_a8_workspace_bytes(M, IC, OC));
+    if (st != EXL3_OK || M == 0) return st;
+    LinearWorkspace ws;
+    a8_layout(M, IC, OC, &ws, wsp, nullptr);
+    cudaStream_t s = (cudaStream_t)stream;
+    ShardDesc d = {code, nullptr, nullptr, rout, s_out, OC, K, col0};
+    if (gemm_mode(M) == GemmMode::kDecode && M <= 8)
+        return run_gemm("gemm_a8_into", reinterpret_cast<const uint16_t *>(A), M, IC, &d, 1, out, ldo, ws, false, s,
+                        nullptr, As, true);
+    cudaError_t e = launch_codes_to_f16(A, M * IC, ws.u, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm_a8_into: codes");
+    return run_gemm("gemm_a8_into", ws.u, M, IC, &d, 1, out, ldo, ws, true, s, nullptr, As, false);
+}
+
 static bool shards_shape(const exl3_shard *shards, int32_t n, int *groups, int32_t *max_oc) {
     if (!shards || n < 1 || n > kMaxInlineEntries) return false;
     *groups = 0;
@@ -483,6 +585,60 @@ exl3_status exl3_gemm_into_shards(const uint16_t *u, int64_t M, int32_t IC, cons
     exl3_status st = shards_prepare("gemm_into_shards", u, M, IC, shards, n, out, ldo, wsp, ws_bytes, false, d, &ws);
     if (st != EXL3_OK || M == 0) return st;
     return run_gemm("gemm_into_shards", u, M, IC, d, n, out, ldo, ws, false, (cudaStream_t)stream);
+}
+
+size_t exl3_linear_shards_a8_workspace_bytes(int64_t max_M, int32_t IC, const exl3_shard *shards, int32_t n) {
+    const size_t b = exl3_linear_shards_workspace_bytes(max_M, IC, shards, n);
+    return b ? b + align256((size_t)n * max_M * sizeof(float)) : 0;
+}
+
+exl3_status exl3_linear_into_shards_a8(const uint16_t *x, int64_t M, int32_t IC, const exl3_shard *shards,
+                                       int32_t n, uint16_t *out, int64_t ldo, void *wsp, size_t ws_bytes,
+                                       exl3_stream stream) {
+    ShardDesc d[kMaxInlineEntries];
+    LinearWorkspace ws;
+    exl3_status st = shards_prepare("linear_into_shards_a8", x, M, IC, shards, n, out, ldo, wsp, ws_bytes, true, d,
+                                    &ws);
+    if (st == EXL3_OK && M > 0 && ws_bytes < exl3_linear_shards_a8_workspace_bytes(M, IC, shards, n))
+        st = fail(EXL3_EWORKSPACE, "linear_into_shards_a8: workspace of %zu bytes; this call needs %zu bytes",
+                  ws_bytes, exl3_linear_shards_a8_workspace_bytes(M, IC, shards, n));
+    if (st == EXL3_OK && M > 0) st = check_a8_ic("linear_into_shards_a8", IC);
+    if (st != EXL3_OK || M == 0) return st;
+    float *As = reinterpret_cast<float *>(static_cast<char *>(wsp) + exl3_linear_shards_workspace_bytes(M, IC, shards, n));
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool codes = gemm_mode(M) == GemmMode::kDecode && M <= 8;
+    PretransformShards p = {};
+    p.n = n;
+    for (int i = 0; i < n; i++) {
+        p.s_in[i] = d[i].s_in;
+        p.rin[i] = d[i].rin;
+    }
+    cudaError_t e = launch_quantize_a8(x, M, IC, p, ws.u, !codes, As, s);
+    if (e != cudaSuccess) return cuda_fail(e, "linear_into_shards_a8: quantize");
+    return run_gemm("linear_into_shards_a8", ws.u, M, IC, d, n, out, ldo, ws, true, s, nullptr, As, codes);
+}
+
+exl3_status exl3_gemm_a8_into_shards(const uint8_t *A, const float *As, int64_t M, int32_t IC,
+                                     const exl3_shard *shards, int32_t n, uint16_t *out, int64_t ldo, void *wsp,
+                                     size_t ws_bytes, exl3_stream stream) {
+    ShardDesc d[kMaxInlineEntries];
+    LinearWorkspace ws;
+    exl3_status st = shards_prepare("gemm_a8_into_shards", reinterpret_cast<const uint16_t *>(A), M, IC, shards, n,
+                                    out, ldo, wsp, ws_bytes, false, d, &ws);
+    if (st == EXL3_OK && M > 0 && (!As || ((uintptr_t)As & 3u)))
+        st = fail(EXL3_EINVAL, "gemm_a8_into_shards: As (%p) must be a non-null 4-byte aligned pointer",
+                  (const void *)As);
+    if (st == EXL3_OK && M > 0 && ws_bytes < exl3_linear_shards_a8_workspace_bytes(M, IC, shards, n))
+        st = fail(EXL3_EWORKSPACE, "gemm_a8_into_shards: workspace of %zu bytes; this call needs %zu bytes",
+                  ws_bytes, exl3_linear_shards_a8_workspace_bytes(M, IC, shards, n));
+    if (st != EXL3_OK || M == 0) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (gemm_mode(M) == GemmMode::kDecode && M <= 8)
+        return run_gemm("gemm_a8_into_shards", reinterpret_cast<const uint16_t *>(A), M, IC, d, n, out, ldo, ws, false,
+                        s, nullptr, As, true);
+    cudaError_t e = launch_codes_to_f16(A, (int64_t)n * M * IC, ws.u, s);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm_a8_into_shards: codes");
+    return run_gemm("gemm_a8_into_shards", ws.u, M, IC, d, n, out, ldo, ws, true, s, nullptr, As, false);
 }
 
 exl3_status exl3_linear(const uint16_t *x, int64_t M, int32_t IC, const int16_t *code, int32_t OC, int32_t K,

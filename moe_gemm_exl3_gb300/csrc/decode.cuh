@@ -1,5 +1,6 @@
-// decode.cuh -- the register-resident trellis decode + mma.sync core shared by
-// the decode-mode GEMM (linear.cu) and the one-launch MoE layer (moe_fused.cu).
+// decode.cuh -- the register-resident trellis decode + mma.sync core of the
+// decode-mode GEMM (linear.cu): dense projections, the grouped MoE GEMMs and the
+// 8-bit activation variant.
 #pragma once
 
 #include "common.cuh"
@@ -36,7 +37,22 @@ constexpr size_t group_smem_bytes() {
 //             r0 = e.u_row0 - j * R_half): activations stored per (token, route)
 //             pair rather than per routed row
 //   kUShared  shared memory: row g, channels [c0s, c0s + nch) at su[g * nch + c - c0s]
-enum USrc { kUGlobal = 0, kUGather = 1, kUShared = 2 };
+//   kUCodes   8-bit activation codes (uint8 q + 128, rows e.u_row0 + g of u read
+//             as bytes); the MMA multiplies q exactly, the row scale is applied by
+//             the epilogue
+enum USrc { kUGlobal = 0, kUGather = 1, kUShared = 2, kUCodes = 3 };
+
+// Four 8-bit activation codes (q + 128) -> each q (exact) duplicated into a half2.
+__device__ __forceinline__ void codes_to_dup_f16(uint32_t w, uint32_t (&b)[4]) {
+    const __half2 off = __half2half2(__ushort_as_half(0x6480));   // 1152 = 1024 + 128
+    const uint32_t sel[4] = {0x4040u, 0x4141u, 0x4242u, 0x4343u};
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const uint32_t h = __byte_perm(w, 0x64646464u, sel[i]);   // fp16 1024 + code, twice
+        const __half2 r = __hsub2(*reinterpret_cast<const __half2 *>(&h), off);
+        b[i] = *reinterpret_cast<const uint32_t *>(&r);
+    }
+}
 
 template <int K, int NB, int USRC = kUGlobal>
 __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const GroupEntry &e, const uint16_t *u,
@@ -44,7 +60,7 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
                                                  uint32_t hx, const uint32_t *pow2,
                                                  const int32_t *gather_rows = nullptr, int R_half = 0,
                                                  const uint16_t *su = nullptr, int nch = 0, int c0s = 0) {
-    static_assert(USRC == kUGlobal || NB == 1, "gathered and shared activation rows serve one 8-row block");
+    static_assert(USRC == kUGlobal || NB == 1, "gathered, shared and 8-bit activation rows serve one 8-row block");
     const int g = lane >> 2, q = lane & 3;
     const int TO = e.OC / kTile;
     const uint32_t *tile0 = reinterpret_cast<const uint32_t *>(e.code) + (int64_t)(8 * G + g) * 8 * K + q * 2 * K;
@@ -102,15 +118,22 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
             const int j = e.u_row0 >= R_half ? 1 : 0;
             urow_index = urow ? (int64_t)j * R_half + gather_rows[e.u_row0 - j * R_half + g] : 0;
         }
+        // codes: one byte per channel, addressed through the same pointer type (in
+        // units of two channels, hence the halved offsets)
         const uint16_t *up = USRC == kUShared ? su + g * nch + 16 * ar + 4 * q - c0s
+                           : USRC == kUCodes  ? reinterpret_cast<const uint16_t *>(
+                                                    reinterpret_cast<const uint8_t *>(u) + urow_index * IC + 16 * ar + 4 * q)
                                               : u + urow_index * IC + 16 * ar + 4 * q;
-        constexpr int kUS = 16 * kDecodeWarps;   // activation step (channels) per warp step
+        constexpr int kUS = (USRC == kUCodes ? 8 : 16) * kDecodeWarps;   // activation step per warp step
         auto ldu = [&](const uint16_t *pu) -> uint2 {
             if constexpr (USRC == kUShared) return *reinterpret_cast<const uint2 *>(pu);
+            else if constexpr (USRC == kUCodes) return make_uint2(__ldg(reinterpret_cast<const uint32_t *>(pu)), 0u);
             else return __ldg(reinterpret_cast<const uint2 *>(pu));
         };
         uint32_t wa[2 * K], wb[2 * K];
-        uint2 ua = make_uint2(0u, 0u), ubv = make_uint2(0u, 0u);
+        // rows past the entry multiply zeros (codes: 128 is q = 0)
+        const uint32_t zero = USRC == kUCodes ? 0x80808080u : 0u;
+        uint2 ua = make_uint2(zero, zero), ubv = make_uint2(zero, zero);
         load_quarter<K>(wa, p);
         if (urow) ua = ldu(up);
         if (n > 1) {
@@ -120,7 +143,15 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
         auto row = [&](uint32_t (&w)[2 * K], uint2 &uv, bool refill, const uint32_t *pn, const uint16_t *upn) {
             QuarterStream<K> st;
             st.build(w, quarter_prev_word(w[2 * K - 1], lane));
-            uint32_t b[NB][4] = {{dup_half_lo(uv.x), dup_half_hi(uv.x), dup_half_lo(uv.y), dup_half_hi(uv.y)}};
+            uint32_t b[NB][4];
+            if constexpr (USRC == kUCodes) {
+                codes_to_dup_f16(uv.x, b[0]);
+            } else {
+                b[0][0] = dup_half_lo(uv.x);
+                b[0][1] = dup_half_hi(uv.x);
+                b[0][2] = dup_half_lo(uv.y);
+                b[0][3] = dup_half_hi(uv.y);
+            }
             if (refill) {
                 load_quarter<K>(w, pn);
                 if (urow) uv = ldu(upn);

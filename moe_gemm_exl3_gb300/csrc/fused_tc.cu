@@ -602,6 +602,8 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                         }
                     } else {
                         uint16_t *dst = a.out + (int64_t)nrow * a.ldo + d.out0 + colb;
+                        // the Hadamard scale, times the row's activation scale when there is one
+                        const float hn = a.row_scale ? kHadNorm * __ldg(a.row_scale + d.u_row + nrow) : kHadNorm;
 #pragma unroll
                         for (int jj = 0; jj < 8; jj++) {
                             const int cl = 4 * part + 16 * jj;     // column within the block
@@ -611,8 +613,8 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                             uint32_t o2[2];
 #pragma unroll
                             for (int h = 0; h < 2; h++) {
-                                float y0 = (x[jj + 16 * h] * kHadNorm) * f16_bits_to_f32((uint16_t)(rw[h] & 0xFFFFu));
-                                float y1 = (x[jj + 16 * h + 8] * kHadNorm) * f16_bits_to_f32((uint16_t)(rw[h] >> 16));
+                                float y0 = (x[jj + 16 * h] * hn) * f16_bits_to_f32((uint16_t)(rw[h] & 0xFFFFu));
+                                float y1 = (x[jj + 16 * h + 8] * hn) * f16_bits_to_f32((uint16_t)(rw[h] >> 16));
                                 y0 *= f16_bits_to_f32((uint16_t)(sw[h] & 0xFFFFu));
                                 y1 *= f16_bits_to_f32((uint16_t)(sw[h] >> 16));
                                 o2[h] = (uint32_t)f32_to_bf16_bits(y0) | ((uint32_t)f32_to_bf16_bits(y1) << 16);

@@ -76,7 +76,7 @@ enum GroupMode : int32_t {
 };
 
 struct GroupGemmArgs {
-    const uint16_t *u;            // fp16 activations, row stride IC
+    const uint16_t *u;            // fp16 activations, row stride IC (or 8-bit codes, below)
     int IC;
     int mode;
     const GroupEntry *entries;    // device array (MoE) or nullptr (use inline)
@@ -108,6 +108,11 @@ struct GroupGemmArgs {
     const int32_t *comb_pos;
     uint16_t *comb_y;
     int32_t *comb_counters;       // [T][OC / 128], zero between calls
+    // 8-bit activations: u holds uint8 codes q + 128 (row stride IC bytes); the
+    // epilogue multiplies row r = e.u_row0 + n by row_scale[r] (non-null only
+    // then; one 8-row block per entry)
+    int32_t codes;
+    const float *row_scale;
 };
 constexpr int kMaxInlineEntries = 4;
 
@@ -151,6 +156,9 @@ struct FusedArgs {
     int32_t *err;
     uint32_t hash_xor;
     uint32_t pow2[17];
+    // dense mode, 8-bit activations: output row r of shard s is scaled by
+    // row_scale[u_slot * M + r] (u then holds the codes' exact fp16 values)
+    const float *row_scale;
 };
 bool fused_supported();
 size_t fused_slab_floats(int max_groups, int64_t rows);
@@ -168,9 +176,22 @@ int forced_mode();
 bool prefill_supported();
 // epi 0: the EXL3 output transform (OC a multiple of 128); epi 1: a per-column
 // scale rout, no transform (any OC).
+// row_scale (epi 0 only, may be null): output row m is scaled by row_scale[m].
 cudaError_t launch_prefill(const uint16_t *u, const uint16_t *wt, int64_t M, int IC, int OC,
                            const uint16_t *rout, const uint16_t *s_out, uint16_t *out,
-                           int64_t ldo, int32_t *err, cudaStream_t s, bool *launched, int epi = 0);
+                           int64_t ldo, int32_t *err, cudaStream_t s, bool *launched, int epi = 0,
+                           const float *row_scale = nullptr);
+
+// 8-bit activations.  Pre-transform (once per shard, as launch_pretransform_shards)
+// plus per-row quantization of x [M][IC]: row r = shard * M + m of dst and As,
+// As[r] = amax_r / 127, q = round-half-even(u / As) clamped to [-127, 127];
+// f16_out = false: codes q + 128 into dst as uint8 [n * M][IC]; true: q as exact
+// fp16 into dst as uint16 [n * M][IC].  IC * 4 bytes of shared memory per row.
+cudaError_t launch_quantize_a8(const uint16_t *x, int64_t M, int IC, const PretransformShards &p, void *dst,
+                               bool f16_out, float *As, cudaStream_t s);
+size_t quantize_a8_smem_bytes(int IC);
+// uint8 codes [n] -> q = code - 128 as exact fp16 (n a multiple of 8, both 16-byte aligned).
+cudaError_t launch_codes_to_f16(const uint8_t *A, int64_t n, uint16_t *dst, cudaStream_t s);
 
 // int8 output head, few rows (M <= 32), x16 the fp16 activations: ctr = two
 // zeroed workspace counters.

@@ -201,9 +201,11 @@ __device__ __forceinline__ void grid_dependency_wait() {
 
 // KSET: bit k set = the launch may contain entries of bitrate k (2, 3, 4); only
 // those decode paths are compiled into the kernel, which keeps registers low.
-template <int NB, int KSET, bool GATHER = false>
+// USRC: where the activation rows come from (kUGlobal, kUGather or kUCodes; see
+// group_accumulate).
+template <int NB, int KSET, int USRC = kUGlobal>
 __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(const GroupGemmArgs a) {
-    static_assert(!GATHER || NB == 1, "gathered activation rows serve one 8-row block per entry");
+    static_assert(USRC == kUGlobal || NB == 1, "gathered and 8-bit activation rows serve one 8-row block per entry");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     constexpr int FRAG = 8 * NB * 4 * 32;
     float *red = reinterpret_cast<float *>(smem_raw);                   // [warps][FRAG]
@@ -275,18 +277,12 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
             for (int nb = 0; nb < NB; nb++)
 #pragma unroll
                 for (int r = 0; r < 4; r++) acc[j][nb][r] = 0.f;
-        if constexpr (GATHER) {
-            if ((KSET & 4) && e.K == 2)
-                group_accumulate<2, NB, kUGather>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
-            if ((KSET & 8) && e.K == 3)
-                group_accumulate<3, NB, kUGather>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
-            if ((KSET & 16) && e.K == 4)
-                group_accumulate<4, NB, kUGather>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
-        } else {
-            if ((KSET & 4) && e.K == 2) group_accumulate<2, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2);
-            if ((KSET & 8) && e.K == 3) group_accumulate<3, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2);
-            if ((KSET & 16) && e.K == 4) group_accumulate<4, NB>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2);
-        }
+        if ((KSET & 4) && e.K == 2)
+            group_accumulate<2, NB, USRC>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+        if ((KSET & 8) && e.K == 3)
+            group_accumulate<3, NB, USRC>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+        if ((KSET & 16) && e.K == 4)
+            group_accumulate<4, NB, USRC>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
 
         // ---- CTA reduction in fixed warp order (fragment order, one barrier)
 #pragma unroll
@@ -364,11 +360,13 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
 #pragma unroll
                 for (int i = 0; i < 4; i++) v[i] = red[frag_index<NB>(n, 4 * lane + i)];
                 warp_fwht128(v, lane);
+                // the Hadamard scale, times the row's activation scale when there is one
+                const float hn = a.row_scale ? kHadNorm * __ldg(a.row_scale + e.u_row0 + n) : kHadNorm;
                 float y[4];
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
                     const int h = i >> 1, sh = 16 * (i & 1);
-                    y[i] = (v[i] * kHadNorm) * f16_bits_to_f32((uint16_t)(rs[h] >> sh));
+                    y[i] = (v[i] * hn) * f16_bits_to_f32((uint16_t)(rs[h] >> sh));
                     if (a.mode == kModeDense) y[i] *= f16_bits_to_f32((uint16_t)(ss[h] >> sh));
                 }
                 if (a.mode == kModeDense) {
@@ -419,11 +417,11 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
     }
 }
 
-template <int NB, int KSET, bool GATHER = false>
+template <int NB, int KSET, int USRC = kUGlobal>
 static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t total_hint, cudaStream_t s) {
     constexpr size_t smem = group_smem_bytes<NB>();
     int occ = 1;
-    cudaError_t e = kernel_occupancy((const void *)group_gemm_kernel<NB, KSET, GATHER>, 256, smem, &occ);
+    cudaError_t e = kernel_occupancy((const void *)group_gemm_kernel<NB, KSET, USRC>, 256, smem, &occ);
     if (e != cudaSuccess) return e;
     GroupGemmArgs a = a0;
     a.hash_xor = kHashXor;
@@ -454,7 +452,7 @@ static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t tot
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, group_gemm_kernel<NB, KSET, GATHER>, a);
+    return cudaLaunchKernelEx(&cfg, group_gemm_kernel<NB, KSET, USRC>, a);
 }
 
 template <int NB>
@@ -487,8 +485,18 @@ cudaError_t launch_group_gemm(const GroupGemmArgs &a, int nb, bool pdl, cudaStre
     }
     if (a.gather) {
         // grouped MoE with activation rows stored per pair: one 8-row block per entry, any K
+        if (nb != 1 || a.codes) return cudaErrorInvalidValue;
+        return launch_group_t<1, 28, kUGather>(a, pdl, total, s);
+    }
+    if (a.codes) {
+        // 8-bit activation codes: one 8-row block per entry
         if (nb != 1) return cudaErrorInvalidValue;
-        return launch_group_t<1, 28, true>(a, pdl, total, s);
+        switch (kset) {
+            case 4: return launch_group_t<1, 4, kUCodes>(a, pdl, total, s);
+            case 8: return launch_group_t<1, 8, kUCodes>(a, pdl, total, s);
+            case 16: return launch_group_t<1, 16, kUCodes>(a, pdl, total, s);
+            default: return launch_group_t<1, 28, kUCodes>(a, pdl, total, s);
+        }
     }
     if (nb == 3) nb = 4;
     switch (nb) {

@@ -56,7 +56,7 @@ template <int EPI>
 __global__ void __launch_bounds__(192, 1)
 prefill_gemm_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_w,
                     int M, int IC, int OC, const uint16_t *__restrict__ rout, const uint16_t *__restrict__ s_out,
-                    uint16_t *__restrict__ out, int64_t ldo, int32_t *err) {
+                    uint16_t *__restrict__ out, int64_t ldo, int32_t *err, const float *__restrict__ row_scale) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte alignment for the swizzled tiles
     const uint32_t raw = smem_u32(smem_raw);
@@ -171,6 +171,8 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_const
                 tmem_ld_wait();
                 if (m >= M) continue;
                 uint16_t *dst = out + (int64_t)m * ldo + col;
+                // the Hadamard scale, times the row's activation scale when there is one
+                const float hn = row_scale ? kHadNorm * __ldg(row_scale + m) : kHadNorm;
                 if constexpr (EPI == 1) {
                     // per-column scale, no transform; a partial last block stores its columns one by one
                     const int ncol = OC - col < kHad ? OC - col : kHad;
@@ -218,8 +220,8 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_const
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
                         const int c = c8 * 8 + 2 * q;
-                        float y0 = (v[c] * kHadNorm) * f16_bits_to_f32((uint16_t)(rw[q] & 0xFFFFu));
-                        float y1 = (v[c + 1] * kHadNorm) * f16_bits_to_f32((uint16_t)(rw[q] >> 16));
+                        float y0 = (v[c] * hn) * f16_bits_to_f32((uint16_t)(rw[q] & 0xFFFFu));
+                        float y1 = (v[c + 1] * hn) * f16_bits_to_f32((uint16_t)(rw[q] >> 16));
                         y0 *= f16_bits_to_f32((uint16_t)(sw[q] & 0xFFFFu));
                         y1 *= f16_bits_to_f32((uint16_t)(sw[q] >> 16));
                         o[q] = (uint32_t)f32_to_bf16_bits(y0) | ((uint32_t)f32_to_bf16_bits(y1) << 16);
@@ -256,9 +258,10 @@ bool prefill_supported() { return tma_encode_available(); }
 
 cudaError_t launch_prefill(const uint16_t *u, const uint16_t *wt, int64_t M, int IC, int OC, const uint16_t *rout,
                            const uint16_t *s_out, uint16_t *out, int64_t ldo, int32_t *err, cudaStream_t s,
-                           bool *launched, int epi) {
+                           bool *launched, int epi, const float *row_scale) {
     *launched = false;
-    if (M <= 0 || IC % BK || (epi == 0 && OC % kHad) || M > INT32_MAX) return cudaErrorInvalidValue;
+    if (M <= 0 || IC % BK || (epi == 0 && OC % kHad) || M > INT32_MAX || (epi != 0 && row_scale))
+        return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(u) | reinterpret_cast<uintptr_t>(wt)) & 15u) return cudaErrorInvalidValue;
     CUtensorMap tm_u, tm_w;
     if (!make_map_f16(&tm_u, u, M, IC, BM) || !make_map_f16(&tm_w, wt, OC, IC, BN)) return cudaErrorInvalidValue;
@@ -270,10 +273,10 @@ cudaError_t launch_prefill(const uint16_t *u, const uint16_t *wt, int64_t M, int
     if (grid > tiles) grid = tiles;
     if (epi == 0)
         prefill_gemm_kernel<0><<<(unsigned)grid, 192, SMEM_BYTES, s>>>(tm_u, tm_w, (int)M, IC, OC, rout, s_out, out,
-                                                                       ldo, err);
+                                                                       ldo, err, row_scale);
     else
         prefill_gemm_kernel<1><<<(unsigned)grid, 192, SMEM_BYTES, s>>>(tm_u, tm_w, (int)M, IC, OC, rout, s_out, out,
-                                                                       ldo, err);
+                                                                       ldo, err, nullptr);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) *launched = true;
     return e;
