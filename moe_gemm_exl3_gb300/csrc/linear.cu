@@ -11,70 +11,127 @@ namespace exl3 {
 // --------------------------------------------------------------------------
 // Activation pre-transform: u = Had128((x * s_in) * rin) per 128-channel
 // block (radiance_escha.py, module docstring "THE FORWARD", first factor).
-// One warp per (shard, row, run of bpw <= kPtRun consecutive blocks); lane l
-// holds channels 4l..4l+3 of a block.  A warp issues the loads of its whole run
-// before transforming it, so large calls keep enough bytes in flight; small
-// calls use runs of one block (more warps, shorter latency).
+// Eight lanes serve one block, 16 consecutive channels each (32-byte loads and
+// stores); a warp covers four blocks of the flattened (shard, row, block)
+// order per step and kPtSteps steps, issuing all of its loads first.  The
+// transform: four register stages over a lane's 16 channels (index bits 0..3),
+// three shuffle stages across the 8-lane group (bits 4..6).
 // --------------------------------------------------------------------------
-constexpr int kPtRun = 4;
+constexpr int kPtSteps = 2;
 
+// 16 consecutive 16-bit values: two 16-byte loads when V16, else four 8-byte loads
+// (scale vectors and the pre-transform's own arguments need only 8-byte alignment)
+template <bool V16>
+__device__ __forceinline__ void load16(uint4 (&v)[2], const uint16_t *p) {
+    if constexpr (V16) {
+        v[0] = __ldg(reinterpret_cast<const uint4 *>(p));
+        v[1] = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
+    } else {
+        const uint2 a = __ldg(reinterpret_cast<const uint2 *>(p)), b = __ldg(reinterpret_cast<const uint2 *>(p) + 1);
+        const uint2 c = __ldg(reinterpret_cast<const uint2 *>(p) + 2), d = __ldg(reinterpret_cast<const uint2 *>(p) + 3);
+        v[0] = make_uint4(a.x, a.y, b.x, b.y);
+        v[1] = make_uint4(c.x, c.y, d.x, d.y);
+    }
+}
+
+// V16: x and u are 16-byte aligned (16-byte loads and stores of the activations)
+template <bool V16>
 __global__ void __launch_bounds__(256) pretransform_kernel(const uint16_t *__restrict__ x,
                                                            int64_t M, int IC,
                                                            const __grid_constant__ PretransformShards p,
-                                                           uint16_t *__restrict__ u, int bpw) {
+                                                           uint16_t *__restrict__ u, int steps) {
     // let a dependent launch (the GEMM that reads u) get scheduled early; it
     // still waits for this grid to finish before touching u
     asm volatile("griddepcontrol.launch_dependents;");
     // this launch may itself start before the preceding kernel has finished (a
     // programmatic dependent launch): wait for it before reading x or writing u
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, sub = lane & 7;
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int blocks = IC / kHad;
-    const int runs = (blocks + bpw - 1) / bpw;
-    if (wid >= (int64_t)p.n * M * runs) return;
-    const int sh = (int)(wid / (M * runs));
-    const int64_t rem = wid % (M * runs);
-    const int64_t m = rem / runs;
-    const int b0 = (int)(rem % runs) * bpw;
-    uint2 xv[kPtRun], sv[kPtRun], rv[kPtRun];
+    const int nb = IC / kHad;
+    const int64_t total = (int64_t)p.n * M * nb;
+    uint4 xv[kPtSteps][2], sv[kPtSteps][2], rv[kPtSteps][2];
+    int64_t row[kPtSteps];
+    int c0[kPtSteps];
 #pragma unroll
-    for (int k = 0; k < kPtRun; k++) {
-        if (k < bpw && b0 + k < blocks) {
-            const int c0 = (b0 + k) * kHad + 4 * lane;
-            xv[k] = *reinterpret_cast<const uint2 *>(x + m * IC + c0);
-            sv[k] = __ldg(reinterpret_cast<const uint2 *>(p.s_in[sh] + c0));
-            rv[k] = __ldg(reinterpret_cast<const uint2 *>(p.rin[sh] + c0));
+    for (int k = 0; k < kPtSteps; k++) {
+        const int64_t B = (wid * steps + k) * 4 + (lane >> 3);   // this lane group's block
+        row[k] = -1;
+        if (k < steps && B < total) {
+            const int64_t r = B / nb;                 // shard * M + m
+            const int sh = (int)(r / M);
+            c0[k] = (int)(B - r * nb) * kHad + 16 * sub;
+            row[k] = r;
+            load16<V16>(xv[k], x + (r - sh * M) * IC + c0[k]);
+            load16<false>(sv[k], p.s_in[sh] + c0[k]);
+            load16<false>(rv[k], p.rin[sh] + c0[k]);
         }
     }
 #pragma unroll
-    for (int k = 0; k < kPtRun; k++) {
-        if (!(k < bpw && b0 + k < blocks)) break;   // warp-uniform
-        const int c0 = (b0 + k) * kHad + 4 * lane;
-        const uint32_t xs[2] = {xv[k].x, xv[k].y}, ss[2] = {sv[k].x, sv[k].y}, rs[2] = {rv[k].x, rv[k].y};
-        float v[4];
+    for (int k = 0; k < kPtSteps; k++) {
+        if (k >= steps) break;                       // warp-uniform
+        // lanes of a group past the end transform zeros and store nothing (every
+        // lane joins the shuffles)
+        const bool live = row[k] >= 0;
+        const uint32_t xs[8] = {xv[k][0].x, xv[k][0].y, xv[k][0].z, xv[k][0].w,
+                                xv[k][1].x, xv[k][1].y, xv[k][1].z, xv[k][1].w};
+        const uint32_t ss[8] = {sv[k][0].x, sv[k][0].y, sv[k][0].z, sv[k][0].w,
+                                sv[k][1].x, sv[k][1].y, sv[k][1].z, sv[k][1].w};
+        const uint32_t rs[8] = {rv[k][0].x, rv[k][0].y, rv[k][0].z, rv[k][0].w,
+                                rv[k][1].x, rv[k][1].y, rv[k][1].z, rv[k][1].w};
+        float v[16];
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const uint32_t xb = (xs[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
-            const float sc = f16_bits_to_f32((uint16_t)(ss[i >> 1] >> (16 * (i & 1))));
-            const float r = f16_bits_to_f32((uint16_t)(rs[i >> 1] >> (16 * (i & 1))));
-            v[i] = (bf16_bits_to_f32(xb) * sc) * r;
+        for (int i = 0; i < 16; i++) {
+            const int bs = 16 * (i & 1);
+            v[i] = live ? (bf16_bits_to_f32((xs[i >> 1] >> bs) & 0xFFFFu) *
+                           f16_bits_to_f32((uint16_t)(ss[i >> 1] >> bs))) *
+                              f16_bits_to_f32((uint16_t)(rs[i >> 1] >> bs))
+                        : 0.f;
         }
-        warp_fwht128(v, lane);
-        uint2 o;
-        o.x = (uint32_t)f32_to_f16_bits(v[0] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[1] * kHadNorm) << 16);
-        o.y = (uint32_t)f32_to_f16_bits(v[2] * kHadNorm) | ((uint32_t)f32_to_f16_bits(v[3] * kHadNorm) << 16);
-        *reinterpret_cast<uint2 *>(u + ((int64_t)sh * M + m) * IC + c0) = o;
+#pragma unroll
+        for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                if (i & h) continue;
+                const float a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+        }
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1) {
+            const bool upper = sub & m;
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                const float o = __shfl_xor_sync(kFull, v[i], m);
+                v[i] = upper ? o - v[i] : v[i] + o;
+            }
+        }
+        if (!live) continue;
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+            o[i] = (uint32_t)f32_to_f16_bits(v[2 * i] * kHadNorm) |
+                   ((uint32_t)f32_to_f16_bits(v[2 * i + 1] * kHadNorm) << 16);
+        if constexpr (V16) {
+            uint4 *dst = reinterpret_cast<uint4 *>(u + row[k] * IC + c0[k]);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        } else {
+            uint2 *dst = reinterpret_cast<uint2 *>(u + row[k] * IC + c0[k]);
+#pragma unroll
+            for (int i = 0; i < 4; i++) dst[i] = make_uint2(o[2 * i], o[2 * i + 1]);
+        }
     }
 }
 
 cudaError_t launch_pretransform_shards(const uint16_t *x, int64_t M, int IC, const PretransformShards &p,
                                        uint16_t *u, cudaStream_t s) {
     const int64_t blocks = (int64_t)p.n * M * (IC / kHad);
-    // runs of kPtRun blocks once the blocks alone fill several waves of warps
-    const int bpw = blocks >= (int64_t)device_info().sm_count * 64 * 8 ? kPtRun : 1;
-    const int64_t runs = (IC / kHad + bpw - 1) / bpw;
-    const int64_t warps = (int64_t)p.n * M * runs;
+    // kPtSteps steps per warp once the blocks fill several waves of warps; one
+    // step otherwise (more warps, shorter latency)
+    const int steps = blocks >= (int64_t)device_info().sm_count * 64 * 4 * kPtSteps ? kPtSteps : 1;
+    const int64_t warps = (blocks + 4 * steps - 1) / (4 * steps);
     const int64_t grid = (warps + 7) / 8;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
@@ -85,7 +142,9 @@ cudaError_t launch_pretransform_shards(const uint16_t *x, int64_t M, int IC, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, pretransform_kernel, x, M, IC, p, u, bpw);
+    if (((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(u)) & 15u) == 0)
+        return cudaLaunchKernelEx(&cfg, pretransform_kernel<true>, x, M, IC, p, u, steps);
+    return cudaLaunchKernelEx(&cfg, pretransform_kernel<false>, x, M, IC, p, u, steps);
 }
 
 cudaError_t launch_pretransform(const uint16_t *x, int64_t M, int IC, const uint16_t *s_in,

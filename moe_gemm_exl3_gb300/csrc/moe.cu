@@ -115,6 +115,9 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restri
                                                            int32_t *__restrict__ ids, float *__restrict__ w) {
     // the routing kernel that follows may be scheduled now; it waits for this grid
     asm volatile("griddepcontrol.launch_dependents;");
+    // launched as a programmatic dependent itself: wait for the preceding kernel
+    // before reading the logits or writing ids and w
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -597,8 +600,16 @@ exl3_status exl3_moe_topk_softmax(const float *logits, int32_t T, int32_t E, int
                     kMoeMaxE, topk, kMoeMaxTopk);
     if (T == 0) return EXL3_OK;
     if (!logits || !ids || !w) return fail(EXL3_EINVAL, "moe_topk_softmax: null pointer");
-    topk_softmax_kernel<<<(T + 7) / 8, 256, 0, (cudaStream_t)stream>>>(logits, T, E, topk, ids, w);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((T + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, topk_softmax_kernel, logits, (int)T, (int)E, (int)topk, ids, w);
     if (e != cudaSuccess) return cuda_fail(e, "moe_topk_softmax");
     return EXL3_OK;
 }

@@ -35,8 +35,9 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* alignment */ + 256 /* 
 constexpr uint32_t kIdesc = make_idesc_f16(BM, BN);
 
 // ------------------------------------------------------------ kernel
-// Tile order: groups of kGroupN column tiles, row tiles fastest within a group,
-// so the CTAs running at one time share a few activation and weight tiles in L2.
+// Tile order: groups of kGroupN column tiles; within a group the column tile
+// varies fastest, then the row tile, so the CTAs running at one time share a
+// few activation and weight panels in L2.
 constexpr int kGroupN = 16;
 
 __device__ __forceinline__ void tile_coords(int t, int MT, int NT, int &mt, int &nt) {
