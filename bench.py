@@ -895,8 +895,8 @@ def run_reference(args):
     # blocks per step so that W + K steps fit the budget; at least one block per step,
     # and if even that does not fit, fewer steps are executed (reported as such)
     nblk = int(max(1, min(nblk_total, budget / max(1, K + W) / per_blk)))
-    run_steps = int(max(1, min(K, budget / (nblk * per_blk) - min(W, 1))))
-    for _ in range(min(W, 1)):
+    run_steps = int(max(1, min(K, budget / (nblk * per_blk) - W)))
+    for _ in range(W):
         one(nblk)
     t0 = time.perf_counter()
     for _ in range(run_steps):
@@ -905,7 +905,7 @@ def run_reference(args):
     v = M / t
     wl = GateUp(args)
     line = {"impl": "reference", "metric": wl.metric, "value": round(v, 3), "unit": "tokens/s",
-            "n_gpus": 1, "steps": run_steps, "steps_requested": K, "warmup": min(W, 1),
+            "n_gpus": 1, "steps": run_steps, "steps_requested": K, "warmup": W,
             "ms_per_step": round(t * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)", "config": wl.config(),
             "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": omp_threads(), "kind": "oracle",

@@ -202,6 +202,21 @@ exl3_status exl3_linear_into_noalloc(const uint16_t *x, int64_t M, int32_t IC,
  *   shards   HOST array of n_shards descriptors, 1 <= n_shards <= 4
  *   ws       exl3_linear_shards_workspace_bytes(M, IC, shards, n_shards) bytes
  */
+/*
+ * Codebook of a tensor.  EXL3 checkpoints mark a tensor's codebook with
+ * per-tensor marker entries (vllm-quantpack linear.py, LINEAR_SUFFIXES: "mcg"
+ * and "mul1" beside "trellis", read as present / absent per shard; the vLLM
+ * PR #190 thread: "mcg/mul1 sentinel semantics", MCG-marked modules on one
+ * kernel, legacy and MUL1 shards on another).  The pages give neither
+ * variant's constants, so this build decodes the default (3INST) codebook only:
+ * a shard marked MCG or MUL1 returns EXL3_EUNSUPPORTED before any launch.
+ */
+enum {
+    EXL3_CODEBOOK_3INST = 0,   /* no marker: the default codebook */
+    EXL3_CODEBOOK_MCG = 1,     /* "mcg" marker present */
+    EXL3_CODEBOOK_MUL1 = 2     /* "mul1" marker present */
+};
+
 typedef struct exl3_shard {
     const int16_t *code;      /* [IC/16][OC/16][16*K] */
     const uint16_t *s_in;     /* fp16 [IC] */
@@ -211,6 +226,8 @@ typedef struct exl3_shard {
     int32_t OC;
     int32_t K;
     int64_t col0;
+    int32_t codebook;         /* EXL3_CODEBOOK_*; 0 (zero-initialised) is the default */
+    int32_t reserved;         /* 0 */
 } exl3_shard;
 
 size_t exl3_linear_shards_workspace_bytes(int64_t max_M, int32_t IC, const exl3_shard *shards,

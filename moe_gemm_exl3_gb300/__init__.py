@@ -40,11 +40,15 @@ class Exl3Error(RuntimeError):
         self.status = status
 
 
+CODEBOOKS = {"3inst": 0, "mcg": 1, "mul1": 2}
+
+
 class Shard(ctypes.Structure):
     """exl3_shard: one source tensor of a merged layer."""
     _fields_ = [("code", ctypes.c_void_p), ("s_in", ctypes.c_void_p), ("rin", ctypes.c_void_p),
                 ("rout", ctypes.c_void_p), ("s_out", ctypes.c_void_p), ("OC", ctypes.c_int32),
-                ("K", ctypes.c_int32), ("col0", ctypes.c_int64)]
+                ("K", ctypes.c_int32), ("col0", ctypes.c_int64), ("codebook", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class Projection(ctypes.Structure):
@@ -235,19 +239,20 @@ def _shard_array(shards, IC):
     col = 0
     for i, sh in enumerate(shards):
         code, K, s_in, rin, rout, s_out = sh[:6]
-        col0 = sh[6] if len(sh) > 6 else col
+        col0 = sh[6] if len(sh) > 6 and sh[6] is not None else col
+        codebook = CODEBOOKS[sh[7]] if len(sh) > 7 else 0
         if code.dim() != 3 or code.shape[2] != 16 * K or code.shape[0] * 16 != IC:
             raise ValueError(f"shard {i}: code {tuple(code.shape)} does not match K={K}, IC={IC}")
         OC = code.shape[1] * 16
         arr[i] = Shard(_ptr(code, torch.int16, "code"), _ptr(s_in, torch.float16, "s_in"),
                        _ptr(rin, torch.float16, "rin"), _ptr(rout, torch.float16, "rout"),
-                       _ptr(s_out, torch.float16, "s_out"), OC, K, col0)
+                       _ptr(s_out, torch.float16, "s_out"), OC, K, col0, codebook, 0)
         col = col0 + OC
     return arr
 
 
 def exl3_linear_shards_workspace_bytes(max_M: int, IC: int, shards) -> int:
-    """shards: sequence of (code, K, s_in, rin, rout, s_out[, col0]) device tensors."""
+    """shards: sequence of (code, K, s_in, rin, rout, s_out[, col0[, codebook]]); codebook "3inst" (default), "mcg" or "mul1"."""
     arr = _shard_array(shards, IC)
     return int(lib().exl3_linear_shards_workspace_bytes(max_M, IC, arr, len(shards)))
 

@@ -518,6 +518,16 @@ exl3_status exl3_gemm_a8_into(const uint8_t *A, const float *As, int64_t M, int3
     return run_gemm("gemm_a8_into", ws.u, M, IC, &d, 1, out, ldo, ws, true, s, nullptr, As, false);
 }
 
+// A shard's codebook marker: only the default codebook is decoded (its constants
+// are the only ones the method's description fixes).
+static exl3_status check_codebook(const char *fn, const exl3_shard &h, int i) {
+    if (h.codebook == EXL3_CODEBOOK_3INST) return EXL3_OK;
+    if (h.codebook == EXL3_CODEBOOK_MCG || h.codebook == EXL3_CODEBOOK_MUL1)
+        return fail(EXL3_EUNSUPPORTED, "%s: shard %d is marked with the %s codebook; this build decodes the default "
+                    "(3INST) codebook only", fn, i, h.codebook == EXL3_CODEBOOK_MCG ? "MCG" : "MUL1");
+    return fail(EXL3_EINVAL, "%s: shard %d: codebook = %d (0 default, 1 MCG, 2 MUL1)", fn, i, h.codebook);
+}
+
 static bool shards_shape(const exl3_shard *shards, int32_t n, int *groups, int32_t *max_oc) {
     if (!shards || n < 1 || n > kMaxInlineEntries) return false;
     *groups = 0;
@@ -548,7 +558,9 @@ static exl3_status shards_prepare(const char *fn, const uint16_t *x, int64_t M, 
     for (int i = 0; i < n; i++) {
         const exl3_shard &h = shards[i];
         const uint16_t *si = need_in ? h.s_in : h.rout, *ri = need_in ? h.rin : h.rout;
-        exl3_status st = check_linear_args(fn, x, M, IC, h.code, h.OC, h.K, si, ri, h.rout, h.s_out);
+        exl3_status st = check_codebook(fn, h, i);
+        if (st != EXL3_OK) return st;
+        st = check_linear_args(fn, x, M, IC, h.code, h.OC, h.K, si, ri, h.rout, h.s_out);
         if (st == EXL3_OK)
             st = check_out_ws(fn, M, h.OC, out, ldo, h.col0, wsp, ws_bytes,
                               exl3_linear_shards_workspace_bytes(M, IC, shards, n));
@@ -798,7 +810,9 @@ exl3_status exl3_linear_projections(const exl3_projection *p, int32_t n, int64_t
         const exl3_projection &pr = p[i];
         for (int k = 0; k < pr.n_shards; k++) {
             const exl3_shard &h = pr.shards[k];
-            exl3_status st = check_linear_args(fn, pr.x, M, pr.IC, h.code, h.OC, h.K, h.s_in, h.rin, h.rout, h.s_out);
+            exl3_status st = check_codebook(fn, h, k);
+            if (st == EXL3_OK)
+                st = check_linear_args(fn, pr.x, M, pr.IC, h.code, h.OC, h.K, h.s_in, h.rin, h.rout, h.s_out);
             if (st == EXL3_OK) st = check_out_ws(fn, M, h.OC, pr.out, pr.ldo, h.col0, wsp, ws_bytes, need);
             if (st != EXL3_OK) return st;
         }

@@ -76,3 +76,33 @@ def test_long_moe_calls_run_in_passes_of_bounded_workspace():
     assert L.exl3_moe_workspace_bytes(1, 128 * 40000, 128, 8, 2) == 0
     st = L.exl3_moe_grouped(None, 1, 128 * 40000, 128, 8, 2, None, None, None, None, None, 0, None)
     assert st == m.EXL3_EINVAL and b"counters" in L.exl3_last_error()
+
+
+def test_struct_layouts_match_the_binding(tmp_path):
+    # the ctypes mirrors of exl3_shard and exl3_projection have the C layout
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "exl3.h"\n'
+                   'int main(void) { printf("%zu %zu %zu %zu %zu\\n", sizeof(exl3_shard), '
+                   'offsetof(exl3_shard, col0), offsetof(exl3_shard, codebook), sizeof(exl3_projection), '
+                   'offsetof(exl3_projection, ldo)); return 0; }\n')
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.check_call(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = [int(v) for v in subprocess.check_output([str(exe)]).split()]
+    want = [ctypes.sizeof(m.Shard), m.Shard.col0.offset, m.Shard.codebook.offset, ctypes.sizeof(m.Projection),
+            m.Projection.ldo.offset]
+    assert got == want
+
+
+def test_marked_codebooks_are_rejected_before_any_launch():
+    # a shard carrying the MCG or MUL1 marker fails validation on the host (its
+    # decode constants are not part of this build); an unknown value is invalid
+    b.build()
+    L = m.lib()
+    for cb, st_want, word in ((1, m.EXL3_EUNSUPPORTED, b"MCG"), (2, m.EXL3_EUNSUPPORTED, b"MUL1"),
+                              (7, m.EXL3_EINVAL, b"codebook = 7")):
+        sh = (m.Shard * 1)()
+        sh[0] = m.Shard(4096, 4096, 4096, 4096, 4096, 256, 2, 0, cb, 0)   # never dereferenced
+        st = L.exl3_linear_into_shards(4096, 1, 256, sh, 1, 8192, 256, 16384, 1 << 20, None)
+        assert st == st_want
+        assert word in L.exl3_last_error()
