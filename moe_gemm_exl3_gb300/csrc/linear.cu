@@ -258,6 +258,18 @@ __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Parts per column group when the groups fit the grid: as many as the grid
+// allows, but each part keeps at least kMinRowsPerWarp tile rows per warp (a
+// part's fixed costs, the load ramp and the split-K handshake, outweigh a few
+// rows of decode).
+constexpr int kMinRowsPerWarp = 4;
+__host__ __device__ __forceinline__ int decode_parts(int fit, int A) {
+    int cap = A / (kMinRowsPerWarp * kDecodeWarps);
+    if (cap < 1) cap = 1;
+    int p = fit < cap ? fit : cap;
+    return p < 1 ? 1 : p;
+}
+
 // KSET: bit k set = the launch may contain entries of bitrate k (2, 3, 4); only
 // those decode paths are compiled into the kernel, which keeps registers low.
 // USRC: where the activation rows come from (kUGlobal, kUGather or kUCodes; see
@@ -290,16 +302,21 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
     }
     const int64_t total = (int64_t)n_groups * A;
     const int c = blockIdx.x;
+    // entry lists built on the device (MoE): when the groups fit the grid, whole
+    // groups or a few parts of each, as the host does for dense launches
+    int parts = a.parts;
+    if (parts == 0 && a.n_entries_dev && n_groups > 0 && n_groups <= (int)gridDim.x)
+        parts = decode_parts(gridDim.x / n_groups, A);
     int nCTA;
     int64_t f, f_end;
-    if (a.parts > 0) {
+    if (parts > 0) {
         // item partition: CTA c takes part c % parts of column group c / parts, so a
         // CTA never switches groups and a group's partials come from exactly `parts` CTAs
-        nCTA = n_groups * a.parts;
+        nCTA = n_groups * parts;
         if (c >= nCTA) return;
-        const int g = c / a.parts, pp = c - g * a.parts;
-        f = (int64_t)g * A + (int64_t)pp * A / a.parts;
-        f_end = (int64_t)g * A + (int64_t)(pp + 1) * A / a.parts;
+        const int g = c / parts, pp = c - g * parts;
+        f = (int64_t)g * A + (int64_t)pp * A / parts;
+        f_end = (int64_t)g * A + (int64_t)(pp + 1) * A / parts;
     } else {
         // stream-K: every CTA of the partition must own at least one unit (an empty
         // range would never arrive at its group's counter): with fewer units than
@@ -361,9 +378,9 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
 
         // ---- split-K across CTAs
         int c_first, c_last;     // the CTAs that own units of group gi
-        if (a.parts > 0) {
-            c_first = gi * a.parts;
-            c_last = c_first + a.parts - 1;
+        if (parts > 0) {
+            c_first = gi * parts;
+            c_last = c_first + parts - 1;
         } else {
             const int64_t x0 = (int64_t)gi * A, x1 = (int64_t)(gi + 1) * A - 1;
             c_first = (int)(((x0 + 1) * nCTA - 1) / total);
@@ -494,9 +511,8 @@ static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t tot
         // one part of one group (no group switches inside a CTA, equal work per CTA)
         const int64_t groups = total_hint / A;
         if (groups > 0 && groups <= grid) {
-            int64_t parts = grid / groups;
-            if (parts > A) parts = A;
-            a.parts = (int32_t)parts;
+            const int parts = decode_parts((int)(grid / groups), (int)A);
+            a.parts = parts;
             grid = groups * parts;
         }
     }
