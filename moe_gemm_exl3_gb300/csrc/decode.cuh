@@ -22,9 +22,11 @@ __device__ __forceinline__ int frag_index(int n, int oc) {
 template <int NB>
 struct DecodeOcc { static constexpr int value = NB <= 2 ? 2 : 1; };
 
-template <int NB>
+// Shared memory of the grouped GEMM: per accumulator set (two when paired) the
+// warps' fragments, then the entries, then the arrival flag.
+template <int NB, bool PAIR = false>
 constexpr size_t group_smem_bytes() {
-    return sizeof(float) * kDecodeWarps * 8 * NB * 4 * 32 + sizeof(GroupEntry) + 16;
+    return (PAIR ? 2 : 1) * (sizeof(float) * kDecodeWarps * 8 * NB * 4 * 32 + sizeof(GroupEntry)) + 16;
 }
 
 

@@ -67,7 +67,7 @@ struct GroupEntry {
     int32_t u_row0;
     int32_t nrows;            // <= 8 * NB of the launch
     int32_t g0;               // first global column-group index of this entry
-    int32_t pad_;
+    int32_t slot;             // MoE: the expert's bank slot (the paired FC1 epilogue's w2_suh row)
 };
 
 enum GroupMode : int32_t {
@@ -113,6 +113,12 @@ struct GroupGemmArgs {
     // then; one 8-row block per entry)
     int32_t codes;
     const float *row_scale;
+    // Paired FC1 (gathered rows, entries 2i / 2i + 1 = w1 / w3 of one expert row
+    // block): the epilogue writes FC2's input act_out[row][col] (fp16, row stride
+    // OC) = Had128((silu(g) * u) * act_suh[slot][col]) instead of fp32 rows.
+    int32_t pair_act;
+    const uint16_t *act_suh;
+    uint16_t *act_out;
 };
 constexpr int kMaxInlineEntries = 4;
 

@@ -273,18 +273,24 @@ __host__ __device__ __forceinline__ int decode_parts(int fit, int A) {
 // KSET: bit k set = the launch may contain entries of bitrate k (2, 3, 4); only
 // those decode paths are compiled into the kernel, which keeps registers low.
 // USRC: where the activation rows come from (kUGlobal, kUGather or kUCodes; see
-// group_accumulate).
-template <int NB, int KSET, int USRC = kUGlobal>
+// group_accumulate).  PAIR (MoE FC1 with gathered rows): consecutive entries 2i,
+// 2i + 1 are an expert row block's w1 and w3; a column group covers both (2A
+// units: w1's tile rows, then w3's), and its epilogue produces FC2's input,
+// Had((silu(g) * u) * w2_suh[slot]), instead of two fp32 rows.
+template <int NB, int KSET, int USRC = kUGlobal, bool PAIR = false>
 __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(const GroupGemmArgs a) {
     static_assert(USRC == kUGlobal || NB == 1, "gathered and 8-bit activation rows serve one 8-row block per entry");
+    static_assert(!PAIR || USRC == kUGather, "the paired epilogue serves the gathered FC1");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     constexpr int FRAG = 8 * NB * 4 * 32;
-    float *red = reinterpret_cast<float *>(smem_raw);                   // [warps][FRAG]
-    GroupEntry *s_ent = reinterpret_cast<GroupEntry *>(red + kDecodeWarps * FRAG);
-    int *s_last = reinterpret_cast<int *>(s_ent + 1);
+    constexpr int NSUB = PAIR ? 2 : 1;                                  // accumulator sets: (gate, up) when paired
+    float *red = reinterpret_cast<float *>(smem_raw);                   // [NSUB][warps][FRAG]
+    GroupEntry *s_ent = reinterpret_cast<GroupEntry *>(red + NSUB * kDecodeWarps * FRAG);
+    int *s_last = reinterpret_cast<int *>(s_ent + NSUB);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int A = a.IC / kTile;
+    const int AU = NSUB * A;   // units (tile rows) per column group
 
     // everything below reads what the preceding kernel in the stream wrote
     grid_dependency_wait();
@@ -295,18 +301,18 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
     int n_groups;
     const int n_entries = a.n_entries_dev ? *a.n_entries_dev : a.n_inline;
     if (a.n_groups_per_entry > 0) {
-        n_groups = n_entries * a.n_groups_per_entry;
+        n_groups = (PAIR ? n_entries / 2 : n_entries) * a.n_groups_per_entry;
     } else {
         n_groups = 0;
         for (int i = 0; i < n_entries; i++) n_groups += a.inline_e[i].OC / kHad;
     }
-    const int64_t total = (int64_t)n_groups * A;
+    const int64_t total = (int64_t)n_groups * AU;
     const int c = blockIdx.x;
     // entry lists built on the device (MoE): when the groups fit the grid, whole
     // groups or a few parts of each, as the host does for dense launches
     int parts = a.parts;
     if (parts == 0 && a.n_entries_dev && n_groups > 0 && n_groups <= (int)gridDim.x)
-        parts = decode_parts(gridDim.x / n_groups, A);
+        parts = decode_parts(gridDim.x / n_groups, AU);
     int nCTA;
     int64_t f, f_end;
     if (parts > 0) {
@@ -315,8 +321,8 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
         nCTA = n_groups * parts;
         if (c >= nCTA) return;
         const int g = c / parts, pp = c - g * parts;
-        f = (int64_t)g * A + (int64_t)pp * A / parts;
-        f_end = (int64_t)g * A + (int64_t)(pp + 1) * A / parts;
+        f = (int64_t)g * AU + (int64_t)pp * AU / parts;
+        f_end = (int64_t)g * AU + (int64_t)(pp + 1) * AU / parts;
     } else {
         // stream-K: every CTA of the partition must own at least one unit (an empty
         // range would never arrive at its group's counter): with fewer units than
@@ -329,12 +335,15 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
     const uint32_t hx = a.hash_xor;
 
     while (f < f_end) {
-        const int gi = (int)(f / A);                 // global column-group index
-        const int a_lo = (int)(f % A);
-        const int a_hi = (int)((int64_t)A < a_lo + (f_end - f) ? (int64_t)A : a_lo + (f_end - f));
-        // the entry owning group gi
+        const int gi = (int)(f / AU);                // global column-group index
+        const int a_lo = (int)(f % AU);
+        const int a_hi = (int)((int64_t)AU < a_lo + (f_end - f) ? (int64_t)AU : a_lo + (f_end - f));
+        // the entry owning group gi (both entries of the pair)
         if (threadIdx.x == 0) {
-            if (a.n_groups_per_entry > 0) {
+            if (PAIR) {
+                s_ent[0] = a.entries[2 * (gi / a.n_groups_per_entry)];
+                s_ent[1] = a.entries[2 * (gi / a.n_groups_per_entry) + 1];
+            } else if (a.n_groups_per_entry > 0) {
                 *s_ent = a.entries ? a.entries[gi / a.n_groups_per_entry] : a.inline_e[gi / a.n_groups_per_entry];
             } else {
                 int i = 0;
@@ -346,35 +355,47 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
         const GroupEntry e = *s_ent;
         const int G = a.n_groups_per_entry > 0 ? gi % a.n_groups_per_entry : gi - e.g0;
 
-        float acc[8][NB][4];
+        // one accumulator set per sub-range (paired: w1's tile rows, then w3's),
+        // each reduced over the warps in fixed order into its own region of red
+#pragma unroll 1
+        for (int sub = 0; sub < NSUB; sub++) {
+            const int lo = PAIR ? (a_lo > sub * A ? a_lo : sub * A) - sub * A : a_lo;
+            const int hi = PAIR ? (a_hi < (sub + 1) * A ? a_hi : (sub + 1) * A) - sub * A : a_hi;
+            const GroupEntry es = PAIR ? s_ent[sub] : e;
+            float acc[8][NB][4];
 #pragma unroll
-        for (int j = 0; j < 8; j++)
+            for (int j = 0; j < 8; j++)
 #pragma unroll
-            for (int nb = 0; nb < NB; nb++)
+                for (int nb = 0; nb < NB; nb++)
 #pragma unroll
-                for (int r = 0; r < 4; r++) acc[j][nb][r] = 0.f;
-        if ((KSET & 4) && e.K == 2)
-            group_accumulate<2, NB, USRC>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
-        if ((KSET & 8) && e.K == 3)
-            group_accumulate<3, NB, USRC>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
-        if ((KSET & 16) && e.K == 4)
-            group_accumulate<4, NB, USRC>(acc, e, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
-
-        // ---- CTA reduction in fixed warp order (fragment order, one barrier)
+                    for (int r = 0; r < 4; r++) acc[j][nb][r] = 0.f;
+            if (lo < hi) {
+                if ((KSET & 4) && es.K == 2)
+                    group_accumulate<2, NB, USRC>(acc, es, a.u, a.IC, G, lo, hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+                if ((KSET & 8) && es.K == 3)
+                    group_accumulate<3, NB, USRC>(acc, es, a.u, a.IC, G, lo, hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+                if ((KSET & 16) && es.K == 4)
+                    group_accumulate<4, NB, USRC>(acc, es, a.u, a.IC, G, lo, hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+            }
+            float *rs = red + sub * kDecodeWarps * FRAG;
+            // ---- CTA reduction in fixed warp order (fragment order, one barrier)
 #pragma unroll
-        for (int j = 0; j < 8; j++)
+            for (int j = 0; j < 8; j++)
 #pragma unroll
-            for (int nb = 0; nb < NB; nb++)
+                for (int nb = 0; nb < NB; nb++)
 #pragma unroll
-                for (int r = 0; r < 4; r++) red[warp * FRAG + ((j * NB + nb) * 4 + r) * 32 + lane] = acc[j][nb][r];
-        __syncthreads();
-        for (int i = threadIdx.x; i < FRAG; i += blockDim.x) {
-            float sum = red[i];
+                    for (int r = 0; r < 4; r++) rs[warp * FRAG + ((j * NB + nb) * 4 + r) * 32 + lane] = acc[j][nb][r];
+            __syncthreads();
+            for (int i = threadIdx.x; i < FRAG; i += blockDim.x) {
+                float sum = rs[i];
 #pragma unroll
-            for (int wv = 1; wv < kDecodeWarps; wv++) sum += red[wv * FRAG + i];
-            red[i] = sum;
+                for (int wv = 1; wv < kDecodeWarps; wv++) sum += rs[wv * FRAG + i];
+                rs[i] = sum;
+            }
+            __syncthreads();
         }
-        __syncthreads();
+        // element i of the reduced sets (i < NSUB * FRAG) lives at red[ridx(i)]
+        auto ridx = [&](int i) { return PAIR ? (i / FRAG) * (kDecodeWarps * FRAG) + i % FRAG : i; };
 
         // ---- split-K across CTAs
         int c_first, c_last;     // the CTAs that own units of group gi
@@ -382,14 +403,14 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
             c_first = gi * parts;
             c_last = c_first + parts - 1;
         } else {
-            const int64_t x0 = (int64_t)gi * A, x1 = (int64_t)(gi + 1) * A - 1;
+            const int64_t x0 = (int64_t)gi * AU, x1 = (int64_t)(gi + 1) * AU - 1;
             c_first = (int)(((x0 + 1) * nCTA - 1) / total);
             c_last = (int)(((x1 + 1) * nCTA - 1) / total);
         }
         bool do_epilogue = true;
         if (c_first != c_last) {
-            float *slot = a.partials + (int64_t)(c + gi) * FRAG;
-            for (int i = threadIdx.x; i < FRAG; i += blockDim.x) slot[i] = red[i];
+            float *slot = a.partials + (int64_t)(c + gi) * (NSUB * FRAG);
+            for (int i = threadIdx.x; i < NSUB * FRAG; i += blockDim.x) slot[i] = red[ridx(i)];
             __threadfence();
             __syncthreads();
             if (threadIdx.x == 0) {
@@ -402,30 +423,64 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
                 __threadfence();
                 // CTA order outermost so each CTA's elements load in parallel; the
                 // sum runs in ascending CTA order (deterministic)
-                constexpr int PER = (FRAG + kDecodeWarps * 32 - 1) / (kDecodeWarps * 32);
+                constexpr int PER = (NSUB * FRAG + kDecodeWarps * 32 - 1) / (kDecodeWarps * 32);
                 float sum[PER];
 #pragma unroll
                 for (int k = 0; k < PER; k++) sum[k] = 0.f;
                 for (int cc = c_first; cc <= c_last; cc++) {
-                    const float *src = a.partials + (int64_t)(cc + gi) * FRAG;
+                    const float *src = a.partials + (int64_t)(cc + gi) * (NSUB * FRAG);
 #pragma unroll
                     for (int k = 0; k < PER; k++) {
                         const int i = threadIdx.x + k * kDecodeWarps * 32;
-                        if (i < FRAG) sum[k] += __ldcg(src + i);
+                        if (i < NSUB * FRAG) sum[k] += __ldcg(src + i);
                     }
                 }
 #pragma unroll
                 for (int k = 0; k < PER; k++) {
                     const int i = threadIdx.x + k * kDecodeWarps * 32;
-                    if (i < FRAG) red[i] = sum[k];
+                    if (i < NSUB * FRAG) red[ridx(i)] = sum[k];
                 }
                 if (threadIdx.x == 0) a.counters[gi] = 0;
                 __syncthreads();
             }
         }
 
+        // ---- paired epilogue: g = Had128(v_w1) * svh_w1, u = Had128(v_w3) * svh_w3,
+        // then FC2's input h2 = Had128((silu(g) * u) * w2_suh[slot]) -> fp16
+        if (PAIR && do_epilogue) {
+            const GroupEntry e3 = s_ent[1];
+            const int oc0 = G * kHad + 4 * lane;
+            const uint2 pg = __ldg(reinterpret_cast<const uint2 *>(e.post + oc0));
+            const uint2 pu = __ldg(reinterpret_cast<const uint2 *>(e3.post + oc0));
+            const uint2 ps = __ldg(reinterpret_cast<const uint2 *>(a.act_suh + (int64_t)e.slot * e.OC + oc0));
+            const uint32_t wg[2] = {pg.x, pg.y}, wu[2] = {pu.x, pu.y}, ws[2] = {ps.x, ps.y};
+            for (int n = warp; n < e.nrows; n += kDecodeWarps) {
+                float vg[4], vu[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    vg[i] = red[frag_index<NB>(n, 4 * lane + i)];
+                    vu[i] = red[kDecodeWarps * FRAG + frag_index<NB>(n, 4 * lane + i)];
+                }
+                warp_fwht128(vg, lane);
+                warp_fwht128(vu, lane);
+                float h[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int hh = i >> 1, sh = 16 * (i & 1);
+                    const float g = (vg[i] * kHadNorm) * f16_bits_to_f32((uint16_t)(wg[hh] >> sh));
+                    const float u = (vu[i] * kHadNorm) * f16_bits_to_f32((uint16_t)(wu[hh] >> sh));
+                    const float silu = g / (1.0f + __expf(-g));
+                    h[i] = (silu * u) * f16_bits_to_f32((uint16_t)(ws[hh] >> sh));
+                }
+                warp_fwht128(h, lane);
+                uint2 o;
+                o.x = (uint32_t)f32_to_f16_bits(h[0] * kHadNorm) | ((uint32_t)f32_to_f16_bits(h[1] * kHadNorm) << 16);
+                o.y = (uint32_t)f32_to_f16_bits(h[2] * kHadNorm) | ((uint32_t)f32_to_f16_bits(h[3] * kHadNorm) << 16);
+                *reinterpret_cast<uint2 *>(a.act_out + (e.out_off + n) * (int64_t)e.OC + oc0) = o;
+            }
+        }
         // ---- epilogue: Had128 of each row's 128 columns, then the post-scales
-        if (do_epilogue) {
+        if (!PAIR && do_epilogue) {
             const int oc0 = G * kHad + 4 * lane;
             const uint2 rv = __ldg(reinterpret_cast<const uint2 *>(e.post + oc0));
             uint2 sv = make_uint2(0x3C003C00u, 0x3C003C00u);
@@ -493,11 +548,11 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
     }
 }
 
-template <int NB, int KSET, int USRC = kUGlobal>
+template <int NB, int KSET, int USRC = kUGlobal, bool PAIR = false>
 static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t total_hint, cudaStream_t s) {
-    constexpr size_t smem = group_smem_bytes<NB>();
+    constexpr size_t smem = group_smem_bytes<NB, PAIR>();
     int occ = 1;
-    cudaError_t e = kernel_occupancy((const void *)group_gemm_kernel<NB, KSET, USRC>, 256, smem, &occ);
+    cudaError_t e = kernel_occupancy((const void *)group_gemm_kernel<NB, KSET, USRC, PAIR>, 256, smem, &occ);
     if (e != cudaSuccess) return e;
     GroupGemmArgs a = a0;
     a.hash_xor = kHashXor;
@@ -527,7 +582,7 @@ static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t tot
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, group_gemm_kernel<NB, KSET, USRC>, a);
+    return cudaLaunchKernelEx(&cfg, group_gemm_kernel<NB, KSET, USRC, PAIR>, a);
 }
 
 template <int NB>
@@ -561,8 +616,10 @@ cudaError_t launch_group_gemm(const GroupGemmArgs &a, int nb, bool pdl, cudaStre
     if (a.gather) {
         // grouped MoE with activation rows stored per pair: one 8-row block per entry, any K
         if (nb != 1 || a.codes) return cudaErrorInvalidValue;
+        if (a.pair_act) return launch_group_t<1, 28, kUGather, true>(a, pdl, total, s);
         return launch_group_t<1, 28, kUGather>(a, pdl, total, s);
     }
+    if (a.pair_act) return cudaErrorInvalidValue;
     if (a.codes) {
         // 8-bit activation codes: one 8-row block per entry
         if (nb != 1) return cudaErrorInvalidValue;

@@ -102,7 +102,14 @@ MoeLayout moe_layout(int T, int H, int I, int E, int topk) {
     L.st2 = take(sizeof(float) * (size_t)L.R * H);
     const int groups1 = 2 * L.max_entries * (I / kHad), groups2 = L.max_entries * (H / kHad);
     const int gmax = groups1 > groups2 ? groups1 : groups2;
-    L.slab = take(sizeof(float) * (L.fused ? fused_slab_floats(gmax, kFusedRowsNT) : group_slab_floats(gmax, L.nb)));
+    // one 8-row block per entry: FC1 may run paired, one column group per (expert
+    // row block, 128 columns of I) with two accumulator sets per slab slot
+    size_t dec_slab = group_slab_floats(gmax, L.nb);
+    if (L.nb == 1) {
+        const size_t paired = 2 * group_slab_floats(L.max_entries * (I / kHad), 1);
+        if (paired > dec_slab) dec_slab = paired;
+    }
+    L.slab = take(sizeof(float) * (L.fused ? fused_slab_floats(gmax, kFusedRowsNT) : dec_slab));
     L.total = off;
     return L;
 }
@@ -372,6 +379,7 @@ __device__ __forceinline__ void route_body(const RouteArgs &a) {
                 ge.u_row0 = j * a.R + r0;
                 ge.out_off = j * a.R + r0;
                 ge.nrows = nr;
+                ge.slot = p;
                 a.ent1[2 * idx + j] = ge;
             }
             GroupEntry ge = {};
@@ -717,25 +725,18 @@ exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
         g1.entries = ent1;
         g1.n_entries_dev = counts + 1;
         g1.n_groups_per_entry = I / kHad;
-        g1.out_rows = st1;
         g1.partials = slab;
         g1.counters = counters;
         g1.gather = 1;
         g1.R = R;
         g1.topk = topk;
         g1.row_pair = row_pair;
+        // w1 and w3 of an expert row block in one column group: the epilogue applies
+        // the activation and FC2's input transform (no fp32 FC1 rows, no act launch)
+        g1.pair_act = 1;
+        g1.act_suh = b.w2_suh;
+        g1.act_out = h2;
         if ((e = launch_group_gemm(g1, 1, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC1");
-        {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(warp_grid((int64_t)R * (I / kHad)));
-            cfg.blockDim = dim3(256);
-            cfg.stream = s;
-            cfg.attrs = pdl_attr;
-            cfg.numAttrs = 1;
-            if ((e = cudaLaunchKernelEx(&cfg, act_kernel, (const float *)st1, I, R, b.w2_suh, (const int32_t *)row_slot,
-                                        (const int32_t *)counts, h2)) != cudaSuccess)
-                return cuda_fail(e, "moe_grouped: act");
-        }
         GroupGemmArgs g2 = {};
         g2.u = h2;
         g2.IC = I;
@@ -755,7 +756,7 @@ exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
         g2.comb_y = y;
         g2.comb_counters = counters + kCombCounterBase;
         if ((e = launch_group_gemm(g2, 1, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC2");
-        trace("moe_grouped T=%d H=%d I=%d E=%d topk=%d rows<=%d gemm=decode (4 launches)", T, H, I, E, topk, R);
+        trace("moe_grouped T=%d H=%d I=%d E=%d topk=%d rows<=%d gemm=decode (3 launches)", T, H, I, E, topk, R);
         return EXL3_OK;
     }
     route_kernel<<<1, 1024, 0, s>>>(ra);
