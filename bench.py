@@ -455,14 +455,14 @@ class Moe:
             self.touched.append(int(per_slot[slots].sum()))
         bank_mb = (self.bank["w13"].numel() + self.bank["w2"].numel()) * 2 / 1e6
         self.l2 = f"{R} rotating token batches (different experts per step; bank {bank_mb:.0f} MB)"
-        # top-k, then (one 8-row block per entry) route + rotation, FC1 with the activation
+        # top-k, then (one 8-row block per entry) routing + rotation, FC1 with the activation
         # in its epilogue, FC2 with the combine; otherwise route, rotate, FC1, act, FC2, combine
         self.launches_per_step = 4 if self.T * self.TOPK <= 4 * self.E else 7
 
     def step(self, r, x=None):
-        m = self.m
-        m.exl3_moe_topk_softmax(self.ls[r], self.TOPK, self.ids, self.w)
-        m.exl3_moe_grouped(self.xs[r] if x is None else x, self.ids, self.w, self.bank, self.ws, y=self.y)
+        # the layer from router logits in one call (top-k, routing, FC1, FC2, combine)
+        self.m.exl3_moe_forward(self.xs[r] if x is None else x, self.ls[r], self.TOPK, self.bank, self.ws, y=self.y,
+                                ids=self.ids, w=self.w)
 
     def roofline(self, torch, stream):
         # the layer's launch chain: code bytes of the touched experts / layer time

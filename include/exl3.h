@@ -427,7 +427,7 @@ typedef struct exl3_moe_bank {
 exl3_status exl3_moe_topk_softmax(const float *logits, int32_t T, int32_t E, int32_t topk,
                                   int32_t *ids, float *w, exl3_stream stream);
 
-/* Workspace bytes exl3_moe_grouped needs for T tokens of this geometry. */
+/* Workspace bytes exl3_moe_grouped and exl3_moe_forward need for T tokens of this geometry. */
 size_t exl3_moe_workspace_bytes(int32_t T, int32_t H, int32_t I, int32_t E, int32_t topk);
 
 /*
@@ -446,6 +446,18 @@ size_t exl3_moe_workspace_bytes(int32_t T, int32_t H, int32_t I, int32_t E, int3
 exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
                              int32_t E, int32_t topk, const int32_t *ids, const float *w,
                              const exl3_moe_bank *bank, uint16_t *y,
+                             void *ws, size_t ws_bytes, exl3_stream stream);
+
+/*
+ * The whole MoE layer from the router logits: exl3_moe_topk_softmax followed by
+ * exl3_moe_grouped, with ids [T][topk] and w [T][topk] as outputs (the routing
+ * the layer used), in one call on the caller's stream.  logits fp32 [T][E];
+ * requires topk <= E; other arguments and the workspace as for
+ * exl3_moe_grouped.
+ */
+exl3_status exl3_moe_forward(const uint16_t *x, const float *logits, int32_t T, int32_t H,
+                             int32_t I, int32_t E, int32_t topk, const exl3_moe_bank *bank,
+                             int32_t *ids, float *w, uint16_t *y,
                              void *ws, size_t ws_bytes, exl3_stream stream);
 
 /* ------------------------------------------------------------- embedding */

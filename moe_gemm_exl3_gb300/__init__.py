@@ -31,7 +31,7 @@ EXPORTS = ("exl3_last_error", "exl3_version", "exl3_linear_workspace_bytes", "ex
            "exl3_lm_head_workspace_bytes", "exl3_lm_head_int8", "exl3_projections_workspace_bytes",
            "exl3_linear_projections", "exl3_linear_a8_workspace_bytes", "exl3_quantize_a8",
            "exl3_linear_into_a8", "exl3_gemm_a8_into", "exl3_linear_shards_a8_workspace_bytes",
-           "exl3_linear_into_shards_a8", "exl3_gemm_a8_into_shards")
+           "exl3_linear_into_shards_a8", "exl3_gemm_a8_into_shards", "exl3_moe_forward")
 
 
 class Exl3Error(RuntimeError):
@@ -104,6 +104,8 @@ def lib() -> ctypes.CDLL:
                 "exl3_moe_workspace_bytes": ([i32, i32, i32, i32, i32], sz),
                 "exl3_moe_grouped": ([vp, i32, i32, i32, i32, i32, vp, vp, ctypes.POINTER(MoeBank), vp,
                                       vp, sz, vp], ctypes.c_int),
+                "exl3_moe_forward": ([vp, vp, i32, i32, i32, i32, i32, ctypes.POINTER(MoeBank), vp, vp, vp, vp,
+                                      sz, vp], ctypes.c_int),
                 "exl3_embed_int8_gather": ([vp, vp, i64, i32, vp, i64, vp, vp, vp], ctypes.c_int),
                 "exl3_lm_head_workspace_bytes": ([i64, i32, i64], sz),
                 "exl3_projections_workspace_bytes": ([i64, ctypes.POINTER(Projection), i32], sz),
@@ -475,6 +477,27 @@ def exl3_moe_grouped(x, ids, w, bank: dict, ws, y=None) -> torch.Tensor:
                                   _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(x.device)),
            "exl3_moe_grouped")
     return y
+
+
+def exl3_moe_forward(x, logits, topk: int, bank: dict, ws, y=None, ids=None, w=None):
+    """The MoE layer from router logits [T, E]: returns (y, ids, w), the routing the layer used."""
+    T, H = x.shape
+    E = bank["perm"].shape[0]
+    I = bank["w2_suh"].shape[1]
+    if logits.shape != (T, E):
+        raise ValueError(f"logits must be [{T}, {E}], got {tuple(logits.shape)}")
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    if ids is None:
+        ids = torch.empty((T, topk), dtype=torch.int32, device=x.device)
+    if w is None:
+        w = torch.empty((T, topk), dtype=torch.float32, device=x.device)
+    b = moe_bank_struct(bank)
+    _check(lib().exl3_moe_forward(_ptr(x, torch.bfloat16, "x"), _ptr(logits, torch.float32, "logits"), T, H, I, E,
+                                  topk, ctypes.byref(b), _ptr(ids, torch.int32, "ids"), _ptr(w, torch.float32, "w"),
+                                  _ptr(y, torch.bfloat16, "y"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+                                  _stream(x.device)), "exl3_moe_forward")
+    return y, ids, w
 
 
 # ---------------------------------------------------------------- embedding

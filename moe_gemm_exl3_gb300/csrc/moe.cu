@@ -117,18 +117,10 @@ MoeLayout moe_layout(int T, int H, int I, int E, int topk) {
 // ------------------------------------------------------------------ top-k
 // One warp per token: each lane holds the logits e = lane, lane + 32, ...; each
 // of the topk rounds is a warp arg-max (largest logit, ties to the lower expert
-// id); then softmax over the selected logits.
-__global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restrict__ logits, int T, int E, int topk,
-                                                           int32_t *__restrict__ ids, float *__restrict__ w) {
-    // the routing kernel that follows may be scheduled now; it waits for this grid
-    asm volatile("griddepcontrol.launch_dependents;");
-    // launched as a programmatic dependent itself: wait for the preceding kernel
-    // before reading the logits or writing ids and w
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= T) return;
-    const float *l = logits + (int64_t)t * E;
+// id); then softmax over the selected logits.  Lane k < topk ends with the k-th
+// choice's expert id (*id) and weight (*wt).
+__device__ __forceinline__ void topk_warp(const float *__restrict__ l, int E, int topk, int lane, int *id,
+                                          float *wt) {
     constexpr int PER = kMoeMaxE / 32;
     float v[PER];
 #pragma unroll
@@ -162,10 +154,45 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restri
         if (k == 0) sel0 = bv;
         const float ex = expf(bv - sel0);
         den += ex;
-        if (lane == k) my_sel = ex;
-        if (lane == 0) ids[(int64_t)t * topk + k] = be;
+        if (lane == k) {
+            my_sel = ex;
+            *id = be;
+        }
     }
-    if (lane < topk) w[(int64_t)t * topk + lane] = my_sel / den;
+    *wt = my_sel / den;
+}
+
+__global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restrict__ logits, int T, int E, int topk,
+                                                           int32_t *__restrict__ ids, float *__restrict__ w) {
+    // the routing kernel that follows may be scheduled now; it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;");
+    // launched as a programmatic dependent itself: wait for the preceding kernel
+    // before reading the logits or writing ids and w
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int id = 0;
+    float wt = 0.f;
+    topk_warp(logits + (int64_t)t * E, E, topk, lane, &id, &wt);
+    if (lane < topk) {
+        ids[(int64_t)t * topk + lane] = id;
+        w[(int64_t)t * topk + lane] = wt;
+    }
+}
+
+// One warp per token, as a programmatic dependent of the preceding kernel.
+cudaError_t launch_topk(const float *logits, int T, int E, int topk, int32_t *ids, float *w, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((T + 7) / 8));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_softmax_kernel, logits, T, E, topk, ids, w);
 }
 
 // ------------------------------------------------------------------ route
@@ -455,8 +482,8 @@ __device__ __forceinline__ void rotate_pairs(const PairRotateArgs &a, int wid, i
     }
 }
 
-// The first kernel of the three-GEMM-launch chain: CTA 0 routes, the others
-// rotate the pairs' inputs meanwhile (both read only the ids).
+// The first kernel of the small-T chain: CTA 0 routes, the others rotate the
+// pairs' inputs meanwhile (both need only the ids).
 __global__ void __launch_bounds__(1024) route_rotate_kernel(const RouteArgs a, const PairRotateArgs r) {
     // launched as a dependent of the router: wait for its ids; let FC1 be scheduled
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -608,16 +635,7 @@ exl3_status exl3_moe_topk_softmax(const float *logits, int32_t T, int32_t E, int
                     kMoeMaxE, topk, kMoeMaxTopk);
     if (T == 0) return EXL3_OK;
     if (!logits || !ids || !w) return fail(EXL3_EINVAL, "moe_topk_softmax: null pointer");
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((T + 7) / 8));
-    cfg.blockDim = dim3(256);
-    cfg.stream = (cudaStream_t)stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, topk_softmax_kernel, logits, (int)T, (int)E, (int)topk, ids, w);
+    cudaError_t e = launch_topk(logits, T, E, topk, ids, w, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "moe_topk_softmax");
     return EXL3_OK;
 }
@@ -636,10 +654,16 @@ size_t exl3_moe_workspace_bytes(int32_t T, int32_t H, int32_t I, int32_t E, int3
     return full > last ? full : last;
 }
 
-exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I, int32_t E, int32_t topk,
-                             const int32_t *ids, const float *w, const exl3_moe_bank *bank, uint16_t *y, void *wsp,
-                             size_t ws_bytes, exl3_stream stream) {
-    const char *fn = "moe_grouped";
+}  // extern "C"
+
+namespace {
+
+// The layer on T tokens.  logits null: ids and w are the caller's routing
+// (inputs).  logits non-null: ids and w are outputs, this call's own top-k of the
+// logits (the top-k kernel runs first).
+exl3_status moe_layer(const char *fn, const uint16_t *x, const float *logits, int32_t T, int32_t H, int32_t I,
+                      int32_t E, int32_t topk, int32_t *ids, float *w, const exl3_moe_bank *bank, uint16_t *y,
+                      void *wsp, size_t ws_bytes, exl3_stream stream) {
     if (T < 0 || H <= 0 || I <= 0 || H % 128 || I % 128)
         return fail(EXL3_EINVAL, "%s: T = %d, H = %d, I = %d (H and I positive multiples of 128)", fn, T, H, I);
     if (E < 1 || E > kMoeMaxE || topk < 1 || topk > kMoeMaxTopk)
@@ -656,8 +680,8 @@ exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
         if (!x || !ids || !w || !y) return fail(EXL3_EINVAL, "%s: null pointer", fn);
         for (int64_t t0 = 0; t0 < T; t0 += P) {
             const int32_t n = (int32_t)(T - t0 < P ? T - t0 : P);
-            const exl3_status st = exl3_moe_grouped(x + t0 * H, n, H, I, E, topk, ids + t0 * topk, w + t0 * topk, bank,
-                                                    y + t0 * H, wsp, ws_bytes, stream);
+            const exl3_status st = moe_layer(fn, x + t0 * H, logits ? logits + t0 * E : nullptr, n, H, I, E, topk,
+                                             ids + t0 * topk, w + t0 * topk, bank, y + t0 * H, wsp, ws_bytes, stream);
             if (st != EXL3_OK) return st;
         }
         return EXL3_OK;
@@ -705,6 +729,11 @@ exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
     cudaLaunchAttribute pdl_attr[1];
     pdl_attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl_attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (logits) {
+        // the routing below reads ids and w: the top-k first (a programmatic
+        // dependent of whatever precedes the layer, and the routing of it)
+        if ((e = launch_topk(logits, T, E, topk, ids, w, s)) != cudaSuccess) return cuda_fail(e, "moe: top-k");
+    }
     if (chain) {
         PairRotateArgs pr = {x, ids, R, topk, E, H, b, u13};
         const int64_t tasks = (int64_t)R * (H / kHad);
@@ -756,7 +785,7 @@ exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
         g2.comb_y = y;
         g2.comb_counters = counters + kCombCounterBase;
         if ((e = launch_group_gemm(g2, 1, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC2");
-        trace("moe_grouped T=%d H=%d I=%d E=%d topk=%d rows<=%d gemm=decode (3 launches)", T, H, I, E, topk, R);
+        trace("%s T=%d H=%d I=%d E=%d topk=%d rows<=%d gemm=decode (3 launches)", fn, T, H, I, E, topk, R);
         return EXL3_OK;
     }
     route_kernel<<<1, 1024, 0, s>>>(ra);
@@ -821,9 +850,28 @@ exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I,
 
     combine_kernel<<<warp_grid((int64_t)T * (H / kHad)), 256, 0, s>>>(st2, H, T, topk, w, pos, y);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "moe_grouped: combine");
-    trace("moe_grouped T=%d H=%d I=%d E=%d topk=%d rows<=%d nb=%d gemm=%s", T, H, I, E, topk, R, L.nb,
+    trace("%s T=%d H=%d I=%d E=%d topk=%d rows<=%d nb=%d gemm=%s", fn, T, H, I, E, topk, R, L.nb,
           L.fused ? "fused" : "decode");
     return EXL3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+exl3_status exl3_moe_grouped(const uint16_t *x, int32_t T, int32_t H, int32_t I, int32_t E, int32_t topk,
+                             const int32_t *ids, const float *w, const exl3_moe_bank *bank, uint16_t *y, void *wsp,
+                             size_t ws_bytes, exl3_stream stream) {
+    return moe_layer("moe_grouped", x, nullptr, T, H, I, E, topk, const_cast<int32_t *>(ids), const_cast<float *>(w),
+                     bank, y, wsp, ws_bytes, stream);
+}
+
+exl3_status exl3_moe_forward(const uint16_t *x, const float *logits, int32_t T, int32_t H, int32_t I, int32_t E,
+                             int32_t topk, const exl3_moe_bank *bank, int32_t *ids, float *w, uint16_t *y, void *wsp,
+                             size_t ws_bytes, exl3_stream stream) {
+    if (T > 0 && !logits) return fail(EXL3_EINVAL, "moe_forward: null logits");
+    if (topk > E) return fail(EXL3_EINVAL, "moe_forward: topk = %d > E = %d", topk, E);
+    return moe_layer("moe_forward", x, logits, T, H, I, E, topk, ids, w, bank, y, wsp, ws_bytes, stream);
 }
 
 }  // extern "C"

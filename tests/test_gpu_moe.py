@@ -220,3 +220,34 @@ def test_moe_fused_gemm_deterministic(full_bank, pin_gemm_path):
     y2, _ = run_moe(x, ids, w, bank_d, 128, 2048, 768, ws)
     assert np.array_equal(bits(y1), bits(y2))
     assert m.exl3_workspace_error(ws) == 0
+
+
+@pytest.mark.parametrize("T", (1, 16, 64, 65, 512))
+def test_moe_forward_equals_topk_then_grouped(full_bank, T):
+    # the one-call layer from logits (top-k inside the routing launch for small T)
+    # returns the router's ids and weights and the grouped layer's output, bit for bit
+    bank, bank_d = full_bank
+    x, logits = syn.moe_tokens(60 + T, T)
+    ld = dev(logits, torch.float32)
+    xd = dev(x, torch.bfloat16)
+    ids_ref, w_ref = m.exl3_moe_topk_softmax(ld, 8)
+    ws = m.workspace(m.exl3_moe_workspace_bytes(T, 2048, 768, 128, 8))
+    y_ref = m.exl3_moe_grouped(xd, ids_ref, w_ref, bank_d, ws)
+    y, ids, w = m.exl3_moe_forward(xd, ld, 8, bank_d, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids_ref)
+    assert torch.equal(w, w_ref)
+    assert np.array_equal(bits(y), bits(y_ref))
+
+
+def test_moe_forward_small_bank_matches_oracle():
+    E, H, I, topk, T = 6, 256, 128, 3, 9
+    bank = syn.moe_bank(15, E=E, H=H, I=I, distinct_down_k=True)
+    x, logits = syn.moe_tokens(16, T, H=H, E=E)
+    ws = m.workspace(m.exl3_moe_workspace_bytes(T, H, I, E, topk))
+    y, ids, w = m.exl3_moe_forward(dev(x, torch.bfloat16), dev(logits, torch.float32), topk, bank_dev(bank), ws)
+    torch.cuda.synchronize()
+    rid, rw = oracle.topk_softmax(logits, topk)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=2e-6, atol=1e-7)
+    assert_rows_close(as_f64(y), oracle.moe_f64(x, rid, rw, bank))
