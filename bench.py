@@ -249,9 +249,9 @@ class GateUp:
                 "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
                 "traffic": {"decode": lambda: profile_traffic(f"decode_gemm_gate_up_m{self.M}.json",
-                                                              ["linear.cu", "decode.cuh", "common.cuh", "internal.h"]),
+                                                              ["linear.cu", "decode.cuh", "common.cuh"]),
                             "fused": lambda: profile_traffic(f"fused_gemm_gate_up_m{self.M}.json",
-                                                             ["fused_tc.cu", "tc_ptx.cuh", "common.cuh", "internal.h"]),
+                                                             ["fused_tc.cu", "tc_ptx.cuh", "common.cuh"]),
                             "prefill": lambda: None}[gemm_path(self.M)](),
                 "per_launch_us": round(ms * 1e3, 2), "algorithmic_bytes_per_launch": alg,
                 "code_GBps": round(sum(self.code_bytes(K) for K in self.KS) / (ms * 1e-3) / 1e9, 1)}
@@ -388,7 +388,7 @@ class Prefill:
                 "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops_sustained: timed inside a long run of "
                                f"steps under the power cap; fp16 has the same dense rate)",
                 "frac_of_burst": round(a / burst, 4),
-                "traffic": profile_traffic(f"prefill_gemm_m{self.M}.json", ["prefill.cu", "tc_ptx.cuh", "common.cuh", "internal.h"]),
+                "traffic": profile_traffic(f"prefill_gemm_m{self.M}.json", ["prefill.cu", "tc_ptx.cuh", "common.cuh"]),
                 "per_launch_us": round(ms * 1e3, 1), "reconstruct_us": round(ms_rec * 1e3, 1),
                 "algorithmic_flops_per_launch": fl}
 
@@ -672,7 +672,7 @@ class LmHead:
             return {"bound": "hbm", "kernel": "lm_head_decode_kernel (int8 table streamed, mma.sync)",
                     "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
-                    "traffic": profile_traffic(f"lm_head_decode_m{self.M}.json", ["lm_head.cu", "common.cuh", "internal.h"]),
+                    "traffic": profile_traffic(f"lm_head_decode_m{self.M}.json", ["lm_head.cu", "common.cuh"]),
                     "per_launch_us": round(ms * 1e3, 2), "algorithmic_bytes_per_launch": alg}
         fl = 2.0 * self.M * self.H * self.V
         a = fl / (ms * 1e-3) / 1e12
