@@ -165,11 +165,13 @@ __device__ __forceinline__ void warp_fwht128(float (&v)[4], int lane) {
     v[0] = a0 + a2; v[1] = a1 + a3; v[2] = a0 - a2; v[3] = a1 - a3;
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = lane & m;
+        // upper lane: p - v, lower lane: v + p, as one FMA with a sign of +-1
+        // (exact product, the same single rounding)
+        const float sgn = (lane & m) ? -1.f : 1.f;
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            float p = __shfl_xor_sync(kFull, v[i], m);
-            v[i] = upper ? p - v[i] : v[i] + p;
+            const float p = __shfl_xor_sync(kFull, v[i], m);
+            v[i] = fmaf(sgn, v[i], p);
         }
     }
 }

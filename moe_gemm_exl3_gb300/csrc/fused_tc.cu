@@ -577,10 +577,11 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                 }
 #pragma unroll
                 for (int m = 1; m < 4; m <<= 1) {
+                    const float sgn = (part & m) ? -1.f : 1.f;   // o - x or x + o as one exact-sign FMA
 #pragma unroll
                     for (int i = 0; i < 32; i++) {
                         const float o = __shfl_xor_sync(kFull, x[i], m);
-                        x[i] = (part & m) ? o - x[i] : x[i] + o;
+                        x[i] = fmaf(sgn, x[i], o);
                     }
                 }
                 const int nrow = c0 + ti;

@@ -100,11 +100,13 @@ __global__ void __launch_bounds__(256) pretransform_kernel(const uint16_t *__res
         }
 #pragma unroll
         for (int m = 1; m < 8; m <<= 1) {
-            const bool upper = sub & m;
+            // the lane holding the upper index takes o - v, the lower v + o: one FMA
+            // with a sign of +-1 (exact, the same single rounding)
+            const float sgn = (sub & m) ? -1.f : 1.f;
 #pragma unroll
             for (int i = 0; i < 16; i++) {
                 const float o = __shfl_xor_sync(kFull, v[i], m);
-                v[i] = upper ? o - v[i] : v[i] + o;
+                v[i] = fmaf(sgn, v[i], o);
             }
         }
         if (!live) continue;
