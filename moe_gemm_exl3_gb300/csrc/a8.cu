@@ -28,9 +28,10 @@ __global__ void __launch_bounds__(256) quantize_a8_kernel(const uint16_t *__rest
                                                           void *__restrict__ dst, float *__restrict__ As) {
     extern __shared__ __align__(16) float su[];   // [IC]
     __shared__ float s_amax[8];
-    // a dependent launch may be scheduled now; it waits for this grid before reading
-    asm volatile("griddepcontrol.launch_dependents;");
+    // wait for the preceding kernel, then let a dependent launch be scheduled (it
+    // waits for this grid before reading; a reconstruct may run alongside)
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t m = blockIdx.x;                 // row of dst and As
     const int sh = (int)(m / M);
@@ -109,8 +110,8 @@ __global__ void __launch_bounds__(256) quantize_a8_kernel(const uint16_t *__rest
 // 8 codes -> 8 exact fp16 values per thread.
 __global__ void __launch_bounds__(256) codes_to_f16_kernel(const uint8_t *__restrict__ A, int64_t n8,
                                                            uint16_t *__restrict__ dst) {
-    asm volatile("griddepcontrol.launch_dependents;");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
         const uint2 c = __ldg(reinterpret_cast<const uint2 *>(A) + i);

@@ -332,7 +332,11 @@ static exl3_status run_gemm(const char *fn, const uint16_t *u, int64_t M, int32_
     if (mode == GemmMode::kPrefill) {
         for (int i = 0; i < n; i++) {
             bool launched = false;
-            e = launch_reconstruct(sh[i].code, IC, sh[i].OC, sh[i].K, ws.wt, /*transposed=*/true, s);
+            // a programmatic dependent of the kernel before it only when that kernel is
+            // this call's pre-transform (pdl) or the previous shard's GEMM (which triggers
+            // only by completing): both have waited for all earlier work, so the staging
+            // buffer is free and the reconstruct may overlap the pre-transform
+            e = launch_reconstruct(sh[i].code, IC, sh[i].OC, sh[i].K, ws.wt, /*transposed=*/true, s, pdl || i > 0);
             if (e != cudaSuccess) return cuda_fail(e, fn);
             e = launch_prefill(u + (int64_t)slot(i) * M * IC, ws.wt, M, IC, sh[i].OC, sh[i].rout, sh[i].s_out,
                                out + sh[i].col0, ldo, ws.err, s, &launched, 0,

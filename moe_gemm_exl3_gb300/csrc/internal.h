@@ -51,8 +51,12 @@ struct PretransformShards {
 };
 cudaError_t launch_pretransform_shards(const uint16_t *x, int64_t M, int IC, const PretransformShards &p,
                                        uint16_t *u, cudaStream_t s);
+// pdl: launch as a programmatic dependent of the preceding kernel, which must
+// itself have waited for everything before it before triggering (the
+// pre-transforms do): the reconstruct then overlaps that kernel and completes
+// after it.
 cudaError_t launch_reconstruct(const int16_t *code, int IC, int OC, int K, uint16_t *W,
-                               bool transposed, cudaStream_t s);
+                               bool transposed, cudaStream_t s, bool pdl = false);
 cudaError_t launch_codebook_table(uint16_t *table, cudaStream_t s);
 
 // One problem of the grouped decode-mode GEMM: a code tensor [IC/16][OC/16][16K]

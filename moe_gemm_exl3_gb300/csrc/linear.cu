@@ -40,12 +40,13 @@ __global__ void __launch_bounds__(256) pretransform_kernel(const uint16_t *__res
                                                            int64_t M, int IC,
                                                            const __grid_constant__ PretransformShards p,
                                                            uint16_t *__restrict__ u, int steps) {
-    // let a dependent launch (the GEMM that reads u) get scheduled early; it
-    // still waits for this grid to finish before touching u
-    asm volatile("griddepcontrol.launch_dependents;");
     // this launch may itself start before the preceding kernel has finished (a
     // programmatic dependent launch): wait for it before reading x or writing u
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // then let a dependent launch be scheduled: the GEMM that reads u (it waits for
+    // this grid), or the reconstruct, which writes only the staging buffer and may
+    // run alongside (every kernel before this one has completed by now)
+    asm volatile("griddepcontrol.launch_dependents;");
     const int lane = threadIdx.x & 31, sub = lane & 7;
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int nb = IC / kHad;
@@ -202,20 +203,31 @@ __global__ void __launch_bounds__(256) reconstruct_kernel(const int16_t *__restr
             *reinterpret_cast<uint2 *>(W + (int64_t)(16 * b + c) * IC + 16 * a + 4 * q) = make_uint2(p0, p1);
         }
     }
+    // launched as a programmatic dependent of the pre-transform, this grid runs
+    // alongside it; it completes only once the pre-transform has, so the GEMM that
+    // waits for this grid sees both u and W (a no-op without the dependency)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 cudaError_t launch_reconstruct(const int16_t *code, int IC, int OC, int K, uint16_t *W,
-                               bool transposed, cudaStream_t s) {
+                               bool transposed, cudaStream_t s, bool pdl) {
     const int64_t quarters = (int64_t)(IC / kTile) * (OC / kTile) * 4;
-    const unsigned grid = (unsigned)((quarters + 255) / 256);
     const Pow2Table p2 = make_pow2_table();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((quarters + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
     switch (K) {
-        case 2: reconstruct_kernel<2><<<grid, 256, 0, s>>>(code, IC, OC, W, transposed, p2); break;
-        case 3: reconstruct_kernel<3><<<grid, 256, 0, s>>>(code, IC, OC, W, transposed, p2); break;
-        case 4: reconstruct_kernel<4><<<grid, 256, 0, s>>>(code, IC, OC, W, transposed, p2); break;
+        case 2: return cudaLaunchKernelEx(&cfg, reconstruct_kernel<2>, code, IC, OC, W, transposed, p2);
+        case 3: return cudaLaunchKernelEx(&cfg, reconstruct_kernel<3>, code, IC, OC, W, transposed, p2);
+        case 4: return cudaLaunchKernelEx(&cfg, reconstruct_kernel<4>, code, IC, OC, W, transposed, p2);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 __global__ void codebook_table_kernel(uint16_t *table) {
