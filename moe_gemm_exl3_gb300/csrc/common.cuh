@@ -176,6 +176,55 @@ __device__ __forceinline__ void warp_fwht128(float (&v)[4], int lane) {
     }
 }
 
+// Unnormalised Had128 of 128 values held 16 per lane by a group of 8 lanes
+// (sub = lane % 8): v[i] = value (16 * sub + i).  Four register stages (index
+// bits 0..3), then three shuffle stages within the group (bits 4..6 = sub bits
+// 0..2).  Every lane of the warp must take part (the shuffles span the warp).
+__device__ __forceinline__ void group8_fwht128(float (&v)[16], int sub) {
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            if (i & h) continue;
+            const float a = v[i], b = v[i + h];
+            v[i] = a + b;
+            v[i + h] = a - b;
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+        // upper lane o - v, lower lane v + o: one FMA with an exact sign of +-1
+        const float sgn = (sub & m) ? -1.f : 1.f;
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const float o = __shfl_xor_sync(kFull, v[i], m);
+            v[i] = fmaf(sgn, v[i], o);
+        }
+    }
+}
+
+// 16 consecutive 16-bit values: two 16-byte loads when V16, else four 8-byte
+// loads (scale vectors need only 8-byte alignment).
+template <bool V16>
+__device__ __forceinline__ void load16x16(uint4 (&v)[2], const uint16_t *p) {
+    if constexpr (V16) {
+        v[0] = __ldg(reinterpret_cast<const uint4 *>(p));
+        v[1] = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
+    } else {
+        const uint2 a = __ldg(reinterpret_cast<const uint2 *>(p)), b = __ldg(reinterpret_cast<const uint2 *>(p) + 1);
+        const uint2 c = __ldg(reinterpret_cast<const uint2 *>(p) + 2), d = __ldg(reinterpret_cast<const uint2 *>(p) + 3);
+        v[0] = make_uint4(a.x, a.y, b.x, b.y);
+        v[1] = make_uint4(c.x, c.y, d.x, d.y);
+    }
+}
+
+// Half i (0..15) of 16 consecutive 16-bit values held in two uint4.
+__device__ __forceinline__ uint32_t half_bits(const uint4 (&v)[2], int i) {
+    const uint4 &q = v[i >> 3];
+    const uint32_t w = (i & 4) ? ((i & 2) ? q.w : q.z) : ((i & 2) ? q.y : q.x);
+    return (w >> (16 * (i & 1))) & 0xFFFFu;
+}
+
 // ---------------------------------------------------------------- MMA
 // D += A * B, m16n8k16, fp16 operands, fp32 accumulate (legacy warp-level MMA).
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,

@@ -19,21 +19,6 @@ namespace exl3 {
 // --------------------------------------------------------------------------
 constexpr int kPtSteps = 2;
 
-// 16 consecutive 16-bit values: two 16-byte loads when V16, else four 8-byte loads
-// (scale vectors and the pre-transform's own arguments need only 8-byte alignment)
-template <bool V16>
-__device__ __forceinline__ void load16(uint4 (&v)[2], const uint16_t *p) {
-    if constexpr (V16) {
-        v[0] = __ldg(reinterpret_cast<const uint4 *>(p));
-        v[1] = __ldg(reinterpret_cast<const uint4 *>(p) + 1);
-    } else {
-        const uint2 a = __ldg(reinterpret_cast<const uint2 *>(p)), b = __ldg(reinterpret_cast<const uint2 *>(p) + 1);
-        const uint2 c = __ldg(reinterpret_cast<const uint2 *>(p) + 2), d = __ldg(reinterpret_cast<const uint2 *>(p) + 3);
-        v[0] = make_uint4(a.x, a.y, b.x, b.y);
-        v[1] = make_uint4(c.x, c.y, d.x, d.y);
-    }
-}
-
 // V16: x and u are 16-byte aligned (16-byte loads and stores of the activations)
 template <bool V16>
 __global__ void __launch_bounds__(256) pretransform_kernel(const uint16_t *__restrict__ x,
@@ -63,9 +48,9 @@ __global__ void __launch_bounds__(256) pretransform_kernel(const uint16_t *__res
             const int sh = (int)(r / M);
             c0[k] = (int)(B - r * nb) * kHad + 16 * sub;
             row[k] = r;
-            load16<V16>(xv[k], x + (r - sh * M) * IC + c0[k]);
-            load16<false>(sv[k], p.s_in[sh] + c0[k]);
-            load16<false>(rv[k], p.rin[sh] + c0[k]);
+            load16x16<V16>(xv[k], x + (r - sh * M) * IC + c0[k]);
+            load16x16<false>(sv[k], p.s_in[sh] + c0[k]);
+            load16x16<false>(rv[k], p.rin[sh] + c0[k]);
         }
     }
 #pragma unroll
@@ -74,42 +59,13 @@ __global__ void __launch_bounds__(256) pretransform_kernel(const uint16_t *__res
         // lanes of a group past the end transform zeros and store nothing (every
         // lane joins the shuffles)
         const bool live = row[k] >= 0;
-        const uint32_t xs[8] = {xv[k][0].x, xv[k][0].y, xv[k][0].z, xv[k][0].w,
-                                xv[k][1].x, xv[k][1].y, xv[k][1].z, xv[k][1].w};
-        const uint32_t ss[8] = {sv[k][0].x, sv[k][0].y, sv[k][0].z, sv[k][0].w,
-                                sv[k][1].x, sv[k][1].y, sv[k][1].z, sv[k][1].w};
-        const uint32_t rs[8] = {rv[k][0].x, rv[k][0].y, rv[k][0].z, rv[k][0].w,
-                                rv[k][1].x, rv[k][1].y, rv[k][1].z, rv[k][1].w};
         float v[16];
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-            const int bs = 16 * (i & 1);
-            v[i] = live ? (bf16_bits_to_f32((xs[i >> 1] >> bs) & 0xFFFFu) *
-                           f16_bits_to_f32((uint16_t)(ss[i >> 1] >> bs))) *
-                              f16_bits_to_f32((uint16_t)(rs[i >> 1] >> bs))
+        for (int i = 0; i < 16; i++)
+            v[i] = live ? (bf16_bits_to_f32(half_bits(xv[k], i)) * f16_bits_to_f32((uint16_t)half_bits(sv[k], i))) *
+                              f16_bits_to_f32((uint16_t)half_bits(rv[k], i))
                         : 0.f;
-        }
-#pragma unroll
-        for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-            for (int i = 0; i < 16; i++) {
-                if (i & h) continue;
-                const float a = v[i], b = v[i + h];
-                v[i] = a + b;
-                v[i + h] = a - b;
-            }
-        }
-#pragma unroll
-        for (int m = 1; m < 8; m <<= 1) {
-            // the lane holding the upper index takes o - v, the lower v + o: one FMA
-            // with a sign of +-1 (exact, the same single rounding)
-            const float sgn = (sub & m) ? -1.f : 1.f;
-#pragma unroll
-            for (int i = 0; i < 16; i++) {
-                const float o = __shfl_xor_sync(kFull, v[i], m);
-                v[i] = fmaf(sgn, v[i], o);
-            }
-        }
+        group8_fwht128(v, sub);
         if (!live) continue;
         uint32_t o[8];
 #pragma unroll
