@@ -124,23 +124,23 @@ __device__ __forceinline__ void lds_quarter(uint32_t (&w)[2 * K], uint32_t addr)
 // oc_tile is spread over the lanes so that each half-warp's 8-byte stores hit
 // 16 distinct bank pairs.
 
-// Wait for a stage's code, load this thread's quarter, release the ring slot.
+// Wait for a stage's code and load this thread's quarter into registers.  The
+// ring slot stays held until the quarter is decoded (ft_decode_quarter).
 template <int K>
 __device__ __forceinline__ bool ft_fetch(const FusedArgs &a, uint32_t (&w)[2 * K], uint32_t cfull, uint32_t cph,
-                                         uint32_t cempty, uint32_t code_slot, int kt, int oc_tile, int q, int lane,
-                                         volatile int *abort) {
+                                         uint32_t code_slot, int kt, int oc_tile, int q, volatile int *abort) {
     if (!__all_sync(kFull, mbar_wait(cfull, cph, a.err, abort))) return false;
     lds_quarter<K>(w, code_slot + (uint32_t)(kt * 256 * K + oc_tile * 32 * K + q * 8 * K));
-    __syncwarp();
-    if (lane == 0) mbar_arrive(cempty);
     return true;
 }
 
-// Decode a quarter held in registers into its A slot, then publish it to the MMA issuer.
+// Decode a quarter held in registers into its A slot, publish it to the MMA
+// issuer and release the code slot it came from.
 template <int K>
 __device__ __forceinline__ bool ft_decode_quarter(const FusedArgs &a, const uint32_t (&w)[2 * K], uint32_t empty,
-                                                  uint32_t empty_parity, uint32_t full, uint32_t a_base, int kt,
-                                                  int oc_tile, int q, int lane, volatile int *abort) {
+                                                  uint32_t empty_parity, uint32_t full, uint32_t cempty,
+                                                  uint32_t a_base, int kt, int oc_tile, int q, int lane,
+                                                  volatile int *abort) {
     if (!__all_sync(kFull, mbar_wait(empty, empty_parity, a.err, abort))) return false;
     QuarterStream<K> st;
     st.build(w, quarter_prev_word(w[2 * K - 1], lane));
@@ -156,11 +156,18 @@ __device__ __forceinline__ bool ft_decode_quarter(const FusedArgs &a, const uint
         const uint32_t addr = a_base + (uint32_t)(c * 8 + oc_tile) * 128u + off;
         asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(w01), "r"(w23) : "memory");
     }
-    // every thread makes its generic-proxy stores visible to the tensor core's
-    // async proxy; then one arrival per warp
+    // Every thread orders its generic-proxy accesses of shared memory before what
+    // the async proxy does next: its stores to the A slot before the MMAs read
+    // them, and its loads of the code slot before the next TMA copy into that
+    // slot (a write-after-read across proxies, which the mbarrier alone does not
+    // order: released without this fence, a slot was seen overwritten before the
+    // last warp had read it).  Then one arrival per warp on each barrier.
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
-    if (lane == 0) mbar_arrive(full);
+    if (lane == 0) {
+        mbar_arrive(full);
+        mbar_arrive(cempty);
+    }
     return true;
 }
 
@@ -178,13 +185,14 @@ __device__ __forceinline__ bool ft_decode_run(const FusedArgs &a, uint32_t code_
                                               volatile int *abort) {
     for (; g < end; g += FT_NGROUPS) {
         uint32_t w[2 * K];
-        if (!ft_fetch<K>(a, w, bar0 + 8u * (B_CFULL + ds.cs), ds.cph, bar0 + 8u * (B_CEMPTY + ds.cs),
-                         code_base + ds.cs * FT_CSLOT, kt, oc_tile, q, lane, abort))
+        const uint32_t cempty = bar0 + 8u * (B_CEMPTY + ds.cs);
+        if (!ft_fetch<K>(a, w, bar0 + 8u * (B_CFULL + ds.cs), ds.cph, code_base + ds.cs * FT_CSLOT, kt, oc_tile, q,
+                         abort))
             return false;
         ds.cs += FT_NGROUPS;
         if (ds.cs >= CSTAGES) { ds.cs -= CSTAGES; ds.cph ^= 1; }
         if (!ft_decode_quarter<K>(a, w, bar0 + 8u * (B_EMPTY + ds.slot), ds.eph, bar0 + 8u * (B_FULL + ds.slot),
-                                  a_ring + ds.slot * FT_A_BYTES, kt, oc_tile, q, lane, abort))
+                                  cempty, a_ring + ds.slot * FT_A_BYTES, kt, oc_tile, q, lane, abort))
             return false;
         ds.slot += FT_NGROUPS;
         if (ds.slot >= FT_ASLOTS) { ds.slot -= FT_ASLOTS; ds.eph ^= 1; }

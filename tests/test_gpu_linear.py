@@ -351,6 +351,29 @@ def test_fused_repeated_calls_deterministic():
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("M", (64, 96, 128))
+def test_fused_back_to_back_calls_bitwise_stable(M):
+    # Merged gate/up calls issued back to back on one workspace, no host sync in
+    # between.  The split-K partials are summed in CTA order, so every call must
+    # give identical bits.  A code-ring slot handed to the next TMA copy before
+    # every decoder warp had read it showed up here as about one wrong split
+    # column group per call.
+    n = 60
+    x, shards = syn.gate_up(1, M=M)
+    OC = shards[0].code.shape[1] * 16
+    sets = [shard_set(sh, i * OC) for i, sh in enumerate(shards)]
+    ws = m.workspace(m.exl3_linear_shards_workspace_bytes(M, x.shape[1], sets))
+    xd = dev(x, torch.bfloat16)
+    outs = torch.empty((n, M, 2 * OC), dtype=torch.bfloat16, device="cuda")
+    for i in range(n):
+        m.exl3_linear_into_shards(xd, sets, outs[i], ws)
+    o = outs.view(torch.int16)
+    bad = (o != o[:1]).view(n, M, -1, 128).any(dim=3).any(dim=1)   # [call][column group]
+    calls, groups = torch.nonzero(bad, as_tuple=True)
+    assert calls.numel() == 0, f"calls {calls.unique().tolist()} differ in groups {groups.unique().tolist()}"
+    assert m.exl3_workspace_error(ws) == 0
+
+
 def test_fused_single_stage_segments(pin_gemm_path):
     # IC = 128: two stages per column group, so CTAs at group boundaries get
     # one-stage segments that only one of the two MMA issuers accumulates
