@@ -252,8 +252,14 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    // everything below reads what the preceding kernel (the pre-transform) wrote
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Rows mode reads the entry lists the preceding kernel (the routing) built, so
+    // it waits for that kernel here.  Dense mode takes from the preceding kernel
+    // (the pre-transform) only the activations and the row scales: the two roles
+    // that read them, the B producer and the epilogue, wait before their first
+    // access, and the code fetch and the decode start while that kernel still
+    // runs.  Before its wait a role reads only the code (never written by a kernel)
+    // and writes only shared and tensor memory.
+    if constexpr (ROWS) asm volatile("griddepcontrol.wait;" ::: "memory");
 
     int n_groups = 0;
     if constexpr (ROWS) {
@@ -383,6 +389,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
     } else if (warp == W_BLOAD) {
         // ---------------- TMA producer of the B tiles, two stages per chunk
         if (lane == 0) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");   // the activations
             bool ok = true;
             FT_FOR_SEGMENTS({
                 if (!ok) break;
@@ -461,6 +468,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
         })
     } else {
         // ---------------- epilogue, warps 4..7 (128 threads, named barrier 1)
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // the row scales; outputs after the preceding kernel
         const int r = (warp & 3) * 32 + lane;         // TMEM lane = operand row of this thread
         const int et = (warp - W_EPI) * 32 + lane;    // 0..127
         const int ti = et >> 2, part = et & 3;        // transpose phase: row in chunk, quarter of the block
