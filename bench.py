@@ -455,9 +455,11 @@ class Moe:
             self.touched.append(int(per_slot[slots].sum()))
         bank_mb = (self.bank["w13"].numel() + self.bank["w2"].numel()) * 2 / 1e6
         self.l2 = f"{R} rotating token batches (different experts per step; bank {bank_mb:.0f} MB)"
-        # top-k, then (one 8-row block per entry) routing + rotation, FC1 with the activation
-        # in its epilogue, FC2 with the combine; otherwise route, rotate, FC1, act, FC2, combine
-        self.launches_per_step = 4 if self.T * self.TOPK <= 4 * self.E else 7
+        # one 8-row block per entry: top-k (inside the routing launch up to 8 tokens),
+        # routing + rotation, FC1 with the activation in its epilogue, FC2 with the
+        # combine; otherwise top-k, route, rotate, FC1, act, FC2, combine
+        chain = self.T * self.TOPK <= 4 * self.E
+        self.launches_per_step = (3 if self.T <= 8 else 4) if chain else 7
 
     def step(self, r, x=None):
         # the layer from router logits in one call (top-k, routing, FC1, FC2, combine)

@@ -23,8 +23,9 @@
  *   - bf16 and fp16 values are passed as uint16_t bit patterns.
  *   - Code tensors are int16 [IC/16][OC/16][16*K], one block of 16*K words per
  *     16x16 weight tile, the first index along the input channels
- *     (radiance_escha.py: "_TILE = 16  # code tensor is [IC//16, OC//16, 16*K]";
- *     K = last dim / 16).  K must be 2, 3 or 4.
+ *     (radiance_escha.py: the module's 16-wide tile constant and the code
+ *     tensor shape it documents; K is the last dimension divided by 16).  K must
+ *     be 2, 3 or 4.
  *   - IC and OC must be multiples of 128: the incoherence transform is blocked
  *     at 128 channels and a boundary inside a block would change the transform
  *     (radiance_escha.py, create_weights / process_weights_after_loading).
@@ -32,7 +33,7 @@
  *     returns EXL3_EINVAL (nothing is launched) and exl3_last_error() names the
  *     sizes involved.  No entry point aborts the process.
  *   - M == 0 (no rows) is a no-op returning EXL3_OK (radiance_escha.py,
- *     escha_linear_into: "if M == 0: return").
+ *     escha_linear_into returns at once when there are no rows).
  *
  * Trellis decode reading (the pages give only the tensor shapes): a tile's
  * 16K words are a stream read most-significant bit first; weight t (0..255,
@@ -204,10 +205,10 @@ exl3_status exl3_linear_into_noalloc(const uint16_t *x, int64_t M, int32_t IC,
  */
 /*
  * Codebook of a tensor.  EXL3 checkpoints mark a tensor's codebook with
- * per-tensor marker entries (vllm-quantpack linear.py, LINEAR_SUFFIXES: "mcg"
- * and "mul1" beside "trellis", read as present / absent per shard; the vLLM
- * PR #190 thread: "mcg/mul1 sentinel semantics", MCG-marked modules on one
- * kernel, legacy and MUL1 shards on another).  The pages give neither
+ * per-tensor marker entries (vllm-quantpack linear.py, LINEAR_SUFFIXES lists
+ * mcg and mul1 beside trellis, read as present / absent per shard; in the vLLM
+ * PR #190 thread a commit treats the two markers as sentinels and sends
+ * MCG-marked modules to one kernel, legacy and MUL1 shards to another).  The pages give neither
  * variant's constants, so this build decodes the default (3INST) codebook only:
  * a shard marked MCG or MUL1 returns EXL3_EUNSUPPORTED before any launch.
  */
@@ -464,8 +465,8 @@ exl3_status exl3_moe_forward(const uint16_t *x, const float *logits, int32_t T, 
 
 /*
  * int8 embedding gather with per-row scale (vllm-quantpack exl3/embedding.py,
- * embedding(): "dequantized on the GATHERED rows so the table itself stays
- * int8"):  out[i][:] = bf16(q[ids[i]][:] * scale[ids[i]]), one rounding.
+ * embedding(): only the gathered rows are converted, so the table stays int8
+ * in memory):  out[i][:] = bf16(q[ids[i]][:] * scale[ids[i]]), one rounding.
  *   q int8 [V][H] (row-major), scale fp16 [V], ids int32 [N], out bf16 [N][H].
  * An id outside [0, V) writes a row of zeros (the masking vLLM's vocab-parallel
  * embedding applies, same file's module docstring) and, if n_bad (device

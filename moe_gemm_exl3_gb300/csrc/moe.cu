@@ -2,6 +2,8 @@
 // w13 = [w1 | w3] per K-sorted slot, w2, fp16 suh/svh vectors [E, ...]).
 //
 // Launch chain, all on the caller's stream, no host synchronization:
+//   top-k     (from router logits) ids and softmax weights, one warp per token;
+//             for a few tokens inside the routing launch
 //   route     ids -> expert-sorted rows (stable counting sort), per-row slot,
 //             per-pair row position, and the grouped-GEMM entry lists
 //   rotate    u1 = Had(x_t * w13_suh[p][0]), u3 = Had(x_t * w13_suh[p][1]) per
@@ -40,6 +42,8 @@ constexpr int kMoeMaxTopk = 32;
 // y) sit in the upper half of the workspace counters; the grouped GEMMs' split-K
 // counters use the lower half.
 constexpr int64_t kCombCounterBase = 32768;
+// Tokens up to which the small-T chain folds the top-k into its first launch.
+constexpr int kFoldTopkTokens = 8;
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -115,13 +119,13 @@ MoeLayout moe_layout(int T, int H, int I, int E, int topk) {
 }
 
 // ------------------------------------------------------------------ top-k
-// One warp per token: each lane holds the logits e = lane, lane + 32, ...; each
-// of the topk rounds is a warp arg-max (largest logit, ties to the lower expert
-// id); then softmax over the selected logits.  Lane k < topk ends with the k-th
-// choice's expert id (*id) and weight (*wt).
-__device__ __forceinline__ void topk_warp(const float *__restrict__ l, int E, int topk, int lane, int *id,
-                                          float *wt) {
-    constexpr int PER = kMoeMaxE / 32;
+// One warp per token: each lane holds the logits e = lane, lane + 32, ... (PER of
+// them, E <= 32 PER); each of the topk rounds is a warp arg-max (largest logit,
+// ties to the lower expert id); then softmax over the selected logits.  Lane
+// k < topk ends with the k-th choice's expert id (*id) and weight (*wt).
+template <int PER>
+__device__ __forceinline__ void topk_warp_n(const float *__restrict__ l, int E, int topk, int lane, int *id,
+                                            float *wt) {
     float v[PER];
 #pragma unroll
     for (int i = 0; i < PER; i++) {
@@ -160,6 +164,21 @@ __device__ __forceinline__ void topk_warp(const float *__restrict__ l, int E, in
         }
     }
     *wt = my_sel / den;
+}
+
+// The rounds run over as few logits per lane as E needs (each round is on the
+// layer's critical path): 4 per lane for E <= 128.
+__device__ __forceinline__ void topk_warp(const float *__restrict__ l, int E, int topk, int lane, int *id,
+                                          float *wt) {
+    static_assert(kMoeMaxE == 32 * 32, "the widest instance holds 32 logits per lane");
+    if (E <= 128)
+        topk_warp_n<4>(l, E, topk, lane, id, wt);
+    else if (E <= 256)
+        topk_warp_n<8>(l, E, topk, lane, id, wt);
+    else if (E <= 512)
+        topk_warp_n<16>(l, E, topk, lane, id, wt);
+    else
+        topk_warp_n<32>(l, E, topk, lane, id, wt);
 }
 
 __global__ void __launch_bounds__(256) topk_softmax_kernel(const float *__restrict__ logits, int T, int E, int topk,
@@ -446,14 +465,29 @@ struct PairRotateArgs {
     const int32_t *ids;
     int R, topk, E, H;
     exl3_moe_bank bank;
-    uint16_t *u;   // fp16 [2][R][H]
+    uint16_t *u;         // fp16 [2][R][H]
+    const float *logits; // non-null: the ids are this launch's own top-k of the logits [T][E]
 };
 
 __device__ __forceinline__ void rotate_pairs(const PairRotateArgs &a, int wid, int nwarps, int lane) {
     const int blocks = a.H / kHad;
+    int t_have = -1, id_have = 0;   // the token whose top-k this warp holds, lane k's choice
     for (int task = wid; task < a.R * blocks; task += nwarps) {
         const int i = task / blocks, c = (task - i * blocks) * kHad + 4 * lane;
-        const int e = a.ids[i];
+        int e;
+        if (a.logits) {
+            // the warp ranks the token's logits itself (the same result as the routing
+            // CTA's, which writes ids and w) rather than wait for another CTA
+            const int t = i / a.topk;
+            if (t != t_have) {
+                float unused;
+                topk_warp(a.logits + (int64_t)t * a.E, a.E, a.topk, lane, &id_have, &unused);
+                t_have = t;
+            }
+            e = __shfl_sync(kFull, id_have, i - t * a.topk);
+        } else {
+            e = a.ids[i];
+        }
         if (e < 0 || e >= a.E) continue;
         const int p = a.bank.perm[e];
         if (p < 0 || p >= a.E) continue;
@@ -483,12 +517,30 @@ __device__ __forceinline__ void rotate_pairs(const PairRotateArgs &a, int wid, i
 }
 
 // The first kernel of the small-T chain: CTA 0 routes, the others rotate the
-// pairs' inputs meanwhile (both need only the ids).
-__global__ void __launch_bounds__(1024) route_rotate_kernel(const RouteArgs a, const PairRotateArgs r) {
-    // launched as a dependent of the router: wait for its ids; let FC1 be scheduled
+// pairs' inputs meanwhile (both need only the ids).  With router logits (r.logits
+// non-null) CTA 0 first takes each token's top-k (one warp per token) and writes
+// them to ids_out (the ids the routing reads) and w_out, and every rotating warp
+// ranks its own token's logits.
+__global__ void __launch_bounds__(1024) route_rotate_kernel(const RouteArgs a, const PairRotateArgs r,
+                                                            int32_t *ids_out, float *w_out) {
+    // launched as a dependent of the kernel that wrote the ids or the logits: wait
+    // for it; let FC1 be scheduled
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
     if (blockIdx.x == 0) {
+        if (r.logits) {
+            const int lane = threadIdx.x & 31, T = a.R / a.topk;
+            for (int t = threadIdx.x >> 5; t < T; t += blockDim.x >> 5) {
+                int id = 0;
+                float wt = 0.f;
+                topk_warp(r.logits + (int64_t)t * a.E, a.E, a.topk, lane, &id, &wt);
+                if (lane < a.topk) {
+                    ids_out[(int64_t)t * a.topk + lane] = id;
+                    w_out[(int64_t)t * a.topk + lane] = wt;
+                }
+            }
+            __syncthreads();   // the routing below reads the ids
+        }
         route_body(a);
         return;
     }
@@ -729,13 +781,18 @@ exl3_status moe_layer(const char *fn, const uint16_t *x, const float *logits, in
     cudaLaunchAttribute pdl_attr[1];
     pdl_attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl_attr[0].val.programmaticStreamSerializationAllowed = 1;
-    if (logits) {
+    // At a few tokens the chain's first launch takes the top-k itself (one launch
+    // fewer; every rotating warp then ranks its own token's logits, which costs
+    // more than the launch it saves once there are many routes: T = 64 measured
+    // 198.7 -> 206.2 us, T = 1 36.9 -> 35.7 us).
+    const bool fold_topk = logits && chain && T <= kFoldTopkTokens;
+    if (logits && !fold_topk) {
         // the routing below reads ids and w: the top-k first (a programmatic
         // dependent of whatever precedes the layer, and the routing of it)
         if ((e = launch_topk(logits, T, E, topk, ids, w, s)) != cudaSuccess) return cuda_fail(e, "moe: top-k");
     }
     if (chain) {
-        PairRotateArgs pr = {x, ids, R, topk, E, H, b, u13};
+        PairRotateArgs pr = {x, ids, R, topk, E, H, b, u13, fold_topk ? logits : nullptr};
         const int64_t tasks = (int64_t)R * (H / kHad);
         const int64_t rot_ctas = (tasks + 31) / 32 < 4 * (int64_t)device_info().sm_count ? (tasks + 31) / 32
                                                                                           : 4 * (int64_t)device_info().sm_count;
@@ -745,7 +802,7 @@ exl3_status moe_layer(const char *fn, const uint16_t *x, const float *logits, in
         cfg.stream = s;
         cfg.attrs = pdl_attr;
         cfg.numAttrs = 1;
-        if ((e = cudaLaunchKernelEx(&cfg, route_rotate_kernel, ra, pr)) != cudaSuccess)
+        if ((e = cudaLaunchKernelEx(&cfg, route_rotate_kernel, ra, pr, ids, w)) != cudaSuccess)
             return cuda_fail(e, "moe_grouped: route");
         GroupGemmArgs g1 = {};
         g1.u = u13;

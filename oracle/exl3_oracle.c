@@ -15,13 +15,13 @@
  *
  * Sources (web pages this reference restates):
  *   [escha]  radiance_escha.py (vLLM method for escha EXL3 trellis W2
- *            checkpoints): module docstring "THE FORWARD", the two "easy
- *            mistakes", the per-shard rationale; process_weights_after_loading
+ *            checkpoints): module docstring "THE FORWARD", the two mistakes
+ *            it warns about, the per-shard rationale; process_weights_after_loading
  *            (code tensor [IC/16, OC/16, 16K], K = last dim / 16, rin per
  *            shard); escha_linear_into (M == 0 no-op, ldo / col0 slice).
- *   [linear] vllm-quantpack 0.1.0, exl3/linear.py: module docstring
- *            ("packed tail-biting trellis", "bitrate implied by the trellis
- *            width"), Exl3LinearMethod._forward (one GEMM per shard).
+ *   [linear] vllm-quantpack 0.1.0, exl3/linear.py: module docstring (the
+ *            code is a packed, tail-biting trellis whose width gives the
+ *            bitrate), Exl3LinearMethod._forward (one GEMM per shard).
  *   [embed]  vllm-quantpack 0.1.0, exl3/embedding.py: embedding() --
  *            q[ids] converted, times s[ids].
  *   [bank]   bank.py (one layer's EXL3 expert bank): w13 = [w1 | w3] per
