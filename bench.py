@@ -379,15 +379,16 @@ class Prefill:
                                                                            self.out, 0, self.ws), 8)
         ms_rec = kernel_time_ms(torch, stream, lambda j: m.exl3_reconstruct(self.code, self.K, W), 8)
         ms = ms_all - ms_rec
-        _, burst, _ = peaks()
-        tf, src = sustained_tflops()
+        _, burst, src = peaks()
+        ts, _ = sustained_tflops()
         fl = 2.0 * self.M * self.IC * self.OC
         a = fl / (ms * 1e-3) / 1e12
+        # timed alone (a few graph replays, tens of ms): the burst peak
         return {"bound": "tensor", "kernel": "prefill_gemm_kernel (tcgen05 128x256 tiles)",
-                "achieved": round(a, 1), "peak": tf, "unit": "TFLOP/s", "frac": round(a / tf, 4),
-                "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops_sustained: timed inside a long run of "
-                               f"steps under the power cap; fp16 has the same dense rate)",
-                "frac_of_burst": round(a / burst, 4),
+                "achieved": round(a, 1), "peak": burst, "unit": "TFLOP/s", "frac": round(a / burst, 4),
+                "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops burst: the kernel timed alone; fp16 has "
+                               f"the same dense rate)",
+                "frac_of_sustained": round(a / ts, 4),
                 "traffic": profile_traffic(f"prefill_gemm_m{self.M}.json", ["prefill.cu", "tc_ptx.cuh", "common.cuh"]),
                 "per_launch_us": round(ms * 1e3, 1), "reconstruct_us": round(ms_rec * 1e3, 1),
                 "algorithmic_flops_per_launch": fl}
@@ -610,11 +611,12 @@ class Layer:
                     "code_bytes": self.code_bytes}
         fl = sum(2.0 * self.M * sh.IC * sh.OC for _, _, sh in self.projs)
         a = fl / (ms * 1e-3) / 1e12
-        ts, tsrc = sustained_tflops()
+        ts, _ = sustained_tflops()
+        # timed alone (a few graph replays, tens of ms): the burst peak
         return {"bound": "tensor", "kernel": "the layer's launches (flops / layer time)", "achieved": round(a, 1),
-                "peak": ts, "unit": "TFLOP/s", "frac": round(a / ts, 4),
-                "peak_source": f"{tsrc} (MEASURED_PEAKS.json bf16_tflops_sustained: a long run of steps)",
-                "frac_of_burst": round(a / tf, 4), "traffic": None, "per_layer_us": round(ms * 1e3, 1)}
+                "peak": tf, "unit": "TFLOP/s", "frac": round(a / tf, 4),
+                "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops burst: the layer timed alone)",
+                "frac_of_sustained": round(a / ts, 4), "traffic": None, "per_layer_us": round(ms * 1e3, 1)}
 
     def e2e_io(self, torch, dev):
         xh = torch.from_numpy(np.ascontiguousarray(self.projs[0][1]).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -678,11 +680,12 @@ class LmHead:
                     "per_launch_us": round(ms * 1e3, 2), "algorithmic_bytes_per_launch": alg}
         fl = 2.0 * self.M * self.H * self.V
         a = fl / (ms * 1e-3) / 1e12
-        ts, tsrc = sustained_tflops()
+        ts, _ = sustained_tflops()
+        # timed alone (a few graph replays, tens of ms): the burst peak
         return {"bound": "tensor", "kernel": "int8->fp16 chunks + prefill_gemm_kernel (row-scale epilogue)",
-                "achieved": round(a, 1), "peak": ts, "unit": "TFLOP/s", "frac": round(a / ts, 4),
-                "peak_source": f"{tsrc} (MEASURED_PEAKS.json bf16_tflops_sustained: a long run of steps)",
-                "frac_of_burst": round(a / tf, 4), "traffic": None, "per_call_us": round(ms * 1e3, 1)}
+                "achieved": round(a, 1), "peak": tf, "unit": "TFLOP/s", "frac": round(a / tf, 4),
+                "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops burst: the call timed alone)",
+                "frac_of_sustained": round(a / ts, 4), "traffic": None, "per_call_us": round(ms * 1e3, 1)}
 
     def e2e_io(self, torch, dev):
         xh = torch.from_numpy(self.xnp[0].view(np.int16)).view(torch.bfloat16).pin_memory()
