@@ -222,6 +222,25 @@ def test_moe_fused_gemm_deterministic(full_bank, pin_gemm_path):
     assert m.exl3_workspace_error(ws) == 0
 
 
+@pytest.mark.parametrize("T", (1, 16, 512))
+def test_moe_forward_back_to_back_bitwise_stable(full_bank, T):
+    # Layers issued back to back on one workspace without a host sync give identical
+    # bits (T = 512 runs FC1 and FC2 on the tensor-core GEMM in rows mode, whose code
+    # ring is filled by bulk copies and must not be overwritten before it is read).
+    n = 24
+    bank, bank_d = full_bank
+    x, logits = syn.moe_tokens(80 + T, T)
+    xd, ld = dev(x, torch.bfloat16), dev(logits, torch.float32)
+    ws = m.workspace(m.exl3_moe_workspace_bytes(T, 2048, 768, 128, 8))
+    ys = torch.empty((n, T, 2048), dtype=torch.bfloat16, device="cuda")
+    for i in range(n):
+        m.exl3_moe_forward(xd, ld, 8, bank_d, ws, y=ys[i])
+    o = ys.view(torch.int16)
+    bad = (o != o[:1]).view(n, -1).any(dim=1)
+    assert not bool(bad.any()), f"calls {torch.nonzero(bad).flatten().tolist()} differ from the first"
+    assert m.exl3_workspace_error(ws) == 0
+
+
 @pytest.mark.parametrize("T", (1, 16, 64, 65, 512))
 def test_moe_forward_equals_topk_then_grouped(full_bank, T):
     # the one-call layer from logits (top-k inside the routing launch for small T)
