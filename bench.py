@@ -531,7 +531,7 @@ class Gather:
         a = alg / (ms * 1e-3) / 1e9
         return {"bound": "hbm", "kernel": "gather_kernel", "achieved": round(a, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(a / hbm, 4), "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
-                "traffic": profile_traffic("gather_8192.json", ["gather.cu"]), "per_launch_us": round(ms * 1e3, 2),
+                "traffic": profile_traffic("gather_8192.json", ["gather.cu", "common.cuh"]), "per_launch_us": round(ms * 1e3, 2),
                 "algorithmic_bytes_per_launch": alg}
 
     def e2e_io(self, torch, dev):
