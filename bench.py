@@ -142,15 +142,18 @@ def kernel_time_ms(torch, stream, fn, n, reps=4):
     return e0.elapsed_time(e1) / (reps * n)
 
 
-def profile_traffic(name, src_files):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the current sources."""
+def profile_traffic(name):
+    """DRAM bytes per launch from a committed ncu record, if the source files it lists
+    (the kernel's own) still hash to what they were when it was captured."""
     p = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
+    if not d.get("source_files"):
+        return None
     h = hashlib.sha256()
-    for s in src_files:
+    for s in d["source_files"]:
         with open(os.path.join(ROOT, "moe_gemm_exl3_gb300", "csrc", s), "rb") as f:
             h.update(f.read())
     if d.get("source_sha256_16") != h.hexdigest()[:16]:
@@ -248,10 +251,8 @@ class GateUp:
         return {"bound": "hbm", "kernel": kernel + " (gate K=2 + up K=3 in one call)",
                 "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
-                "traffic": {"decode": lambda: profile_traffic(f"decode_gemm_gate_up_m{self.M}.json",
-                                                              ["linear.cu", "decode.cuh", "common.cuh"]),
-                            "fused": lambda: profile_traffic(f"fused_gemm_gate_up_m{self.M}.json",
-                                                             ["fused_tc.cu", "tc_ptx.cuh", "common.cuh"]),
+                "traffic": {"decode": lambda: profile_traffic(f"decode_gemm_gate_up_m{self.M}.json"),
+                            "fused": lambda: profile_traffic(f"fused_gemm_gate_up_m{self.M}.json"),
                             "prefill": lambda: None}[gemm_path(self.M)](),
                 "per_launch_us": round(ms * 1e3, 2), "algorithmic_bytes_per_launch": alg,
                 "code_GBps": round(sum(self.code_bytes(K) for K in self.KS) / (ms * 1e-3) / 1e9, 1)}
@@ -389,7 +390,7 @@ class Prefill:
                 "peak_source": f"{src} (MEASURED_PEAKS.json bf16_tflops burst: the kernel timed alone; fp16 has "
                                f"the same dense rate)",
                 "frac_of_sustained": round(a / ts, 4),
-                "traffic": profile_traffic(f"prefill_gemm_m{self.M}.json", ["prefill.cu", "tc_ptx.cuh", "common.cuh"]),
+                "traffic": profile_traffic(f"prefill_gemm_m{self.M}.json"),
                 "per_launch_us": round(ms * 1e3, 1), "reconstruct_us": round(ms_rec * 1e3, 1),
                 "algorithmic_flops_per_launch": fl}
 
@@ -531,7 +532,7 @@ class Gather:
         a = alg / (ms * 1e-3) / 1e9
         return {"bound": "hbm", "kernel": "gather_kernel", "achieved": round(a, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(a / hbm, 4), "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
-                "traffic": profile_traffic("gather_8192.json", ["gather.cu", "common.cuh"]), "per_launch_us": round(ms * 1e3, 2),
+                "traffic": profile_traffic("gather_8192.json"), "per_launch_us": round(ms * 1e3, 2),
                 "algorithmic_bytes_per_launch": alg}
 
     def e2e_io(self, torch, dev):
@@ -676,7 +677,7 @@ class LmHead:
             return {"bound": "hbm", "kernel": "lm_head_decode_kernel (int8 table streamed, mma.sync)",
                     "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
-                    "traffic": profile_traffic(f"lm_head_decode_m{self.M}.json", ["lm_head.cu", "common.cuh"]),
+                    "traffic": profile_traffic(f"lm_head_decode_m{self.M}.json"),
                     "per_launch_us": round(ms * 1e3, 2), "algorithmic_bytes_per_launch": alg}
         fl = 2.0 * self.M * self.H * self.V
         a = fl / (ms * 1e-3) / 1e12
