@@ -767,10 +767,11 @@ exl3_status moe_layer(const char *fn, const uint16_t *x, const float *logits, in
     cudaStream_t s = (cudaStream_t)stream;
     const int R = L.R;
 
-    // One 8-row block per entry: four launches (route with the per-pair input
-    // rotation alongside, FC1 on the pairs' rows, the activation, FC2 with the
-    // weighted combine in its epilogue), chained as programmatic dependents.
-    // Otherwise the separate passes below.
+    // One 8-row block per entry: the routing with the per-pair input rotation
+    // alongside (and, up to kFoldTopkTokens tokens, the top-k), FC1 on the pairs'
+    // rows with the activation in its epilogue, FC2 with the weighted combine in
+    // its epilogue, chained as programmatic dependents.  Otherwise the separate
+    // passes below.
     const int GH = H / kHad;
     const bool chain = !L.fused && L.nb == 1 &&
                        (int64_t)L.max_entries * (2 * (I / kHad) > GH ? 2 * (I / kHad) : GH) <= kCombCounterBase &&
