@@ -38,11 +38,10 @@ constexpr size_t group_smem_bytes() {
 //   kUGather  row gather_rows[r0 + g] of half j of u (j = e.u_row0 >= R_half,
 //             r0 = e.u_row0 - j * R_half): activations stored per (token, route)
 //             pair rather than per routed row
-//   kUShared  shared memory: row g, channels [c0s, c0s + nch) at su[g * nch + c - c0s]
 //   kUCodes   8-bit activation codes (uint8 q + 128, rows e.u_row0 + g of u read
 //             as bytes); the MMA multiplies q exactly, the row scale is applied by
 //             the epilogue
-enum USrc { kUGlobal = 0, kUGather = 1, kUShared = 2, kUCodes = 3 };
+enum USrc { kUGlobal = 0, kUGather = 1, kUCodes = 2 };
 
 // Four 8-bit activation codes (q + 128) -> each q (exact) duplicated into a half2.
 __device__ __forceinline__ void codes_to_dup_f16(uint32_t w, uint32_t (&b)[4]) {
@@ -60,9 +59,8 @@ template <int K, int NB, int USRC = kUGlobal>
 __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const GroupEntry &e, const uint16_t *u,
                                                  int IC, int G, int a_lo, int a_hi, int lane, int warp,
                                                  uint32_t hx, const uint32_t *pow2,
-                                                 const int32_t *gather_rows = nullptr, int R_half = 0,
-                                                 const uint16_t *su = nullptr, int nch = 0, int c0s = 0) {
-    static_assert(USRC == kUGlobal || NB == 1, "gathered, shared and 8-bit activation rows serve one 8-row block");
+                                                 const int32_t *gather_rows = nullptr, int R_half = 0) {
+    static_assert(USRC == kUGlobal || NB == 1, "gathered and 8-bit activation rows serve one 8-row block");
     const int g = lane >> 2, q = lane & 3;
     const int TO = e.OC / kTile;
     const uint32_t *tile0 = reinterpret_cast<const uint32_t *>(e.code) + (int64_t)(8 * G + g) * 8 * K + q * 2 * K;
@@ -122,14 +120,12 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
         }
         // codes: one byte per channel, addressed through the same pointer type (in
         // units of two channels, hence the halved offsets)
-        const uint16_t *up = USRC == kUShared ? su + g * nch + 16 * ar + 4 * q - c0s
-                           : USRC == kUCodes  ? reinterpret_cast<const uint16_t *>(
-                                                    reinterpret_cast<const uint8_t *>(u) + urow_index * IC + 16 * ar + 4 * q)
-                                              : u + urow_index * IC + 16 * ar + 4 * q;
+        const uint16_t *up = USRC == kUCodes ? reinterpret_cast<const uint16_t *>(
+                                                  reinterpret_cast<const uint8_t *>(u) + urow_index * IC + 16 * ar + 4 * q)
+                                            : u + urow_index * IC + 16 * ar + 4 * q;
         constexpr int kUS = (USRC == kUCodes ? 8 : 16) * kDecodeWarps;   // activation step per warp step
         auto ldu = [&](const uint16_t *pu) -> uint2 {
-            if constexpr (USRC == kUShared) return *reinterpret_cast<const uint2 *>(pu);
-            else if constexpr (USRC == kUCodes) return make_uint2(__ldg(reinterpret_cast<const uint32_t *>(pu)), 0u);
+            if constexpr (USRC == kUCodes) return make_uint2(__ldg(reinterpret_cast<const uint32_t *>(pu)), 0u);
             else return __ldg(reinterpret_cast<const uint2 *>(pu));
         };
         uint32_t wa[2 * K], wb[2 * K];
