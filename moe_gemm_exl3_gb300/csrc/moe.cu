@@ -456,6 +456,89 @@ __device__ __forceinline__ void route_body(const RouteArgs &a) {
 
 __global__ void __launch_bounds__(1024) route_kernel(const RouteArgs a) { route_body(a); }
 
+// The routing of at most 32 (token, choice) pairs by one warp, lane i holding pair
+// i: ranking the keys (slot, pair index) gives route_body's stable slot-major row
+// order, and with it the same positions, rows, entry lists and counts, without
+// the CTA-wide passes (tables, scans, barriers) that dominate it for a few pairs.
+__device__ __forceinline__ void route_small(const RouteArgs &a, int lane) {
+    int p = -1;
+    if (lane < a.R) {
+        const int e = a.ids[lane];
+        if (e >= 0 && e < a.E) p = a.bank.perm[e];
+        if (p >= 0 && p < a.E) {
+            const int kg = a.bank.k_gu[p], kd = a.bank.k_d[p];
+            if (kg < 2 || kg > 4 || kd < 2 || kd > 4) p = -1;
+        } else {
+            p = -1;
+        }
+        if (p < 0) record_error(a.err, kErrBadExpertId);
+    }
+    const bool valid = p >= 0;
+    const unsigned key = valid ? ((unsigned)p << 5) | (unsigned)lane : 0xFFFFFFFFu;
+    const unsigned peers = __match_any_sync(kFull, valid ? p : -1 - lane);   // lanes of the same slot
+    const int n = __popc(peers);                                             // rows of this slot
+    const bool leader = valid && (__ffs(peers) - 1) == lane;                 // its lowest pair
+    const int nchunks = leader ? (n + a.chunk - 1) / a.chunk : 0;
+    int rank = 0, ebase = 0, entries = 0;
+    for (int j = 0; j < 32; j++) {
+        const unsigned kj = __shfl_sync(kFull, key, j);
+        const int cj = __shfl_sync(kFull, nchunks, j);
+        rank += kj < key;                                   // rows before this one
+        ebase += (kj >> 5) < (key >> 5) ? cj : 0;          // entries of the slots before this one
+        entries += cj;
+    }
+    const int rows = __popc(__ballot_sync(kFull, valid));
+    if (lane < a.R) a.pos[lane] = valid ? rank : -1;
+    if (valid) {
+        a.row_pair[rank] = lane;
+        a.row_slot[rank] = p;
+    }
+    if (lane == 0) {
+        a.counts[0] = rows;
+        a.counts[1] = 2 * entries;
+        a.counts[2] = entries;
+    }
+    for (int c = 0; c < nchunks; c++) {
+        const int r0 = rank + c * a.chunk;               // the leader's rank is its slot's first row
+        const int nr = n - c * a.chunk < a.chunk ? n - c * a.chunk : a.chunk;
+        const int idx = ebase + c;
+        for (int j = 0; j < 2; j++) {
+            GroupEntry ge = {};
+            ge.code = a.bank.w13 + (j == 0 ? a.bank.off_w1[p] : a.bank.off_w3[p]);
+            ge.post = a.bank.w13_svh + ((int64_t)p * 2 + j) * a.I;
+            ge.post2 = nullptr;
+            ge.K = a.bank.k_gu[p];
+            ge.OC = a.I;
+            ge.u_row0 = j * a.R + r0;
+            ge.out_off = j * a.R + r0;
+            ge.nrows = nr;
+            ge.slot = p;
+            a.ent1[2 * idx + j] = ge;
+        }
+        GroupEntry ge = {};
+        ge.code = a.bank.w2 + a.bank.off_w2[p];
+        ge.post = a.bank.w2_svh + (int64_t)p * a.H;
+        ge.post2 = nullptr;
+        ge.K = a.bank.k_d[p];
+        ge.OC = a.H;
+        ge.u_row0 = r0;
+        ge.out_off = r0;
+        ge.nrows = nr;
+        a.ent2[idx] = ge;
+    }
+    if (a.y_zero) {
+        // tokens whose routes are all invalid get y = 0 (no combine reaches them)
+        const unsigned vb = __ballot_sync(kFull, valid);
+        const unsigned mk = a.topk >= 32 ? 0xFFFFFFFFu : (1u << a.topk) - 1u;
+        const int T = a.R / a.topk;
+        for (int t = 0; t < T; t++) {
+            if ((vb >> (t * a.topk)) & mk) continue;
+            for (int c = 8 * lane; c < a.H; c += 8 * 32)
+                *reinterpret_cast<uint4 *>(a.y_zero + (int64_t)t * a.H + c) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+}
+
 // Input rotation per (token, route) pair, before the rows are known:
 // u[j][i] = Had(x_t * w13_suh[p][j]) for pair i = t * topk + k routed to slot p
 // (pairs whose expert id, slot or bitrate is invalid are skipped; the routing
@@ -540,6 +623,10 @@ __global__ void __launch_bounds__(1024) route_rotate_kernel(const RouteArgs a, c
                 }
             }
             __syncthreads();   // the routing below reads the ids
+        }
+        if (a.R <= 32) {
+            if (threadIdx.x < 32) route_small(a, threadIdx.x);
+            return;
         }
         route_body(a);
         return;

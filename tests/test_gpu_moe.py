@@ -63,13 +63,14 @@ def test_moe_small_bank_mixed_k(T):
     assert m.exl3_workspace_error(ws) == 0
 
 
-@pytest.mark.parametrize("T", (16, 40))
-def test_moe_skewed_routing_splits_entries(T):
+@pytest.mark.parametrize("T,topk", ((16, 4), (40, 4), (16, 2)))
+def test_moe_skewed_routing_splits_entries(T, topk):
     # every token picks the same experts: each gets T rows, more than one row block
-    E, H, I, topk = 16, 256, 128, 4
+    # (16 tokens x 2 routes: the one-warp routing of at most 32 pairs, two blocks per slot)
+    E, H, I = 16, 256, 128
     bank = syn.moe_bank(21, E=E, H=H, I=I, distinct_down_k=True)
     x, logits = syn.moe_tokens(30 + T, T, H=H, E=E)
-    logits[:, [2, 7, 11, 13]] += 50.0
+    logits[:, [2, 7, 11, 13][:topk]] += 50.0
     ids, w = oracle.topk_softmax(logits, topk)
     assert len(np.unique(ids)) == topk
     y, ws = run_moe(x, ids, w, bank_dev(bank), E, H, I)
@@ -174,6 +175,25 @@ def test_moe_invalid_expert_id_is_recorded_and_skipped():
     w0 = w.copy()
     w0[2, 1] = 0.0
     assert_rows_close(as_f64(y), oracle.moe_f64(x, ids, w0, bank))
+
+
+@pytest.mark.parametrize("T", (4, 20))
+def test_moe_token_without_a_valid_route_gets_zeros(T):
+    # T = 4: the one-warp routing (8 pairs); T = 20: the CTA-wide routing (40 pairs)
+    E, H, I, topk = 6, 256, 128, 2
+    bank = syn.moe_bank(17, E=E, H=H, I=I)
+    x, logits = syn.moe_tokens(18 + T, T, H=H, E=E)
+    ids, w = oracle.topk_softmax(logits, topk)
+    bad = ids.copy()
+    bad[1, :] = [99, -3]
+    y, ws = run_moe(x, bad, w, bank_dev(bank), E, H, I)
+    assert m.exl3_workspace_error(ws) == 2
+    got = as_f64(y)
+    assert np.all(got[1] == 0.0)
+    keep = np.array([t for t in range(T) if t != 1])
+    ref = oracle.moe_f64(np.ascontiguousarray(x[keep]), np.ascontiguousarray(ids[keep]),
+                         np.ascontiguousarray(w[keep]), bank)
+    assert_rows_close(got[keep], ref)
 
 
 def test_moe_zero_tokens_is_a_no_op():
