@@ -506,7 +506,25 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                     for (int i = 0; i < 32; i++) v[i] += t[i];
                 }
             };
-            if (split) {
+            // The first contributor of a split group (its range ends in this group, so
+            // this is its last segment) usually arrives last, at the end of its work.
+            // If every other contributor has arrived already, it keeps its own part in
+            // TMEM and adds only theirs: the sum runs in the same CTA order (its own
+            // part first), so the result is the same, bit for bit.
+            // (dense launches only: in rows mode it measured slower)
+            bool own_in_tmem = false;
+            if (!ROWS && split && c == c_first) {
+                if (et == 0)
+                    *s_last = *reinterpret_cast<volatile int32_t *>(a.counters + gi) == c_last - c_first;
+                named_bar(1, 128);
+                own_in_tmem = *s_last != 0;
+                named_bar(1, 128);   // s_last is written again below
+                if (own_in_tmem) {
+                    __threadfence();   // the others wrote their partials before arriving
+                    if (et == 0) a.counters[gi] = 0;
+                }
+            }
+            if (split && !own_in_tmem) {
                 float *slot = a.partials + (int64_t)(c + gi) * frag;
                 for (int c0 = 0; c0 < rows; c0 += 32) {
                     float v[32];
@@ -527,7 +545,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                 if (et == 0) a.counters[gi] = 0;
             }
             for (int c0 = 0; c0 < rows; c0 += 32) {
-                if (split) {
+                if (split && !own_in_tmem) {
                     // sum the contributors' slabs for rows c0 .. c0 + 31 (32 x 128
                     // floats): thread et takes float4 f = et + 128 k, coalesced; two
                     // contributors' loads in flight at a time, added in ascending
@@ -569,6 +587,40 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                     load_acc(c0, v);
 #pragma unroll
                     for (int i = 0; i < 32; i++) T[i * FT_TSTRIDE + (r >> 5) * 36 + (r & 31)] = v[i];
+                    if (own_in_tmem) {
+                        // this CTA's part is in T: add the other contributors' slabs in CTA
+                        // order, every load of a contributor issued at once (thread et: float4
+                        // f = et + 128 k; a thread reads and rewrites only its own positions)
+                        named_bar(1, 128);
+                        const float4 *pbase = reinterpret_cast<const float4 *>(a.partials + (int64_t)c0 * FT_BM);
+#pragma unroll
+                        for (int kb = 0; kb < 8; kb += 4) {
+                            float4 acc[4];
+#pragma unroll
+                            for (int k = 0; k < 4; k++) {
+                                const int f = et + 128 * (kb + k), row = f >> 5, cq = f & 31;
+                                acc[k] = *reinterpret_cast<const float4 *>(T + row * FT_TSTRIDE + (cq >> 3) * 36 + 4 * (cq & 7));
+                            }
+                            for (int cc = c_first + 1; cc <= c_last; cc++) {
+                                const float4 *pc = pbase + (int64_t)(cc + gi) * (frag / 4);
+                                float4 t[4];
+#pragma unroll
+                                for (int k = 0; k < 4; k++) {
+                                    const int f = et + 128 * (kb + k);
+                                    t[k] = c0 + (f >> 5) < rows ? __ldcg(pc + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+                                }
+#pragma unroll
+                                for (int k = 0; k < 4; k++) {
+                                    acc[k].x += t[k].x; acc[k].y += t[k].y; acc[k].z += t[k].z; acc[k].w += t[k].w;
+                                }
+                            }
+#pragma unroll
+                            for (int k = 0; k < 4; k++) {
+                                const int f = et + 128 * (kb + k), row = f >> 5, cq = f & 31;
+                                *reinterpret_cast<float4 *>(T + row * FT_TSTRIDE + (cq >> 3) * 36 + 4 * (cq & 7)) = acc[k];
+                            }
+                        }
+                    }
                 }
                 named_bar(1, 128);
                 // row c0 + ti, values of operand rows 32*part .. 32*part + 31
@@ -642,7 +694,7 @@ __global__ void __launch_bounds__(FT_THREADS, 1) fused_tc_kernel(const __grid_co
                 }
                 named_bar(1, 128);   // T is rewritten by the next chunk
             }
-            if (!split) {
+            if (!split || own_in_tmem) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_ACCE + b));
