@@ -188,6 +188,17 @@ def gemm_path(M):
     return "decode" if M <= 16 else ("fused" if M <= 128 else "prefill")
 
 
+def decode_kernel(torch, M, OCs):
+    """The decode-mode kernel of a merged call: the paired one (a 16-warp CTA per
+    column group of each of two equal shards) at up to 8 rows, when each shard
+    has more column groups than half the SMs and no more than the SMs."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    g = OCs[0] // 128
+    if M <= 8 and len(OCs) == 2 and OCs[0] == OCs[1] and sms < 2 * g and g <= sms:
+        return "group_pair_kernel"
+    return "group_gemm_kernel"
+
+
 def linear_launches(M, n_shards):
     """Kernel launches of one linear call: the pre-transform plus the GEMM path's."""
     return 1 + (2 * n_shards if gemm_path(M) == "prefill" else 1)
@@ -246,7 +257,7 @@ class GateUp:
         alg = sum(self.code_bytes(K) + 2 * self.M * self.IC + 2 * self.M * self.OC + 2 * 2 * self.OC
                   for K in self.KS)
         a = alg / (ms * 1e-3) / 1e9
-        kernel = {"decode": "group_gemm_kernel", "fused": "fused_tc_kernel",
+        kernel = {"decode": decode_kernel(torch, self.M, (self.OC, self.OC)), "fused": "fused_tc_kernel",
                   "prefill": "reconstruct + prefill_gemm_kernel"}[gemm_path(self.M)]
         return {"bound": "hbm", "kernel": kernel + " (gate K=2 + up K=3 in one call)",
                 "achieved": round(a, 1), "peak": hbm, "unit": "GB/s", "frac": round(a / hbm, 4),
@@ -317,7 +328,7 @@ class GateUpA8(GateUp):
         alg = sum(self.code_bytes(K) + self.M * self.IC + 4 * self.M + 2 * self.M * self.OC + 2 * 2 * self.OC
                   for K in self.KS)
         a = alg / (ms * 1e-3) / 1e9
-        kernel = {"decode": "group_gemm_kernel (8-bit codes)" if self.M <= 8 else "group_gemm_kernel",
+        kernel = {"decode": decode_kernel(torch, self.M, (self.OC, self.OC)) + (" (8-bit codes)" if self.M <= 8 else ""),
                   "fused": "codes_to_f16 + fused_tc_kernel",
                   "prefill": "codes_to_f16 + reconstruct + prefill_gemm_kernel"}[gemm_path(self.M)]
         return {"bound": "hbm", "kernel": kernel + " (gate K=2 + up K=3 in one call)",

@@ -192,11 +192,13 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
 
 
 // The output transform of one column group for entry rows [0, nrows): Had128
-// of each row's 128 accumulated columns (red, fragment order), times post (and
-// post2 if given); f(n, oc0, y[4]) stores row n's 4 columns oc0..oc0+3 (one
-// warp per row, lane l holds columns 4l..4l+3).
+// of each row's 128 accumulated columns (red, fragment order), times the
+// row's scale row_scale[n] if given, then post (and post2 if given);
+// f(n, oc0, y[4]) stores row n's 4 columns oc0..oc0+3 (one warp per row, lane
+// l holds columns 4l..4l+3).
 template <int NB, class Store>
-__device__ __forceinline__ void group_epilogue(const float *red, int nrows, const uint16_t *post, const uint16_t *post2,
+__device__ __forceinline__ void group_epilogue(const float *red, int nrows, const float *row_scale,
+                                               const uint16_t *post, const uint16_t *post2,
                                                int G, int lane, int warp, Store f) {
     const int oc0 = G * kHad + 4 * lane;
     const uint2 rv = __ldg(reinterpret_cast<const uint2 *>(post + oc0));
@@ -208,11 +210,12 @@ __device__ __forceinline__ void group_epilogue(const float *red, int nrows, cons
 #pragma unroll
         for (int i = 0; i < 4; i++) v[i] = red[frag_index<NB>(n, 4 * lane + i)];
         warp_fwht128(v, lane);
+        const float hn = row_scale ? kHadNorm * __ldg(row_scale + n) : kHadNorm;
         float y[4];
 #pragma unroll
         for (int i = 0; i < 4; i++) {
             const int h = i >> 1, sh = 16 * (i & 1);
-            y[i] = (v[i] * kHadNorm) * f16_bits_to_f32((uint16_t)(rs[h] >> sh));
+            y[i] = (v[i] * hn) * f16_bits_to_f32((uint16_t)(rs[h] >> sh));
             if (post2) y[i] *= f16_bits_to_f32((uint16_t)(ss[h] >> sh));
         }
         f(n, oc0, y);

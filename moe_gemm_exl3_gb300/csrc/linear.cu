@@ -518,6 +518,124 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
     }
 }
 
+// --------------------------------------------------------------------------
+// Two dense shards of equal width (a merged gate/up layer) at up to 8 rows,
+// with more column groups per shard than half the SMs and at most as many as
+// the SMs.  With one group per 8-warp CTA, two CTAs share most SMs: where a
+// cheap (smaller K) and an expensive group meet, the cheap CTA ends early and
+// the other runs on alone at half the warps; other SMs hold two expensive
+// groups, or one group only.  Here one 16-warp CTA per SM takes shard 0's
+// group G (warps 0-7) and shard 1's group G (warps 8-15): every SM carries
+// one group of each shard.  The halves share nothing; each reduces its group
+// in fixed warp order and runs the epilogue (no split-K, deterministic).
+// Measured against moving the last tile rows of the costlier group to the
+// other half (either way round, 8 to 40 rows): every such split was slower,
+// its second load ramp costing more than the balance gains.
+// --------------------------------------------------------------------------
+constexpr int kPairThreads = 2 * kDecodeWarps * 32;
+constexpr size_t kPairFrag = 8 * 4 * 32;   // floats of one warp's fragments (one 8-row block)
+constexpr size_t kPairSmem = 2 * sizeof(float) * kDecodeWarps * kPairFrag;
+
+// USRC: fp16 rows of u or 8-bit codes (kUGlobal / kUCodes; see group_accumulate).
+template <int KSET, int USRC>
+__global__ void __launch_bounds__(kPairThreads, 1) group_pair_kernel(const GroupGemmArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    constexpr int FRAG = (int)kPairFrag;
+    const int lane = threadIdx.x & 31;
+    const int warp = (threadIdx.x >> 5) & (kDecodeWarps - 1);   // warp within the half
+    const int ht = threadIdx.x & (kDecodeWarps * 32 - 1);       // thread within the half
+    const int A = a.IC / kTile;
+    const int G = blockIdx.x;
+    const uint32_t hx = a.hash_xor;
+
+    grid_dependency_wait();
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    // one half: accumulate all A tile rows of group G of e, reduce over the
+    // half's warps into red[0, FRAG), then the dense epilogue
+    auto half = [&](const GroupEntry &e, float *red, int bar) {
+        float acc[8][1][4];
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) acc[j][0][q] = 0.f;
+        if ((KSET & 4) && e.K == 2) group_accumulate<2, 1, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2);
+        if ((KSET & 8) && e.K == 3) group_accumulate<3, 1, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2);
+        if ((KSET & 16) && e.K == 4) group_accumulate<4, 1, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2);
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) red[warp * FRAG + (j * 4 + q) * 32 + lane] = acc[j][0][q];
+        asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kDecodeWarps * 32) : "memory");
+        for (int i = ht; i < FRAG; i += kDecodeWarps * 32) {
+            float sum = red[i];
+#pragma unroll
+            for (int wv = 1; wv < kDecodeWarps; wv++) sum += red[wv * FRAG + i];
+            red[i] = sum;
+        }
+        asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kDecodeWarps * 32) : "memory");
+        const float *rsc = a.row_scale ? a.row_scale + e.u_row0 : nullptr;
+        group_epilogue<1>(red, e.nrows, rsc, e.post, e.post2, G, lane, warp, [&](int n, int oc0, const float (&y)[4]) {
+            const uint32_t o0 = (uint32_t)f32_to_bf16_bits(y[0]) | ((uint32_t)f32_to_bf16_bits(y[1]) << 16);
+            const uint32_t o1 = (uint32_t)f32_to_bf16_bits(y[2]) | ((uint32_t)f32_to_bf16_bits(y[3]) << 16);
+            *reinterpret_cast<uint2 *>(a.out + (int64_t)n * a.ldo + e.out_off + oc0) = make_uint2(o0, o1);
+        });
+    };
+    float *red = reinterpret_cast<float *>(smem_raw);
+    if (threadIdx.x < kDecodeWarps * 32) half(a.inline_e[0], red, 1);
+    else half(a.inline_e[1], red + kDecodeWarps * FRAG, 2);
+}
+
+// The paired kernel serves this launch: two dense shards of one width and one
+// 8-row block, with more column groups per shard than half the SMs and at most
+// as many as the SMs.
+static bool pair_launch_fits(const GroupGemmArgs &a, int nb) {
+    if (nb != 1 || a.gather || a.pair_act || a.mode != kModeDense) return false;
+    if (a.n_entries_dev || a.entries || a.n_groups_per_entry != 0 || a.n_inline != 2) return false;
+    const GroupEntry &e0 = a.inline_e[0], &e1 = a.inline_e[1];
+    if (e0.OC != e1.OC || e0.nrows != e1.nrows || e0.nrows > 8) return false;
+    const int groups = e0.OC / kHad, sms = device_info().sm_count;
+    return 2 * groups > sms && groups <= sms;
+}
+
+static cudaError_t launch_group_pair(const GroupGemmArgs &a0, int kset, bool pdl, cudaStream_t s) {
+    GroupGemmArgs a = a0;
+    a.hash_xor = kHashXor;
+    for (int i = 0; i < 17; i++) a.pow2[i] = 1u << i;
+    const void *fn;
+    if (a.codes) {
+        switch (kset) {
+            case 4: fn = (const void *)group_pair_kernel<4, kUCodes>; break;
+            case 8: fn = (const void *)group_pair_kernel<8, kUCodes>; break;
+            case 16: fn = (const void *)group_pair_kernel<16, kUCodes>; break;
+            case 12: fn = (const void *)group_pair_kernel<12, kUCodes>; break;
+            default: fn = (const void *)group_pair_kernel<28, kUCodes>; break;
+        }
+    } else {
+        switch (kset) {
+            case 4: fn = (const void *)group_pair_kernel<4, kUGlobal>; break;
+            case 8: fn = (const void *)group_pair_kernel<8, kUGlobal>; break;
+            case 16: fn = (const void *)group_pair_kernel<16, kUGlobal>; break;
+            case 12: fn = (const void *)group_pair_kernel<12, kUGlobal>; break;
+            default: fn = (const void *)group_pair_kernel<28, kUGlobal>; break;
+        }
+    }
+    cudaError_t e = kernel_smem_optin(fn, kPairSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.inline_e[0].OC / kHad));
+    cfg.blockDim = dim3(kPairThreads);
+    cfg.dynamicSmemBytes = kPairSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    void *args[] = {&a};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 template <int NB, int KSET, int USRC = kUGlobal, bool PAIR = false>
 static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t total_hint, cudaStream_t s) {
     constexpr size_t smem = group_smem_bytes<NB, PAIR>();
@@ -590,6 +708,7 @@ cudaError_t launch_group_gemm(const GroupGemmArgs &a, int nb, bool pdl, cudaStre
         return launch_group_t<1, 28, kUGather>(a, pdl, total, s);
     }
     if (a.pair_act) return cudaErrorInvalidValue;
+    if (pair_launch_fits(a, nb)) return launch_group_pair(a, kset, pdl, s);
     if (a.codes) {
         // 8-bit activation codes: one 8-row block per entry
         if (nb != 1) return cudaErrorInvalidValue;

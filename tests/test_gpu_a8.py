@@ -205,6 +205,36 @@ def test_shards_a8_match_oracle_per_shard(M, path, pin_gemm_path):
     assert torch.all(gaps[:, 384:384 + 64] == NAN_BF16) and torch.all(gaps[:, ldo - 64:] == NAN_BF16)
 
 
+@pytest.mark.parametrize("M,Ks", [(1, (2, 3)), (8, (4, 2))])
+def test_paired_shards_a8_every_column(M, Ks):
+    # two shards of one width with 5/8 as many column groups per shard as the GPU
+    # has SMs (the decode path's paired CTAs, on the 8-bit codes): every column
+    # against the oracle's 8-bit projection, and the split entry (quantize, then
+    # the GEMM on the codes) bit for bit equal to the one-call result
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    IC, OC = 1024, 128 * (sms * 5 // 8)
+    g = syn.rng(440 + M)
+    shards = [syn.make_shard(g, IC, OC, K) for K in Ks]
+    x = syn.normal_bf16(g, M, IC, outlier_frac=0.01)
+    sets = _shard_sets(shards, [0, OC])
+    ws = m.workspace(m.exl3_linear_shards_a8_workspace_bytes(M, IC, sets))
+    xd = dev(x, torch.bfloat16)
+    one = torch.full((M, 2 * OC), NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    m.exl3_linear_into_shards_a8(xd, sets, one, ws)
+    A = torch.empty((2, M, IC), dtype=torch.uint8, device="cuda")
+    As = torch.empty((2, M), dtype=torch.float32, device="cuda")
+    for i, st in enumerate(sets):
+        m.exl3_quantize_a8(xd, st[2], st[3], A=A[i], As=As[i])
+    two = torch.empty((M, 2 * OC), dtype=torch.bfloat16, device="cuda")
+    m.exl3_gemm_a8_into_shards(A, As, sets, two, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(one.view(torch.int16), two.view(torch.int16))
+    got = as_f64(one)
+    for i, s in enumerate(shards):
+        y_ref, _, _ = oracle.linear_a8_f64(x, s.code, s.K, s.s_in, s.rin, s.rout, s.s_out)
+        assert_rows_close(got[:, i * OC:(i + 1) * OC], y_ref)
+
+
 @pytest.mark.parametrize("M,path", [(5, "rows"), (20, "rows"), (96, "fused"), (140, "prefill")])
 def test_gemm_a8_into_shards_equals_linear_into_shards_a8(M, path, pin_gemm_path):
     pin_gemm_path(path)

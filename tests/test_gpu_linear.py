@@ -276,6 +276,32 @@ def test_errors_are_reported_not_launched():
     assert m.exl3_workspace_error(ws) == 0
 
 
+@pytest.mark.parametrize("M,Ks", [(1, (2, 3)), (5, (4, 2)), (8, (3, 3)), (8, (2, 4))])
+def test_paired_shards_every_column_and_stable(M, Ks):
+    # Two shards of one width with 5/8 as many column groups per shard as the GPU
+    # has SMs: the decode path gives each 16-warp CTA one group of each shard,
+    # one to each half of its warps.  Every column against the oracle, and 20
+    # back-to-back calls identical bit for bit.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    IC, OC = 1024, 128 * (sms * 5 // 8)
+    x, shards = syn.gate_up(120 + M, M=M, IC=IC, OC=OC, Ks=Ks)
+    sets = [shard_set(sh, i * OC) for i, sh in enumerate(shards)]
+    ws = m.workspace(m.exl3_linear_shards_workspace_bytes(M, IC, sets))
+    xd = dev(x, torch.bfloat16)
+    n = 20
+    outs = torch.full((n, M, 2 * OC), NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    for i in range(n):
+        m.exl3_linear_into_shards(xd, sets, outs[i], ws)
+    torch.cuda.synchronize()
+    o = outs.view(torch.int16)
+    assert bool((o == o[:1]).all()), "back-to-back calls differ"
+    got = as_f64(outs[0])
+    for i, sh in enumerate(shards):
+        ref = oracle.linear_f64(x, sh.code, sh.K, sh.s_in, sh.rin, sh.rout, sh.s_out)
+        assert_rows_close(got[:, i * OC:(i + 1) * OC], ref)
+    assert m.exl3_workspace_error(ws) == 0
+
+
 @pytest.mark.parametrize("M", (1, 8, 20, 40))
 def test_shards_call_equals_per_shard_calls(M):
     # a merged layer in one call gives the per-shard result (three shards, different K and OC)
