@@ -205,14 +205,15 @@ def test_shards_a8_match_oracle_per_shard(M, path, pin_gemm_path):
     assert torch.all(gaps[:, 384:384 + 64] == NAN_BF16) and torch.all(gaps[:, ldo - 64:] == NAN_BF16)
 
 
-@pytest.mark.parametrize("M,Ks", [(1, (2, 3)), (8, (4, 2))])
-def test_paired_shards_a8_every_column(M, Ks):
-    # two shards of one width with 5/8 as many column groups per shard as the GPU
-    # has SMs (the decode path's paired CTAs, on the 8-bit codes): every column
-    # against the oracle's 8-bit projection, and the split entry (quantize, then
-    # the GEMM on the codes) bit for bit equal to the one-call result
+@pytest.mark.parametrize("M,Ks,IC,OC", [(1, (2, 3), 1024, 0), (8, (4, 2), 1024, 0), (8, (2, 3), 5120, 17408)])
+def test_paired_shards_a8_every_column(M, Ks, IC, OC):
+    # two shards of one width (OC = 0: 5/8 as many column groups per shard as the
+    # GPU has SMs; the last case is the merged 5120 -> 2 x 17408 gate/up layer),
+    # on the decode path's paired CTAs, on the 8-bit codes: every column against
+    # the oracle's 8-bit projection, and the split entry (quantize, then the GEMM
+    # on the codes) bit for bit equal to the one-call result
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    IC, OC = 1024, 128 * (sms * 5 // 8)
+    OC = OC or 128 * (sms * 5 // 8)
     g = syn.rng(440 + M)
     shards = [syn.make_shard(g, IC, OC, K) for K in Ks]
     x = syn.normal_bf16(g, M, IC, outlier_frac=0.01)
