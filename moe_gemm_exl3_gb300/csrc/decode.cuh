@@ -31,7 +31,10 @@ constexpr size_t group_smem_bytes() {
 
 
 // Accumulate tile rows [a_lo, a_hi) of one column group into acc (one warp,
-// rows a_lo + warp, a_lo + warp + 8, ...).
+// rows a_lo + warp, a_lo + warp + 8, ...).  wait_u: the kernel has not yet
+// waited for the kernel before it (a programmatic dependent launch); the first
+// code words, weights that no kernel writes, are requested before the wait,
+// the activations after it.
 // Where the activation rows come from (USRC, one 8-row block per entry for the
 // last two):
 //   kUGlobal  rows e.u_row0 + g of u (row stride IC)
@@ -59,7 +62,8 @@ template <int K, int NB, int USRC = kUGlobal>
 __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const GroupEntry &e, const uint16_t *u,
                                                  int IC, int G, int a_lo, int a_hi, int lane, int warp,
                                                  uint32_t hx, const uint32_t *pow2,
-                                                 const int32_t *gather_rows = nullptr, int R_half = 0) {
+                                                 const int32_t *gather_rows = nullptr, int R_half = 0,
+                                                 bool wait_u = false) {
     static_assert(USRC == kUGlobal || NB == 1, "gathered and 8-bit activation rows serve one 8-row block");
     const int g = lane >> 2, q = lane & 3;
     const int TO = e.OC / kTile;
@@ -133,11 +137,10 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
         const uint32_t zero = USRC == kUCodes ? 0x80808080u : 0u;
         uint2 ua = make_uint2(zero, zero), ubv = make_uint2(zero, zero);
         load_quarter<K>(wa, p);
+        if (n > 1) load_quarter<K>(wb, p + stride);
+        if (wait_u) asm volatile("griddepcontrol.wait;" ::: "memory");
         if (urow) ua = ldu(up);
-        if (n > 1) {
-            load_quarter<K>(wb, p + stride);
-            if (urow) ubv = ldu(up + kUS);
-        }
+        if (n > 1 && urow) ubv = ldu(up + kUS);
         auto row = [&](uint32_t (&w)[2 * K], uint2 &uv, bool refill, const uint32_t *pn, const uint16_t *upn) {
             QuarterStream<K> st;
             st.build(w, quarter_prev_word(w[2 * K - 1], lane));
@@ -170,6 +173,7 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
 #pragma unroll
         for (int d = 0; d < PF; d++)
             if (ar + d * kDecodeWarps < a_hi) load_quarter<K>(wq[d], tile0 + (ar + d * kDecodeWarps) * row_words);
+        if (wait_u) asm volatile("griddepcontrol.wait;" ::: "memory");
         load_u(un, ar);
         for (; ar < a_hi; ar += kDecodeWarps) {
             uint32_t w[2 * K];

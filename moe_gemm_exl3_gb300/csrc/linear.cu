@@ -262,8 +262,13 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
     const int A = a.IC / kTile;
     const int AU = NSUB * A;   // units (tile rows) per column group
 
-    // everything below reads what the preceding kernel in the stream wrote
-    grid_dependency_wait();
+    // Entries passed by value (dense launches) name only weights and this
+    // launch's activations: the first code words are requested before waiting
+    // for the preceding kernel in the stream (it may still be writing the
+    // activations), the rest after.  Entry lists on the device (MoE) are that
+    // kernel's output: wait first.
+    const bool hoist = !a.n_entries_dev && !a.entries;
+    if (!hoist) grid_dependency_wait();
     // the next kernel in the stream may be scheduled now: it must itself wait for
     // this grid to complete before touching memory (every kernel here does)
     asm volatile("griddepcontrol.launch_dependents;");
@@ -341,12 +346,18 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
                     for (int r = 0; r < 4; r++) acc[j][nb][r] = 0.f;
             if (lo < hi) {
                 if ((KSET & 4) && es.K == 2)
-                    group_accumulate<2, NB, USRC>(acc, es, a.u, a.IC, G, lo, hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+                    group_accumulate<2, NB, USRC>(acc, es, a.u, a.IC, G, lo, hi, lane, warp, hx, a.pow2, a.row_pair, a.R,
+                                                 hoist);
                 if ((KSET & 8) && es.K == 3)
-                    group_accumulate<3, NB, USRC>(acc, es, a.u, a.IC, G, lo, hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+                    group_accumulate<3, NB, USRC>(acc, es, a.u, a.IC, G, lo, hi, lane, warp, hx, a.pow2, a.row_pair, a.R,
+                                                 hoist);
                 if ((KSET & 16) && es.K == 4)
-                    group_accumulate<4, NB, USRC>(acc, es, a.u, a.IC, G, lo, hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+                    group_accumulate<4, NB, USRC>(acc, es, a.u, a.IC, G, lo, hi, lane, warp, hx, a.pow2, a.row_pair, a.R,
+                                                 hoist);
             }
+            // warps without rows in this range: the split-K slab and counters below
+            // are shared with the preceding kernel
+            if (hoist) grid_dependency_wait();
             float *rs = red + sub * kDecodeWarps * FRAG;
             // ---- CTA reduction in fixed warp order (fragment order, one barrier)
 #pragma unroll
@@ -548,7 +559,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) group_pair_kernel(const Group
     const int G = blockIdx.x;
     const uint32_t hx = a.hash_xor;
 
-    grid_dependency_wait();
+    // the first code words (weights) are requested before waiting for the
+    // preceding kernel, which may still be writing the activations
     asm volatile("griddepcontrol.launch_dependents;");
 
     // one half: accumulate all A tile rows of group G of e, reduce over the
@@ -559,9 +571,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) group_pair_kernel(const Group
         for (int j = 0; j < 8; j++)
 #pragma unroll
             for (int q = 0; q < 4; q++) acc[j][0][q] = 0.f;
-        if ((KSET & 4) && e.K == 2) group_accumulate<2, 1, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2);
-        if ((KSET & 8) && e.K == 3) group_accumulate<3, 1, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2);
-        if ((KSET & 16) && e.K == 4) group_accumulate<4, 1, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2);
+        if ((KSET & 4) && e.K == 2) group_accumulate<2, 1, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2, nullptr, 0, true);
+        if ((KSET & 8) && e.K == 3) group_accumulate<3, 1, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2, nullptr, 0, true);
+        if ((KSET & 16) && e.K == 4) group_accumulate<4, 1, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2, nullptr, 0, true);
+        grid_dependency_wait();   // a no-op once waited; the row scales and out follow
 #pragma unroll
         for (int j = 0; j < 8; j++)
 #pragma unroll
