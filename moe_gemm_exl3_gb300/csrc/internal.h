@@ -123,6 +123,11 @@ struct GroupGemmArgs {
     int32_t pair_act;
     const uint16_t *act_suh;
     uint16_t *act_out;
+    // The device entry list (and the routed-row tables) were written by a kernel
+    // that completed before the preceding kernel in the stream let this launch
+    // start: read them, and request the first code words, before waiting for
+    // the preceding kernel (whose output is only the activations).
+    int32_t entries_ready;
 };
 constexpr int kMaxInlineEntries = 4;
 

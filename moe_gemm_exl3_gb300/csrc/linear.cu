@@ -265,9 +265,10 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
     // Entries passed by value (dense launches) name only weights and this
     // launch's activations: the first code words are requested before waiting
     // for the preceding kernel in the stream (it may still be writing the
-    // activations), the rest after.  Entry lists on the device (MoE) are that
-    // kernel's output: wait first.
-    const bool hoist = !a.n_entries_dev && !a.entries;
+    // activations), the rest after.  So are device entry lists written by an
+    // earlier kernel (entries_ready); those written by the preceding kernel
+    // itself are read after the wait.
+    const bool hoist = (!a.n_entries_dev && !a.entries) || a.entries_ready;
     if (!hoist) grid_dependency_wait();
     // the next kernel in the stream may be scheduled now: it must itself wait for
     // this grid to complete before touching memory (every kernel here does)

@@ -929,6 +929,8 @@ exl3_status moe_layer(const char *fn, const uint16_t *x, const float *logits, in
         g2.comb_pos = pos;
         g2.comb_y = y;
         g2.comb_counters = counters + kCombCounterBase;
+        // the routing launch, two before, wrote the entry lists and tables; FC1 only h2
+        g2.entries_ready = 1;
         if ((e = launch_group_gemm(g2, 1, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC2");
         trace("%s T=%d H=%d I=%d E=%d topk=%d rows<=%d gemm=decode (3 launches)", fn, T, H, I, E, topk, R);
         return EXL3_OK;
@@ -978,6 +980,8 @@ exl3_status moe_layer(const char *fn, const uint16_t *x, const float *logits, in
         g1.out_rows = st1;
         g1.partials = slab;
         g1.counters = counters;
+        // the entry lists come from route_kernel, the launch before the rotation
+        g1.entries_ready = 1;
         if ((e = launch_group_gemm(g1, L.nb, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC1");
 
         act_kernel<<<warp_grid((int64_t)R * (I / kHad)), 256, 0, s>>>(st1, I, R, b.w2_suh, row_slot, counts, h2);
