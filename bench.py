@@ -190,11 +190,11 @@ def gemm_path(M):
 
 def decode_kernel(torch, M, OCs):
     """The decode-mode kernel of a merged call: the paired one (a 16-warp CTA per
-    column group of each of two equal shards) at up to 8 rows, when each shard
+    column group of each of two equal shards) at up to 16 rows, when each shard
     has more column groups than half the SMs and no more than the SMs."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     g = OCs[0] // 128
-    if M <= 8 and len(OCs) == 2 and OCs[0] == OCs[1] and sms < 2 * g and g <= sms:
+    if M <= 16 and len(OCs) == 2 and OCs[0] == OCs[1] and sms < 2 * g and g <= sms:
         return "group_pair_kernel"
     return "group_gemm_kernel"
 

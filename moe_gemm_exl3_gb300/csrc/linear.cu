@@ -545,14 +545,17 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
 // its second load ramp costing more than the balance gains.
 // --------------------------------------------------------------------------
 constexpr int kPairThreads = 2 * kDecodeWarps * 32;
-constexpr size_t kPairFrag = 8 * 4 * 32;   // floats of one warp's fragments (one 8-row block)
-constexpr size_t kPairSmem = 2 * sizeof(float) * kDecodeWarps * kPairFrag;
+// floats of one warp's fragments, and the CTA's shared memory (both halves' warps)
+template <int NB> __host__ __device__ constexpr size_t pair_frag() { return 8 * NB * 4 * 32; }
+template <int NB> constexpr size_t pair_smem() { return 2 * sizeof(float) * kDecodeWarps * pair_frag<NB>(); }
 
 // USRC: fp16 rows of u or 8-bit codes (kUGlobal / kUCodes; see group_accumulate).
-template <int KSET, int USRC>
+// NB: 8-row blocks (up to 16 rows: two, fp16 rows only).
+template <int KSET, int USRC, int NB>
 __global__ void __launch_bounds__(kPairThreads, 1) group_pair_kernel(const GroupGemmArgs a) {
+    static_assert(USRC == kUGlobal || NB == 1, "8-bit activation codes serve one 8-row block");
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    constexpr int FRAG = (int)kPairFrag;
+    constexpr int FRAG = (int)pair_frag<NB>();
     const int lane = threadIdx.x & 31;
     const int warp = (threadIdx.x >> 5) & (kDecodeWarps - 1);   // warp within the half
     const int ht = threadIdx.x & (kDecodeWarps * 32 - 1);       // thread within the half
@@ -567,19 +570,23 @@ __global__ void __launch_bounds__(kPairThreads, 1) group_pair_kernel(const Group
     // one half: accumulate all A tile rows of group G of e, reduce over the
     // half's warps into red[0, FRAG), then the dense epilogue
     auto half = [&](const GroupEntry &e, float *red, int bar) {
-        float acc[8][1][4];
+        float acc[8][NB][4];
 #pragma unroll
         for (int j = 0; j < 8; j++)
 #pragma unroll
-            for (int q = 0; q < 4; q++) acc[j][0][q] = 0.f;
-        if ((KSET & 4) && e.K == 2) group_accumulate<2, 1, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2, nullptr, 0, true);
-        if ((KSET & 8) && e.K == 3) group_accumulate<3, 1, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2, nullptr, 0, true);
-        if ((KSET & 16) && e.K == 4) group_accumulate<4, 1, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2, nullptr, 0, true);
+            for (int nb = 0; nb < NB; nb++)
+#pragma unroll
+                for (int q = 0; q < 4; q++) acc[j][nb][q] = 0.f;
+        if ((KSET & 4) && e.K == 2) group_accumulate<2, NB, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2, nullptr, 0, true);
+        if ((KSET & 8) && e.K == 3) group_accumulate<3, NB, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2, nullptr, 0, true);
+        if ((KSET & 16) && e.K == 4) group_accumulate<4, NB, USRC>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2, nullptr, 0, true);
         grid_dependency_wait();   // a no-op once waited; the row scales and out follow
 #pragma unroll
         for (int j = 0; j < 8; j++)
 #pragma unroll
-            for (int q = 0; q < 4; q++) red[warp * FRAG + (j * 4 + q) * 32 + lane] = acc[j][0][q];
+            for (int nb = 0; nb < NB; nb++)
+#pragma unroll
+                for (int q = 0; q < 4; q++) red[warp * FRAG + ((j * NB + nb) * 4 + q) * 32 + lane] = acc[j][nb][q];
         asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kDecodeWarps * 32) : "memory");
         for (int i = ht; i < FRAG; i += kDecodeWarps * 32) {
             float sum = red[i];
@@ -589,7 +596,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) group_pair_kernel(const Group
         }
         asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(kDecodeWarps * 32) : "memory");
         const float *rsc = a.row_scale ? a.row_scale + e.u_row0 : nullptr;
-        group_epilogue<1>(red, e.nrows, rsc, e.post, e.post2, G, lane, warp, [&](int n, int oc0, const float (&y)[4]) {
+        group_epilogue<NB>(red, e.nrows, rsc, e.post, e.post2, G, lane, warp, [&](int n, int oc0, const float (&y)[4]) {
             const uint32_t o0 = (uint32_t)f32_to_bf16_bits(y[0]) | ((uint32_t)f32_to_bf16_bits(y[1]) << 16);
             const uint32_t o1 = (uint32_t)f32_to_bf16_bits(y[2]) | ((uint32_t)f32_to_bf16_bits(y[3]) << 16);
             *reinterpret_cast<uint2 *>(a.out + (int64_t)n * a.ldo + e.out_off + oc0) = make_uint2(o0, o1);
@@ -601,45 +608,41 @@ __global__ void __launch_bounds__(kPairThreads, 1) group_pair_kernel(const Group
 }
 
 // The paired kernel serves this launch: two dense shards of one width and one
-// 8-row block, with more column groups per shard than half the SMs and at most
-// as many as the SMs.
+// 8-row block (two with fp16 rows), with more column groups per shard than half
+// the SMs and at most as many as the SMs.
 static bool pair_launch_fits(const GroupGemmArgs &a, int nb) {
-    if (nb != 1 || a.gather || a.pair_act || a.mode != kModeDense) return false;
+    if (nb < 1 || nb > (a.codes ? 1 : 2) || a.gather || a.pair_act || a.mode != kModeDense) return false;
     if (a.n_entries_dev || a.entries || a.n_groups_per_entry != 0 || a.n_inline != 2) return false;
     const GroupEntry &e0 = a.inline_e[0], &e1 = a.inline_e[1];
-    if (e0.OC != e1.OC || e0.nrows != e1.nrows || e0.nrows > 8) return false;
+    if (e0.OC != e1.OC || e0.nrows != e1.nrows || e0.nrows > 8 * nb) return false;
     const int groups = e0.OC / kHad, sms = device_info().sm_count;
     return 2 * groups > sms && groups <= sms;
 }
 
-static cudaError_t launch_group_pair(const GroupGemmArgs &a0, int kset, bool pdl, cudaStream_t s) {
+template <int USRC, int NB>
+static const void *pair_kernel(int kset) {
+    switch (kset) {
+        case 4: return (const void *)group_pair_kernel<4, USRC, NB>;
+        case 8: return (const void *)group_pair_kernel<8, USRC, NB>;
+        case 16: return (const void *)group_pair_kernel<16, USRC, NB>;
+        case 12: return (const void *)group_pair_kernel<12, USRC, NB>;
+        default: return (const void *)group_pair_kernel<28, USRC, NB>;
+    }
+}
+
+static cudaError_t launch_group_pair(const GroupGemmArgs &a0, int nb, int kset, bool pdl, cudaStream_t s) {
     GroupGemmArgs a = a0;
     a.hash_xor = kHashXor;
     for (int i = 0; i < 17; i++) a.pow2[i] = 1u << i;
-    const void *fn;
-    if (a.codes) {
-        switch (kset) {
-            case 4: fn = (const void *)group_pair_kernel<4, kUCodes>; break;
-            case 8: fn = (const void *)group_pair_kernel<8, kUCodes>; break;
-            case 16: fn = (const void *)group_pair_kernel<16, kUCodes>; break;
-            case 12: fn = (const void *)group_pair_kernel<12, kUCodes>; break;
-            default: fn = (const void *)group_pair_kernel<28, kUCodes>; break;
-        }
-    } else {
-        switch (kset) {
-            case 4: fn = (const void *)group_pair_kernel<4, kUGlobal>; break;
-            case 8: fn = (const void *)group_pair_kernel<8, kUGlobal>; break;
-            case 16: fn = (const void *)group_pair_kernel<16, kUGlobal>; break;
-            case 12: fn = (const void *)group_pair_kernel<12, kUGlobal>; break;
-            default: fn = (const void *)group_pair_kernel<28, kUGlobal>; break;
-        }
-    }
-    cudaError_t e = kernel_smem_optin(fn, kPairSmem);
+    const void *fn = a.codes ? pair_kernel<kUCodes, 1>(kset)
+                             : (nb == 2 ? pair_kernel<kUGlobal, 2>(kset) : pair_kernel<kUGlobal, 1>(kset));
+    const size_t smem = nb == 2 ? pair_smem<2>() : pair_smem<1>();
+    cudaError_t e = kernel_smem_optin(fn, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.inline_e[0].OC / kHad));
     cfg.blockDim = dim3(kPairThreads);
-    cfg.dynamicSmemBytes = kPairSmem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -722,7 +725,7 @@ cudaError_t launch_group_gemm(const GroupGemmArgs &a, int nb, bool pdl, cudaStre
         return launch_group_t<1, 28, kUGather>(a, pdl, total, s);
     }
     if (a.pair_act) return cudaErrorInvalidValue;
-    if (pair_launch_fits(a, nb)) return launch_group_pair(a, kset, pdl, s);
+    if (pair_launch_fits(a, nb)) return launch_group_pair(a, nb, kset, pdl, s);
     if (a.codes) {
         // 8-bit activation codes: one 8-row block per entry
         if (nb != 1) return cudaErrorInvalidValue;

@@ -276,12 +276,13 @@ def test_errors_are_reported_not_launched():
     assert m.exl3_workspace_error(ws) == 0
 
 
-@pytest.mark.parametrize("M,Ks", [(1, (2, 3)), (5, (4, 2)), (8, (3, 3)), (8, (2, 4))])
+@pytest.mark.parametrize("M,Ks", [(1, (2, 3)), (5, (4, 2)), (8, (3, 3)), (8, (2, 4)), (12, (2, 3)), (16, (4, 3))])
 def test_paired_shards_every_column_and_stable(M, Ks):
     # Two shards of one width with 5/8 as many column groups per shard as the GPU
     # has SMs: the decode path gives each 16-warp CTA one group of each shard,
-    # one to each half of its warps.  Every column against the oracle, and 20
-    # back-to-back calls identical bit for bit.
+    # one to each half of its warps (one 8-row block to M = 8, two to M = 16).
+    # Every column against the oracle, and 20 back-to-back calls identical bit
+    # for bit.
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     IC, OC = 1024, 128 * (sms * 5 // 8)
     x, shards = syn.gate_up(120 + M, M=M, IC=IC, OC=OC, Ks=Ks)
