@@ -240,6 +240,28 @@ exl3_status exl3_linear_into_shards(const uint16_t *x, int64_t M, int32_t IC,
                                     void *ws, size_t ws_bytes, exl3_stream stream);
 
 /*
+ * exl3_linear_into_shards with x and out in host memory.  x_host and out_host
+ * are pinned host buffers mapped into the device's address space
+ * (cudaMallocHost / cudaHostAlloc, or cudaHostRegister with
+ * cudaHostRegisterMapped; with unified addressing all pinned memory is
+ * mapped).  The pre-transform reads x, and the GEMM's epilogue writes out,
+ * through those mappings (over the host link: NVLink-C2C on Grace parts):
+ * there are no staging copies and no device copies of x or out.  For
+ * decode-sized M, where x and out are small, this is the cheapest way to run
+ * the layer on host-resident activations.
+ *   x_host    HOST pinned bf16 [M][IC] (8-byte aligned)
+ *   out_host  HOST pinned bf16 [M][ldo]; only the shards' column slices are written
+ *   shards, ws, stream: as for exl3_linear_into_shards (device memory)
+ * Returns EXL3_EINVAL before any launch if x_host or out_host is not mapped
+ * pinned host memory (pageable host memory and device memory included).
+ * Asynchronous like every call: synchronize the stream before reading out_host.
+ */
+exl3_status exl3_linear_into_shards_host(const uint16_t *x_host, int64_t M, int32_t IC,
+                                         const exl3_shard *shards, int32_t n_shards,
+                                         uint16_t *out_host, int64_t ldo,
+                                         void *ws, size_t ws_bytes, exl3_stream stream);
+
+/*
  * exl3_linear_into_shards on activations already transformed per shard:
  * u fp16 [n_shards][M][IC], u[i] = Had128((x * s_in_i) * rin_i) (as
  * exl3_pretransform writes it); the shards' s_in / rin pointers are ignored.

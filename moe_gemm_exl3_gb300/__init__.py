@@ -31,7 +31,8 @@ EXPORTS = ("exl3_last_error", "exl3_version", "exl3_linear_workspace_bytes", "ex
            "exl3_lm_head_workspace_bytes", "exl3_lm_head_int8", "exl3_projections_workspace_bytes",
            "exl3_linear_projections", "exl3_linear_a8_workspace_bytes", "exl3_quantize_a8",
            "exl3_linear_into_a8", "exl3_gemm_a8_into", "exl3_linear_shards_a8_workspace_bytes",
-           "exl3_linear_into_shards_a8", "exl3_gemm_a8_into_shards", "exl3_moe_forward")
+           "exl3_linear_into_shards_a8", "exl3_gemm_a8_into_shards", "exl3_moe_forward",
+           "exl3_linear_into_shards_host")
 
 
 class Exl3Error(RuntimeError):
@@ -70,6 +71,8 @@ _lock = threading.Lock()
 def lib() -> ctypes.CDLL:
     """Load the in-tree library; raises if it has not been built."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -118,6 +121,8 @@ def lib() -> ctypes.CDLL:
                 "exl3_gemm_a8_into": ([vp, vp, i64, i32, vp, i32, i32, vp, vp, vp, i64, i64, vp, sz, vp],
                                       ctypes.c_int),
                 "exl3_linear_shards_a8_workspace_bytes": ([i64, i32, ctypes.POINTER(Shard), i32], sz),
+                "exl3_linear_into_shards_host": ([vp, i64, i32, ctypes.POINTER(Shard), i32, vp, i64, vp, sz, vp],
+                                                 ctypes.c_int),
                 "exl3_linear_into_shards_a8": ([vp, i64, i32, ctypes.POINTER(Shard), i32, vp, i64, vp, sz, vp],
                                                ctypes.c_int),
                 "exl3_gemm_a8_into_shards": ([vp, vp, i64, i32, ctypes.POINTER(Shard), i32, vp, i64, vp, sz, vp],
@@ -131,7 +136,16 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(device=None) -> int:
+    """The current CUDA stream of device (its raw handle)."""
+    if _raw_stream is not None:
+        # the handle without building a Stream object (a few microseconds a call)
+        if device is None or device.index is None:
+            return _raw_stream(torch.cuda.current_device())
+        return _raw_stream(device.index)
     return torch.cuda.current_stream(device).cuda_stream
 
 
@@ -269,6 +283,22 @@ def exl3_linear_into_shards(x: torch.Tensor, shards, out: torch.Tensor, ws: torc
                                          _ptr(out, torch.bfloat16, "out"), out.shape[-1],
                                          _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(x.device)),
            "exl3_linear_into_shards")
+
+
+def exl3_linear_into_shards_host(x: torch.Tensor, shards, out: torch.Tensor, ws: torch.Tensor) -> None:
+    """exl3_linear_into_shards with x and out in pinned host memory: the kernels read x
+    and write out through their device mappings (see include/exl3.h)."""
+    for t, name in ((x, "x"), (out, "out")):
+        if t.is_cuda or not t.is_pinned():
+            raise ValueError(f"{name} must be a pinned host tensor")
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor")
+    IC = x.shape[-1]
+    M = x.numel() // IC
+    arr = _shard_array(shards, IC)
+    _check(lib().exl3_linear_into_shards_host(x.data_ptr(), M, IC, arr, len(shards), out.data_ptr(), out.shape[-1],
+                                              _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(ws.device)),
+           "exl3_linear_into_shards_host")
 
 
 def _projection_array(projs):

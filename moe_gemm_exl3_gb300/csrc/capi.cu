@@ -594,6 +594,32 @@ exl3_status exl3_linear_into_shards(const uint16_t *x, int64_t M, int32_t IC, co
     return run_gemm("linear_into_shards", ws.u, M, IC, d, n, out, ldo, ws, true, s);
 }
 
+// The device address of mapped pinned host memory p; nullptr if p is anything
+// else (pageable host memory, device memory, an unknown pointer).
+static void *mapped_host(const void *p) {
+    cudaPointerAttributes attr;
+    if (!p || cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return attr.type == cudaMemoryTypeHost ? attr.devicePointer : nullptr;
+}
+
+exl3_status exl3_linear_into_shards_host(const uint16_t *x_host, int64_t M, int32_t IC, const exl3_shard *shards,
+                                         int32_t n, uint16_t *out_host, int64_t ldo, void *wsp, size_t ws_bytes,
+                                         exl3_stream stream) {
+    const uint16_t *x = x_host;
+    uint16_t *out = out_host;
+    if (M > 0) {
+        x = static_cast<const uint16_t *>(mapped_host(x_host));
+        out = static_cast<uint16_t *>(mapped_host(out_host));
+        if (!x) return fail(EXL3_EINVAL, "linear_into_shards_host: x_host (%p) is not mapped pinned host memory", x_host);
+        if (!out)
+            return fail(EXL3_EINVAL, "linear_into_shards_host: out_host (%p) is not mapped pinned host memory", out_host);
+    }
+    return exl3_linear_into_shards(x, M, IC, shards, n, out, ldo, wsp, ws_bytes, stream);
+}
+
 exl3_status exl3_gemm_into_shards(const uint16_t *u, int64_t M, int32_t IC, const exl3_shard *shards, int32_t n,
                                   uint16_t *out, int64_t ldo, void *wsp, size_t ws_bytes, exl3_stream stream) {
     ShardDesc d[kMaxInlineEntries];

@@ -303,6 +303,49 @@ def test_paired_shards_every_column_and_stable(M, Ks):
     assert m.exl3_workspace_error(ws) == 0
 
 
+@pytest.mark.parametrize("M", (1, 8, 13))
+def test_linear_into_shards_host_equals_device_call(M):
+    # x and out in pinned host memory, read and written by the kernels through
+    # their device mappings: the result equals the device-buffer call bit for
+    # bit, and the columns outside the shards keep their poison
+    x, shards = syn.gate_up(1, M=M)
+    OC = 17408
+    sets = [shard_set(sh, 64 + i * OC) for i, sh in enumerate(shards)]
+    ws = m.workspace(m.exl3_linear_shards_workspace_bytes(M, 5120, sets))
+    xd = dev(x, torch.bfloat16)
+    ref = torch.full((M, 2 * OC + 128), NAN_BF16, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    m.exl3_linear_into_shards(xd, sets, ref, ws)
+    xh = xd.cpu().pin_memory()
+    oh = torch.full((M, 2 * OC + 128), NAN_BF16, dtype=torch.int16).pin_memory().view(torch.bfloat16)
+    m.exl3_linear_into_shards_host(xh, sets, oh, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(oh.view(torch.int16), ref.cpu().view(torch.int16))
+    assert bool((oh.view(torch.int16)[:, :64] == NAN_BF16).all())
+    assert m.exl3_workspace_error(ws) == 0
+
+
+def test_linear_into_shards_host_refuses_unmapped_buffers():
+    # pageable host memory and device memory are refused on the host, before any launch
+    import ctypes
+    L = m.lib()
+    x, sh = syn.linear_case(12, 2, 256, 256, 2)
+    sets = [shard_set(sh, 0)]
+    arr = m._shard_array(sets, 256)
+    ws = m.workspace(m.exl3_linear_shards_workspace_bytes(2, 256, sets))
+    st = torch.cuda.current_stream().cuda_stream
+    pageable = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    pinned_x = pageable.pin_memory()
+    pinned_out = torch.empty((2, 256), dtype=torch.bfloat16).pin_memory()
+    dev_out = torch.empty((2, 256), dtype=torch.bfloat16, device="cuda")
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    r = L.exl3_linear_into_shards_host(p(pageable), 2, 256, arr, 1, p(pinned_out), 256, p(ws), ws.numel(), st)
+    assert r == m.EXL3_EINVAL and b"x_host" in L.exl3_last_error()
+    r = L.exl3_linear_into_shards_host(p(pinned_x), 2, 256, arr, 1, p(dev_out), 256, p(ws), ws.numel(), st)
+    assert r == m.EXL3_EINVAL and b"out_host" in L.exl3_last_error()
+    with pytest.raises(ValueError):
+        m.exl3_linear_into_shards_host(pageable, sets, pinned_out, ws)
+
+
 @pytest.mark.parametrize("M", (1, 8, 20, 40))
 def test_shards_call_equals_per_shard_calls(M):
     # a merged layer in one call gives the per-shard result (three shards, different K and OC)
