@@ -653,6 +653,195 @@ static cudaError_t launch_group_pair(const GroupGemmArgs &a0, int nb, int kset, 
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+// --------------------------------------------------------------------------
+// MoE FC1 over w1 and w3 of each expert row block, activation rows gathered
+// per (token, route) pair, in 16-warp CTAs: warps 0-7 decode a range of w1's
+// tile rows and warps 8-15 the same tile rows of w3, at the same time (in
+// group_gemm_kernel's paired mode one set of 8 warps runs w1's rows, then w3's,
+// each with its own load ramp and reduction).  Units are (column group, tile
+// row); when the groups fit the grid each CTA takes one part of one group,
+// otherwise ranges split evenly (stream-K).  Split-K across CTAs, the slab
+// slots (both accumulator sets) and the epilogue, Had128((silu(g) * u) *
+// w2_suh[slot]) as FC2's input, are those of group_gemm_kernel's paired mode.
+// Used for few routed pairs (kPairActMaxPairs): with many groups over the grid,
+// two 8-warp CTAs per SM measured faster, one CTA's reduction and epilogue
+// overlapping the other's decode.
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(2 * kDecodeWarps * 32, 1) group_pair_act_kernel(const GroupGemmArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    constexpr int FRAG = 8 * 4 * 32;
+    constexpr int NT = 2 * kDecodeWarps * 32;
+    float *red = reinterpret_cast<float *>(smem_raw);   // [w1, w3][8 warps][FRAG]
+    GroupEntry *s_ent = reinterpret_cast<GroupEntry *>(red + 2 * kDecodeWarps * FRAG);
+    int *s_last = reinterpret_cast<int *>(s_ent + 2);
+    const int lane = threadIdx.x & 31;
+    const int sub = threadIdx.x >> 8;                             // 0: w1, 1: w3
+    const int warp = (threadIdx.x >> 5) & (kDecodeWarps - 1);     // warp within the half
+    const int ht = threadIdx.x & (kDecodeWarps * 32 - 1);
+    const int A = a.IC / kTile;
+
+    // the entry lists and the gathered rows are the preceding kernel's output
+    grid_dependency_wait();
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int n_groups = (*a.n_entries_dev / 2) * a.n_groups_per_entry;
+    const int64_t total = (int64_t)n_groups * A;
+    const int c = blockIdx.x;
+    int parts = 0, nCTA;
+    int64_t f, f_end;
+    if (n_groups > 0 && n_groups <= (int)gridDim.x) {
+        parts = decode_parts(gridDim.x / n_groups, A);
+        nCTA = n_groups * parts;
+        if (c >= nCTA) return;
+        const int g = c / parts, pp = c - g * parts;
+        f = (int64_t)g * A + (int64_t)pp * A / parts;
+        f_end = (int64_t)g * A + (int64_t)(pp + 1) * A / parts;
+    } else {
+        nCTA = (int64_t)gridDim.x < total ? (int)gridDim.x : (int)total;
+        if (c >= nCTA) return;
+        f = (int64_t)c * total / nCTA;
+        f_end = (int64_t)(c + 1) * total / nCTA;
+    }
+    const uint32_t hx = a.hash_xor;
+    while (f < f_end) {
+        const int gi = (int)(f / A);
+        const int a_lo = (int)(f % A);
+        const int a_hi = (int)((int64_t)A < a_lo + (f_end - f) ? (int64_t)A : a_lo + (f_end - f));
+        if (threadIdx.x < 2) s_ent[threadIdx.x] = a.entries[2 * (gi / a.n_groups_per_entry) + threadIdx.x];
+        __syncthreads();
+        const int G = gi % a.n_groups_per_entry;
+        {
+            const GroupEntry es = s_ent[sub];
+            float acc[8][1][4];
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+#pragma unroll
+                for (int q = 0; q < 4; q++) acc[j][0][q] = 0.f;
+            if (es.K == 2) group_accumulate<2, 1, kUGather>(acc, es, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+            if (es.K == 3) group_accumulate<3, 1, kUGather>(acc, es, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+            if (es.K == 4) group_accumulate<4, 1, kUGather>(acc, es, a.u, a.IC, G, a_lo, a_hi, lane, warp, hx, a.pow2, a.row_pair, a.R);
+            float *rs = red + sub * kDecodeWarps * FRAG;
+#pragma unroll
+            for (int j = 0; j < 8; j++)
+#pragma unroll
+                for (int q = 0; q < 4; q++) rs[warp * FRAG + (j * 4 + q) * 32 + lane] = acc[j][0][q];
+            if (sub) asm volatile("bar.sync 2, %0;" ::"r"(kDecodeWarps * 32) : "memory");
+            else asm volatile("bar.sync 1, %0;" ::"r"(kDecodeWarps * 32) : "memory");
+            for (int i = ht; i < FRAG; i += kDecodeWarps * 32) {
+                float sum = rs[i];
+#pragma unroll
+                for (int wv = 1; wv < kDecodeWarps; wv++) sum += rs[wv * FRAG + i];
+                rs[i] = sum;
+            }
+        }
+        __syncthreads();
+        // element i < 2 FRAG of the reduced sets lives at red[ridx(i)]
+        auto ridx = [&](int i) { return (i / FRAG) * (kDecodeWarps * FRAG) + i % FRAG; };
+
+        // ---- split-K across CTAs
+        int c_first, c_last;
+        if (parts > 0) {
+            c_first = gi * parts;
+            c_last = c_first + parts - 1;
+        } else {
+            const int64_t x0 = (int64_t)gi * A, x1 = (int64_t)(gi + 1) * A - 1;
+            c_first = (int)(((x0 + 1) * nCTA - 1) / total);
+            c_last = (int)(((x1 + 1) * nCTA - 1) / total);
+        }
+        bool do_epilogue = true;
+        if (c_first != c_last) {
+            float *slot = a.partials + (int64_t)(c + gi) * (2 * FRAG);
+            for (int i = threadIdx.x; i < 2 * FRAG; i += NT) slot[i] = red[ridx(i)];
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) *s_last = atomicAdd(a.counters + gi, 1) == c_last - c_first;
+            __syncthreads();
+            do_epilogue = *s_last;
+            if (do_epilogue) {
+                __threadfence();
+                // CTA order outermost (each CTA's elements load together); the sum
+                // runs in ascending CTA order (deterministic)
+                constexpr int PER = 2 * FRAG / NT;
+                float sum[PER];
+#pragma unroll
+                for (int k = 0; k < PER; k++) sum[k] = 0.f;
+                for (int cc = c_first; cc <= c_last; cc++) {
+                    const float *src = a.partials + (int64_t)(cc + gi) * (2 * FRAG);
+#pragma unroll
+                    for (int k = 0; k < PER; k++) sum[k] += __ldcg(src + threadIdx.x + k * NT);
+                }
+#pragma unroll
+                for (int k = 0; k < PER; k++) red[ridx(threadIdx.x + k * NT)] = sum[k];
+                if (threadIdx.x == 0) a.counters[gi] = 0;
+                __syncthreads();
+            }
+        }
+
+        // ---- epilogue: g = Had128(v_w1) * svh_w1, u = Had128(v_w3) * svh_w3,
+        // then FC2's input h2 = Had128((silu(g) * u) * w2_suh[slot]) -> fp16
+        if (do_epilogue) {
+            const GroupEntry e = s_ent[0], e3 = s_ent[1];
+            const int oc0 = G * kHad + 4 * lane;
+            const int w16 = threadIdx.x >> 5;
+            if (w16 < e.nrows) {
+                const uint2 pg = __ldg(reinterpret_cast<const uint2 *>(e.post + oc0));
+                const uint2 pu = __ldg(reinterpret_cast<const uint2 *>(e3.post + oc0));
+                const uint2 ps = __ldg(reinterpret_cast<const uint2 *>(a.act_suh + (int64_t)e.slot * e.OC + oc0));
+                const uint32_t wg[2] = {pg.x, pg.y}, wu[2] = {pu.x, pu.y}, ws[2] = {ps.x, ps.y};
+                const int n = w16;
+                float vg[4], vu[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    vg[i] = red[frag_index<1>(n, 4 * lane + i)];
+                    vu[i] = red[kDecodeWarps * FRAG + frag_index<1>(n, 4 * lane + i)];
+                }
+                warp_fwht128(vg, lane);
+                warp_fwht128(vu, lane);
+                float h[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int hh = i >> 1, sh = 16 * (i & 1);
+                    const float g = (vg[i] * kHadNorm) * f16_bits_to_f32((uint16_t)(wg[hh] >> sh));
+                    const float u = (vu[i] * kHadNorm) * f16_bits_to_f32((uint16_t)(wu[hh] >> sh));
+                    const float silu = g / (1.0f + __expf(-g));
+                    h[i] = (silu * u) * f16_bits_to_f32((uint16_t)(ws[hh] >> sh));
+                }
+                warp_fwht128(h, lane);
+                uint2 o;
+                o.x = (uint32_t)f32_to_f16_bits(h[0] * kHadNorm) | ((uint32_t)f32_to_f16_bits(h[1] * kHadNorm) << 16);
+                o.y = (uint32_t)f32_to_f16_bits(h[2] * kHadNorm) | ((uint32_t)f32_to_f16_bits(h[3] * kHadNorm) << 16);
+                *reinterpret_cast<uint2 *>(a.act_out + (e.out_off + n) * (int64_t)e.OC + oc0) = o;
+            }
+        }
+        __syncthreads();   // red and s_ent are reused by the next segment
+        f += a_hi - a_lo;
+    }
+}
+
+// Routed pairs up to which the paired FC1 runs in group_pair_act_kernel.
+constexpr int kPairActMaxPairs = 32;
+
+static cudaError_t launch_group_pair_act(const GroupGemmArgs &a0, bool pdl, cudaStream_t s) {
+    constexpr size_t smem = sizeof(float) * 2 * kDecodeWarps * 8 * 4 * 32 + 2 * sizeof(GroupEntry) + 16;
+    cudaError_t e = kernel_smem_optin((const void *)group_pair_act_kernel, smem);
+    if (e != cudaSuccess) return e;
+    GroupGemmArgs a = a0;
+    a.hash_xor = kHashXor;
+    for (int i = 0; i < 17; i++) a.pow2[i] = 1u << i;
+    int64_t grid = device_info().sm_count;
+    if (grid > kDecodeMaxCtas) grid = kDecodeMaxCtas;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(2 * kDecodeWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, group_pair_act_kernel, a);
+}
+
 template <int NB, int KSET, int USRC = kUGlobal, bool PAIR = false>
 static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t total_hint, cudaStream_t s) {
     constexpr size_t smem = group_smem_bytes<NB, PAIR>();
@@ -721,7 +910,13 @@ cudaError_t launch_group_gemm(const GroupGemmArgs &a, int nb, bool pdl, cudaStre
     if (a.gather) {
         // grouped MoE with activation rows stored per pair: one 8-row block per entry, any K
         if (nb != 1 || a.codes) return cudaErrorInvalidValue;
-        if (a.pair_act) return launch_group_t<1, 28, kUGather, true>(a, pdl, total, s);
+        // few routed pairs: w1 and w3 side by side in 16-warp CTAs; many: two 8-warp
+        // CTAs per SM, whose reductions and epilogues overlap each other's decode
+        // (measured: T = 1 32.2 -> 30.8 us and T = 4 69.6 -> 64.9 us with the first;
+        // T = 16 131.0 -> 134.4 us and T = 64 192.4 -> 197.6 us)
+        if (a.pair_act)
+            return a.R <= kPairActMaxPairs ? launch_group_pair_act(a, pdl, s)
+                                           : launch_group_t<1, 28, kUGather, true>(a, pdl, total, s);
         return launch_group_t<1, 28, kUGather>(a, pdl, total, s);
     }
     if (a.pair_act) return cudaErrorInvalidValue;

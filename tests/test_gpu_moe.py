@@ -242,7 +242,7 @@ def test_moe_fused_gemm_deterministic(full_bank, pin_gemm_path):
     assert m.exl3_workspace_error(ws) == 0
 
 
-@pytest.mark.parametrize("T", (1, 16, 512))
+@pytest.mark.parametrize("T", (1, 4, 16, 512))
 def test_moe_forward_back_to_back_bitwise_stable(full_bank, T):
     # Layers issued back to back on one workspace without a host sync give identical
     # bits (T = 512 runs FC1 and FC2 on the tensor-core GEMM in rows mode, whose code
