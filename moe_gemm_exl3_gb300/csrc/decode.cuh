@@ -31,7 +31,7 @@ constexpr size_t group_smem_bytes() {
 
 
 // Accumulate tile rows [a_lo, a_hi) of one column group into acc (one warp,
-// rows a_lo + warp, a_lo + warp + 8, ...).  wait_u: the kernel has not yet
+// rows a_lo + warp, a_lo + warp + STEP, ...: STEP warps share the range).  wait_u: the kernel has not yet
 // waited for the kernel before it (a programmatic dependent launch); the first
 // code words, weights that no kernel writes, are requested before the wait,
 // the activations after it.
@@ -58,7 +58,7 @@ __device__ __forceinline__ void codes_to_dup_f16(uint32_t w, uint32_t (&b)[4]) {
     }
 }
 
-template <int K, int NB, int USRC = kUGlobal>
+template <int K, int NB, int USRC = kUGlobal, int STEP = kDecodeWarps>
 __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const GroupEntry &e, const uint16_t *u,
                                                  int IC, int G, int a_lo, int a_hi, int lane, int warp,
                                                  uint32_t hx, const uint32_t *pow2,
@@ -113,8 +113,8 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
         // ahead as soon as its words are realigned (no register copies); the code
         // and activation pointers advance by increments only
         if (ar >= a_hi) return;
-        const int n = (a_hi - ar + kDecodeWarps - 1) / kDecodeWarps;
-        const int64_t stride = row_words * kDecodeWarps;
+        const int n = (a_hi - ar + STEP - 1) / STEP;
+        const int64_t stride = row_words * STEP;
         const uint32_t *p = tile0 + ar * row_words;
         const bool urow = g < e.nrows;
         int64_t urow_index = (int64_t)e.u_row0 + g;
@@ -127,7 +127,7 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
         const uint16_t *up = USRC == kUCodes ? reinterpret_cast<const uint16_t *>(
                                                   reinterpret_cast<const uint8_t *>(u) + urow_index * IC + 16 * ar + 4 * q)
                                             : u + urow_index * IC + 16 * ar + 4 * q;
-        constexpr int kUS = (USRC == kUCodes ? 8 : 16) * kDecodeWarps;   // activation step per warp step
+        constexpr int kUS = (USRC == kUCodes ? 8 : 16) * STEP;   // activation step per warp step
         auto ldu = [&](const uint16_t *pu) -> uint2 {
             if constexpr (USRC == kUCodes) return make_uint2(__ldg(reinterpret_cast<const uint32_t *>(pu)), 0u);
             else return __ldg(reinterpret_cast<const uint2 *>(pu));
@@ -172,10 +172,10 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
         uint32_t wq[PF][2 * K];
 #pragma unroll
         for (int d = 0; d < PF; d++)
-            if (ar + d * kDecodeWarps < a_hi) load_quarter<K>(wq[d], tile0 + (ar + d * kDecodeWarps) * row_words);
+            if (ar + d * STEP < a_hi) load_quarter<K>(wq[d], tile0 + (ar + d * STEP) * row_words);
         if (wait_u) asm volatile("griddepcontrol.wait;" ::: "memory");
         load_u(un, ar);
-        for (; ar < a_hi; ar += kDecodeWarps) {
+        for (; ar < a_hi; ar += STEP) {
             uint32_t w[2 * K];
 #pragma unroll
             for (int i = 0; i < 2 * K; i++) w[i] = wq[0][i];
@@ -183,10 +183,10 @@ __device__ __forceinline__ void group_accumulate(float (&acc)[8][NB][4], const G
             for (int d = 0; d + 1 < PF; d++)
 #pragma unroll
                 for (int i = 0; i < 2 * K; i++) wq[d][i] = wq[d + 1][i];
-            if (ar + PF * kDecodeWarps < a_hi) load_quarter<K>(wq[PF - 1], tile0 + (ar + PF * kDecodeWarps) * row_words);
+            if (ar + PF * STEP < a_hi) load_quarter<K>(wq[PF - 1], tile0 + (ar + PF * STEP) * row_words);
             uint32_t b[NB][4];
             dup_u(b, un);
-            load_u(un, ar + kDecodeWarps);
+            load_u(un, ar + STEP);
             QuarterStream<K> st;
             st.build(w, quarter_prev_word(w[2 * K - 1], lane));
             mma_row(st, b);

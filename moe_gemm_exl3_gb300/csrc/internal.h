@@ -128,6 +128,10 @@ struct GroupGemmArgs {
     // start: read them, and request the first code words, before waiting for
     // the preceding kernel (whose output is only the activations).
     int32_t entries_ready;
+    // Rows mode over device entry lists, one 8-row block of fp16 rows (MoE FC2
+    // at few routed pairs): one 16-warp CTA per column group at a time, the
+    // group's tile rows split over its warps (group_wide_kernel).
+    int32_t wide;
 };
 constexpr int kMaxInlineEntries = 4;
 

@@ -240,6 +240,77 @@ __host__ __device__ __forceinline__ int decode_parts(int fit, int A) {
     return p < 1 ? 1 : p;
 }
 
+// Output transform of column group G of entry e from the reduced fragments rr
+// (fragment order, NB row blocks): Had128 of each row's 128 columns, then the
+// post-scales; rows n0, n0 + nstep, ... < e.nrows, one warp per row.  Dense
+// mode stores bf16 into out; rows mode stores fp32 rows and, with the combine
+// epilogue, sums each token's routes.
+template <int NB>
+__device__ __forceinline__ void group_output(const GroupGemmArgs &a, const float *rr, const GroupEntry &e, int G,
+                                             int lane, int n0, int nstep) {
+    const int oc0 = G * kHad + 4 * lane;
+    const uint2 rv = __ldg(reinterpret_cast<const uint2 *>(e.post + oc0));
+    uint2 sv = make_uint2(0x3C003C00u, 0x3C003C00u);
+    if (a.mode == kModeDense) sv = __ldg(reinterpret_cast<const uint2 *>(e.post2 + oc0));
+    const uint32_t rs[2] = {rv.x, rv.y}, ss[2] = {sv.x, sv.y};
+    for (int n = n0; n < e.nrows; n += nstep) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) v[i] = rr[frag_index<NB>(n, 4 * lane + i)];
+        warp_fwht128(v, lane);
+        // the Hadamard scale, times the row's activation scale when there is one
+        const float hn = a.row_scale ? kHadNorm * __ldg(a.row_scale + e.u_row0 + n) : kHadNorm;
+        float y[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int h = i >> 1, sh = 16 * (i & 1);
+            y[i] = (v[i] * hn) * f16_bits_to_f32((uint16_t)(rs[h] >> sh));
+            if (a.mode == kModeDense) y[i] *= f16_bits_to_f32((uint16_t)(ss[h] >> sh));
+        }
+        if (a.mode == kModeDense) {
+            const uint32_t o0 = (uint32_t)f32_to_bf16_bits(y[0]) | ((uint32_t)f32_to_bf16_bits(y[1]) << 16);
+            const uint32_t o1 = (uint32_t)f32_to_bf16_bits(y[2]) | ((uint32_t)f32_to_bf16_bits(y[3]) << 16);
+            *reinterpret_cast<uint2 *>(a.out + (int64_t)n * a.ldo + e.out_off + oc0) = make_uint2(o0, o1);
+        } else {
+            *reinterpret_cast<float4 *>(a.out_rows + (e.out_off + n) * (int64_t)e.OC + oc0) =
+                make_float4(y[0], y[1], y[2], y[3]);
+            if (a.comb) {
+                // routed row r = token t's route: the last of t's valid routes to
+                // arrive at this column group sums them in route order into y[t]
+                __threadfence();
+                __syncwarp();
+                const int t = a.row_pair[e.out_off + n] / a.topk;
+                const int GH = e.OC / kHad;
+                int last = 0;
+                if (lane == 0) {
+                    int nv = 0;
+                    for (int k = 0; k < a.topk; k++) nv += a.comb_pos[(int64_t)t * a.topk + k] >= 0;
+                    last = atomicAdd(a.comb_counters + (int64_t)t * GH + G, 1) == nv - 1;
+                }
+                last = __shfl_sync(kFull, last, 0);
+                if (last) {
+                    __threadfence();
+                    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int k = 0; k < a.topk; k++) {
+                        const int rk = a.comb_pos[(int64_t)t * a.topk + k];
+                        if (rk < 0) continue;
+                        const float wk = a.comb_w[(int64_t)t * a.topk + k];
+                        const float4 d = __ldcg(reinterpret_cast<const float4 *>(a.out_rows + (int64_t)rk * e.OC + oc0));
+                        sum[0] += wk * d.x;
+                        sum[1] += wk * d.y;
+                        sum[2] += wk * d.z;
+                        sum[3] += wk * d.w;
+                    }
+                    const uint32_t o0 = (uint32_t)f32_to_bf16_bits(sum[0]) | ((uint32_t)f32_to_bf16_bits(sum[1]) << 16);
+                    const uint32_t o1 = (uint32_t)f32_to_bf16_bits(sum[2]) | ((uint32_t)f32_to_bf16_bits(sum[3]) << 16);
+                    *reinterpret_cast<uint2 *>(a.comb_y + (int64_t)t * e.OC + oc0) = make_uint2(o0, o1);
+                    if (lane == 0) a.comb_counters[(int64_t)t * GH + G] = 0;
+                }
+            }
+        }
+    }
+}
+
 // KSET: bit k set = the launch may contain entries of bitrate k (2, 3, 4); only
 // those decode paths are compiled into the kernel, which keeps registers low.
 // USRC: where the activation rows come from (kUGlobal, kUGather or kUCodes; see
@@ -462,69 +533,7 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
             }
         }
         // ---- epilogue: Had128 of each row's 128 columns, then the post-scales
-        if (!PAIR && do_epilogue) {
-            const int oc0 = G * kHad + 4 * lane;
-            const uint2 rv = __ldg(reinterpret_cast<const uint2 *>(e.post + oc0));
-            uint2 sv = make_uint2(0x3C003C00u, 0x3C003C00u);
-            if (a.mode == kModeDense) sv = __ldg(reinterpret_cast<const uint2 *>(e.post2 + oc0));
-            const uint32_t rs[2] = {rv.x, rv.y}, ss[2] = {sv.x, sv.y};
-            for (int n = warp; n < e.nrows; n += kDecodeWarps) {
-                float v[4];
-#pragma unroll
-                for (int i = 0; i < 4; i++) v[i] = red[frag_index<NB>(n, 4 * lane + i)];
-                warp_fwht128(v, lane);
-                // the Hadamard scale, times the row's activation scale when there is one
-                const float hn = a.row_scale ? kHadNorm * __ldg(a.row_scale + e.u_row0 + n) : kHadNorm;
-                float y[4];
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    const int h = i >> 1, sh = 16 * (i & 1);
-                    y[i] = (v[i] * hn) * f16_bits_to_f32((uint16_t)(rs[h] >> sh));
-                    if (a.mode == kModeDense) y[i] *= f16_bits_to_f32((uint16_t)(ss[h] >> sh));
-                }
-                if (a.mode == kModeDense) {
-                    const uint32_t o0 = (uint32_t)f32_to_bf16_bits(y[0]) | ((uint32_t)f32_to_bf16_bits(y[1]) << 16);
-                    const uint32_t o1 = (uint32_t)f32_to_bf16_bits(y[2]) | ((uint32_t)f32_to_bf16_bits(y[3]) << 16);
-                    *reinterpret_cast<uint2 *>(a.out + (int64_t)n * a.ldo + e.out_off + oc0) = make_uint2(o0, o1);
-                } else {
-                    *reinterpret_cast<float4 *>(a.out_rows + (e.out_off + n) * (int64_t)e.OC + oc0) =
-                        make_float4(y[0], y[1], y[2], y[3]);
-                    if (a.comb) {
-                        // routed row r = token t's route: the last of t's valid routes to
-                        // arrive at this column group sums them in route order into y[t]
-                        __threadfence();
-                        __syncwarp();
-                        const int t = a.row_pair[e.out_off + n] / a.topk;
-                        const int GH = e.OC / kHad;
-                        int last = 0;
-                        if (lane == 0) {
-                            int nv = 0;
-                            for (int k = 0; k < a.topk; k++) nv += a.comb_pos[(int64_t)t * a.topk + k] >= 0;
-                            last = atomicAdd(a.comb_counters + (int64_t)t * GH + G, 1) == nv - 1;
-                        }
-                        last = __shfl_sync(kFull, last, 0);
-                        if (last) {
-                            __threadfence();
-                            float sum[4] = {0.f, 0.f, 0.f, 0.f};
-                            for (int k = 0; k < a.topk; k++) {
-                                const int rk = a.comb_pos[(int64_t)t * a.topk + k];
-                                if (rk < 0) continue;
-                                const float wk = a.comb_w[(int64_t)t * a.topk + k];
-                                const float4 d = __ldcg(reinterpret_cast<const float4 *>(a.out_rows + (int64_t)rk * e.OC + oc0));
-                                sum[0] += wk * d.x;
-                                sum[1] += wk * d.y;
-                                sum[2] += wk * d.z;
-                                sum[3] += wk * d.w;
-                            }
-                            const uint32_t o0 = (uint32_t)f32_to_bf16_bits(sum[0]) | ((uint32_t)f32_to_bf16_bits(sum[1]) << 16);
-                            const uint32_t o1 = (uint32_t)f32_to_bf16_bits(sum[2]) | ((uint32_t)f32_to_bf16_bits(sum[3]) << 16);
-                            *reinterpret_cast<uint2 *>(a.comb_y + (int64_t)t * e.OC + oc0) = make_uint2(o0, o1);
-                            if (lane == 0) a.comb_counters[(int64_t)t * GH + G] = 0;
-                        }
-                    }
-                }
-            }
-        }
+        if (!PAIR && do_epilogue) group_output<NB>(a, red, e, G, lane, warp, kDecodeWarps);
         __syncthreads();   // red and s_ent are reused by the next segment
         f += a_hi - a_lo;
     }
@@ -842,6 +851,85 @@ static cudaError_t launch_group_pair_act(const GroupGemmArgs &a0, bool pdl, cuda
     return cudaLaunchKernelEx(&cfg, group_pair_act_kernel, a);
 }
 
+// --------------------------------------------------------------------------
+// Rows mode over device entry lists with few, short column groups (MoE FC2 at
+// a few routed pairs: 48 tile rows a group at I = 768): one 16-warp CTA takes
+// whole column groups in turn (gi = blockIdx.x, + gridDim.x, ...), its warps
+// splitting each group's tile rows three or so apiece, and reduces the group in
+// shared memory in fixed warp order: no split-K, and half the rows per warp of
+// one 8-warp CTA per group.  The caller uses it when every group can have its
+// own CTA (measured at MoE T = 1: 30.8 -> 28.5 us; at T = 2, two groups on some
+// CTAs, 40.5 -> 43.6 us).
+// --------------------------------------------------------------------------
+constexpr int kWideWarps = 2 * kDecodeWarps;
+
+template <int KSET>
+__global__ void __launch_bounds__(kWideWarps * 32, 1) group_wide_kernel(const GroupGemmArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    constexpr int FRAG = 8 * 4 * 32;
+    float *red = reinterpret_cast<float *>(smem_raw);   // [16 warps][FRAG]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int A = a.IC / kTile;
+    // entry lists written by an earlier launch than the preceding one: read them,
+    // and request the first code words, before waiting for the preceding kernel
+    const bool hoist = a.entries_ready != 0;
+    if (!hoist) grid_dependency_wait();
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int n_groups = *a.n_entries_dev * a.n_groups_per_entry;
+    const uint32_t hx = a.hash_xor;
+    for (int gi = blockIdx.x; gi < n_groups; gi += gridDim.x) {
+        const GroupEntry e = a.entries[gi / a.n_groups_per_entry];
+        const int G = gi % a.n_groups_per_entry;
+        float acc[8][1][4];
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) acc[j][0][q] = 0.f;
+        if ((KSET & 4) && e.K == 2)
+            group_accumulate<2, 1, kUGlobal, kWideWarps>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2, nullptr, 0, hoist);
+        if ((KSET & 8) && e.K == 3)
+            group_accumulate<3, 1, kUGlobal, kWideWarps>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2, nullptr, 0, hoist);
+        if ((KSET & 16) && e.K == 4)
+            group_accumulate<4, 1, kUGlobal, kWideWarps>(acc, e, a.u, a.IC, G, 0, A, lane, warp, hx, a.pow2, nullptr, 0, hoist);
+        // the outputs and the combine counters are shared with the preceding kernel
+        if (hoist) grid_dependency_wait();
+#pragma unroll
+        for (int j = 0; j < 8; j++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) red[warp * FRAG + (j * 4 + q) * 32 + lane] = acc[j][0][q];
+        __syncthreads();
+        for (int i = threadIdx.x; i < FRAG; i += kWideWarps * 32) {
+            float sum = red[i];
+#pragma unroll
+            for (int wv = 1; wv < kWideWarps; wv++) sum += red[wv * FRAG + i];
+            red[i] = sum;
+        }
+        __syncthreads();
+        group_output<1>(a, red, e, G, lane, warp, kWideWarps);
+        __syncthreads();   // red is reused by the next group
+    }
+}
+
+static cudaError_t launch_group_wide(const GroupGemmArgs &a0, bool pdl, cudaStream_t s) {
+    constexpr size_t smem = sizeof(float) * kWideWarps * 8 * 4 * 32;
+    cudaError_t e = kernel_smem_optin((const void *)group_wide_kernel<28>, smem);
+    if (e != cudaSuccess) return e;
+    GroupGemmArgs a = a0;
+    a.hash_xor = kHashXor;
+    for (int i = 0; i < 17; i++) a.pow2[i] = 1u << i;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)device_info().sm_count);
+    cfg.blockDim = dim3(kWideWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, group_wide_kernel<28>, a);
+}
+
 template <int NB, int KSET, int USRC = kUGlobal, bool PAIR = false>
 static cudaError_t launch_group_t(const GroupGemmArgs &a0, bool pdl, int64_t total_hint, cudaStream_t s) {
     constexpr size_t smem = group_smem_bytes<NB, PAIR>();
@@ -906,6 +994,13 @@ cudaError_t launch_group_gemm(const GroupGemmArgs &a, int nb, bool pdl, cudaStre
             kset |= 1 << a.inline_e[i].K;
         }
         total = groups * (a.IC / kTile);
+    }
+    if (a.wide) {
+        // whole short groups per 16-warp CTA: rows mode over device entry lists, one 8-row block of fp16 rows
+        if (nb != 1 || a.gather || a.pair_act || a.codes || a.mode != kModeRows || !a.entries || !a.n_entries_dev ||
+            a.n_groups_per_entry <= 0)
+            return cudaErrorInvalidValue;
+        return launch_group_wide(a, pdl, s);
     }
     if (a.gather) {
         // grouped MoE with activation rows stored per pair: one 8-row block per entry, any K

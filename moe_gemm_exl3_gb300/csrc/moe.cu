@@ -931,6 +931,9 @@ exl3_status moe_layer(const char *fn, const uint16_t *x, const float *logits, in
         g2.comb_counters = counters + kCombCounterBase;
         // the routing launch, two before, wrote the entry lists and tables; FC1 only h2
         g2.entries_ready = 1;
+        // when every column group can have its own CTA (at most R entries of H/128
+        // groups), whole groups per 16-warp CTA, three or so tile rows a warp
+        g2.wide = (int64_t)R * (H / kHad) <= device_info().sm_count ? 1 : 0;
         if ((e = launch_group_gemm(g2, 1, true, s)) != cudaSuccess) return cuda_fail(e, "moe_grouped: FC2");
         trace("%s T=%d H=%d I=%d E=%d topk=%d rows<=%d gemm=decode (3 launches)", fn, T, H, I, E, topk, R);
         return EXL3_OK;
