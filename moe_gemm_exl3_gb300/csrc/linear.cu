@@ -540,9 +540,9 @@ __global__ void __launch_bounds__(256, DecodeOcc<NB>::value) group_gemm_kernel(c
 }
 
 // --------------------------------------------------------------------------
-// Two dense shards of equal width (a merged gate/up layer) at up to 8 rows,
-// with more column groups per shard than half the SMs and at most as many as
-// the SMs.  With one group per 8-warp CTA, two CTAs share most SMs: where a
+// Two dense shards of equal width (a merged gate/up layer) at up to 16 rows
+// (one or two 8-row blocks; 8-bit codes: one), with more column groups per
+// shard than half the SMs and at most as many as the SMs.  With one group per 8-warp CTA, two CTAs share most SMs: where a
 // cheap (smaller K) and an expensive group meet, the cheap CTA ends early and
 // the other runs on alone at half the warps; other SMs hold two expensive
 // groups, or one group only.  Here one 16-warp CTA per SM takes shard 0's
